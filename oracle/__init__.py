@@ -1,0 +1,174 @@
+"""fp64 CPU oracle for exact attention: TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  The library under test never imports it, and it imports nothing from
+the library.  The arithmetic lives in ``oracle.c`` (plain C, fp64); this module only builds
+that file with gcc, marshals numpy arrays into it and splits work across host threads.
+
+Every function takes arrays shaped ``[B, H, N, d]`` (``[N, d]`` for the ``*_head`` forms),
+upcasts them exactly to float64 and returns float64 arrays.  ``lse`` is the natural-log
+log-sum-exp of the scaled logits, shaped ``[B, H, N]``.
+
+Parity status of each function (which checks pin it) is listed in the tests
+``tests/test_oracle_pins.py``; every function here is pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i, d = ctypes.c_int, ctypes.c_double
+            lib.oracle_attention_fwd_head.argtypes = [i, i, d, i, _dp, _dp, _dp, _dp, _dp, _dp]
+            lib.oracle_attention_bwd_head.argtypes = [i, i, d, i, _dp, _dp, _dp, _dp, _dp, _dp,
+                                                      _dp, _dp, _dp, _dp]
+            lib.oracle_attention_fwd_tiled_head.argtypes = [i, i, d, i, i, i, _dp, _dp, _dp, _dp,
+                                                            _dp]
+            lib.oracle_attention_rows_head.argtypes = [i, i, d, i, _dp, _dp, _dp, _dp, i, _ip,
+                                                       _dp, _dp, _dp, _dp, i, _ip, _dp, _dp, i]
+            lib.oracle_attention_fwd.argtypes = [i, i, i, d, i, _dp, _dp, _dp, _dp, _dp, i]
+            lib.oracle_attention_bwd.argtypes = [i, i, i, d, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                                 _dp, _dp, _dp, i]
+            for f in (lib.oracle_attention_fwd_head, lib.oracle_attention_bwd_head,
+                      lib.oracle_attention_fwd_tiled_head, lib.oracle_attention_rows_head,
+                      lib.oracle_attention_fwd, lib.oracle_attention_bwd):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # a torch tensor: exact upcast on the host
+        import torch
+
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def attention_fwd(q, k, v, scale: float, causal: bool, nthreads: int | None = None):
+    """Algorithm 0 over every head: returns (O [B,H,N,d], lse [B,H,N]) in float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    o = np.empty_like(q)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().oracle_attention_fwd(B * H, N, d, float(scale), int(bool(causal)), _p(q), _p(k),
+                                      _p(v), _p(o), _p(lse), nthreads or default_threads())
+    _check(rc, "fwd")
+    return o, lse
+
+
+def attention_bwd(q, k, v, do, scale: float, causal: bool, nthreads: int | None = None):
+    """Backward over every head: returns dict with dq, dk, dv, o, lse, delta (float64)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, d = q.shape
+    out = {n: np.empty_like(q) for n in ("dq", "dk", "dv", "o")}
+    out["lse"] = np.empty((B, H, N), dtype=np.float64)
+    out["delta"] = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().oracle_attention_bwd(
+        B * H, N, d, float(scale), int(bool(causal)), _p(q), _p(k), _p(v), _p(do), _p(out["dq"]),
+        _p(out["dk"]), _p(out["dv"]), _p(out["o"]), _p(out["lse"]), _p(out["delta"]),
+        nthreads or default_threads())
+    _check(rc, "bwd")
+    return out
+
+
+def attention_fwd_head(q, k, v, scale: float, causal: bool, want_p: bool = False):
+    """Algorithm 0 on one head [N, d]; returns (O, lse) or (O, lse, P)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    N, d = q.shape
+    o = np.empty_like(q)
+    lse = np.empty(N, dtype=np.float64)
+    P = np.empty((N, N), dtype=np.float64) if want_p else None
+    _check(_load().oracle_attention_fwd_head(N, d, float(scale), int(bool(causal)), _p(q), _p(k),
+                                             _p(v), _p(o), _p(lse), _p(P)), "fwd_head")
+    return (o, lse, P) if want_p else (o, lse)
+
+
+def attention_bwd_head(q, k, v, do, scale: float, causal: bool):
+    """Backward on one head [N, d]; returns dict dq, dk, dv, o, lse, delta."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    N, d = q.shape
+    out = {n: np.empty_like(q) for n in ("dq", "dk", "dv", "o")}
+    out["lse"] = np.empty(N, dtype=np.float64)
+    out["delta"] = np.empty(N, dtype=np.float64)
+    _check(_load().oracle_attention_bwd_head(
+        N, d, float(scale), int(bool(causal)), _p(q), _p(k), _p(v), _p(do), _p(out["dq"]),
+        _p(out["dk"]), _p(out["dv"]), _p(out["o"]), _p(out["lse"]), _p(out["delta"])), "bwd_head")
+    return out
+
+
+def attention_fwd_tiled_head(q, k, v, scale: float, causal: bool, Br: int, Bc: int):
+    """Algorithm 1 (K/V-outer tiled online softmax) on one head; returns (O, lse)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    N, d = q.shape
+    o = np.empty_like(q)
+    lse = np.empty(N, dtype=np.float64)
+    _check(_load().oracle_attention_fwd_tiled_head(N, d, float(scale), int(bool(causal)), int(Br),
+                                                   int(Bc), _p(q), _p(k), _p(v), _p(o), _p(lse)),
+           "fwd_tiled_head")
+    return o, lse
+
+
+def attention_rows_head(q, k, v, do, scale: float, causal: bool, qrows, krows,
+                        nthreads: int | None = None):
+    """Sampled rows of one head [N, d] without materialising N x N.
+
+    Returns dict: o, lse, delta, dq for each row in ``qrows``; dk, dv for each row in ``krows``.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    N, d = q.shape
+    qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32).reshape(-1))
+    kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32).reshape(-1))
+    nq, nk = len(qr), len(kr)
+    out = {
+        "o": np.empty((nq, d)), "lse": np.empty(nq), "delta": np.empty(nq), "dq": np.empty((nq, d)),
+        "dk": np.empty((nk, d)), "dv": np.empty((nk, d)),
+    }
+    _check(_load().oracle_attention_rows_head(
+        N, d, float(scale), int(bool(causal)), _p(q), _p(k), _p(v), _p(do), nq,
+        qr.ctypes.data_as(_ip), _p(out["o"]), _p(out["lse"]), _p(out["delta"]), _p(out["dq"]), nk,
+        kr.ctypes.data_as(_ip), _p(out["dk"]), _p(out["dv"]), nthreads or default_threads()),
+        "rows_head")
+    return out
