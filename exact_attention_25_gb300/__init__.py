@@ -1,0 +1,132 @@
+"""GB300-native exact attention (FlashAttention-style forward and backward) for sm_103a.
+
+The computation lives in ``libfa.so`` (hand-written CUDA: TMA, tcgen05/TMEM, warp-specialised
+roles) behind the C ABI of ``include/fa.h``.  This module is the thin Python binding: the
+``fa_*`` functions mirror the C entry points one to one and only marshal torch tensors into
+pointers and sizes; ``forward``/``backward`` additionally allocate the outputs with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import FA_BF16, FA_F32, FaError, check, load
+
+__all__ = [
+    "FA_BF16", "FA_F32", "FaError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes",
+    "fa_device_status", "fa_set_wait_limit_ns", "fa_causal_block_counts", "forward", "backward",
+]
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("tensors must be [B, H, N, d]")
+    return tuple(int(x) for x in q.shape)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_tensors(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None, impl: int = 0) -> None:
+    """C ``fa_fwd`` (``fa_fwd_impl`` when impl != 0): writes o and lse in place."""
+    _check_tensors(q, k, v, o, lse)
+    B, H, N, d = _shape(q)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+            int(bool(causal)), _dtype_code(q))
+    lib = load()
+    if impl:
+        check(lib.fa_fwd_impl(*args, int(impl), _stream(stream)))
+    else:
+        check(lib.fa_fwd(*args, _stream(stream)))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspace,
+           stream=None, impl: int = 0) -> None:
+    """C ``fa_bwd`` (``fa_bwd_impl`` when impl != 0): writes dq, dk, dv in place."""
+    _check_tensors(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, H, N, d = _shape(q)
+    nbytes = workspace.numel() * workspace.element_size()
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _ptr(workspace),
+            nbytes)
+    lib = load()
+    if impl:
+        check(lib.fa_bwd_impl(*args, int(impl), _stream(stream)))
+    else:
+        check(lib.fa_bwd(*args, _stream(stream)))
+
+
+def fa_device_status(stream=None) -> None:
+    """C ``fa_device_status``: synchronises and raises FaError if a device wait timed out."""
+    check(load().fa_device_status(_stream(stream)))
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    load().fa_set_wait_limit_ns(int(ns))
+
+
+def fa_causal_block_counts(q_block: int, Br: int, Bc: int, N: int) -> tuple[int, int]:
+    """C ``fa_causal_block_counts``: (unmasked blocks, masked diagonal blocks)."""
+    nf, nm = ctypes.c_int(), ctypes.c_int()
+    check(load().fa_causal_block_counts(q_block, Br, Bc, N, ctypes.byref(nf), ctypes.byref(nm)))
+    return nf.value, nm.value
+
+
+def forward(q, k, v, scale: float | None = None, causal: bool = False, stream=None,
+            impl: int = 0):
+    """Allocate O ([B,H,N,d], q's dtype) and LSE ([B,H,N] fp32) and run fa_fwd."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, stream, impl)
+    return o, lse
+
+
+def backward(q, k, v, o, do, lse, scale: float | None = None, causal: bool = False,
+             stream=None, impl: int = 0, workspace=None):
+    """Allocate dQ, dK, dV (and the workspace unless given) and run fa_bwd."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    if scale is None:
+        scale = d ** -0.5
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                                device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, workspace, stream, impl)
+    return dq, dk, dv

@@ -1,0 +1,80 @@
+"""ctypes binding of libfa.so.  Argument marshalling only: every step of the computation runs
+in the library's CUDA kernels.  Tensors are torch CUDA tensors (torch supplies device memory
+and streams); shapes are [B, H, N, d], contiguous.  Raises if the library is missing: there
+is no fallback implementation."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_BF16, FA_F32 = 0, 1
+STATUS = {
+    0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED_D", -3: "FA_ERR_MISALIGNED",
+    -4: "FA_ERR_WORKSPACE", -5: "FA_ERR_LAUNCH", -6: "FA_ERR_DEVICE_TIMEOUT",
+    -7: "FA_ERR_TOO_LARGE", -8: "FA_ERR_UNSUPPORTED_DEVICE",
+}
+# Every symbol include/fa.h declares (tests check the library exports all of them).
+EXPORTS = (
+    "fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_fwd_impl", "fa_bwd_impl",
+    "fa_device_status", "fa_set_wait_limit_ns", "fa_status_string", "fa_last_error",
+    "fa_causal_block_counts", "fa_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{STATUS.get(code, code)}: {what}")
+        self.code = code
+
+
+def load(path: str | None = None):
+    """Load libfa.so (built by ``exact_attention_25_gb300.build``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise FileNotFoundError(
+                f"{p} is missing: build it with exact_attention_25_gb300.build.build() "
+                "(there is no fallback implementation)")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_impl.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+        lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_bytes.restype = sz
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.fa_bwd_impl.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp,
+                                    sz, i, vp]
+        lib.fa_device_status.argtypes = [vp]
+        lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_set_wait_limit_ns.restype = None
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_last_error.argtypes = []
+        lib.fa_last_error.restype = ctypes.c_char_p
+        lib.fa_causal_block_counts.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.fa_version.restype = ctypes.c_char_p
+        for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_device_status",
+                   "fa_causal_block_counts"):
+            getattr(lib, fn).restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def check(rc: int) -> None:
+    if rc != 0:
+        raise FaError(rc, load().fa_last_error().decode())
+
+
+def last_error() -> str:
+    return load().fa_last_error().decode()

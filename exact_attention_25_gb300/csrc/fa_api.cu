@@ -1,0 +1,308 @@
+// Host side of the C ABI declared in include/fa.h: argument validation (before any CUDA
+// call), TMA tensor-map construction, kernel dispatch and the device status word.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "fa_common.cuh"
+
+namespace fa {
+cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdParams& p, cudaStream_t st);
+cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_preprocess(int d, int is_f32, const BwdParams& p, cudaStream_t st,
+                                  int num_sms);
+cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
+
+// Device status word written by bounded waits that give up (0 = fine).
+__device__ int g_status_word;
+}  // namespace fa
+
+namespace {
+
+thread_local std::string t_last_error;
+unsigned long long g_wait_limit_ns = 2000000000ull;
+
+int fail(int code, const std::string& what)
+{
+    t_last_error = what;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where)
+{
+    return fail(FA_ERR_LAUNCH, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+    bool ready = false;
+    int major = 0, minor = 0, sms = 0;
+    int* status = nullptr;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(FA_ERR_LAUNCH, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& di = g_dev[dev];
+    if (!di.ready) {
+        if ((e = cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+            (e = cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+            (e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)))
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (di.major != 10 || di.minor != 3)
+            return fail(FA_ERR_UNSUPPORTED_DEVICE,
+                        "this build targets sm_103a (compute capability 10.3) only");
+        void* ptr = nullptr;
+        if ((e = cudaGetSymbolAddress(&ptr, fa::g_status_word)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        di.status = static_cast<int*>(ptr);
+        di.ready = true;
+    }
+    *out = &di;
+    return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder()
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return FA_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled entry point not available");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return FA_OK;
+}
+
+// 3-D view [BH, N, d] of a bf16 tensor; box = 64 columns (one 128-byte swizzle panel) x
+// `rows` rows x 1 head.  Rows beyond N read as zero.
+int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int rows)
+{
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
+    return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, int d, float scale, int causal, int dtype)
+{
+    if (dtype != FA_BF16 && dtype != FA_F32) return fail(FA_ERR_INVALID_ARG, "dtype must be FA_BF16 or FA_F32");
+    if (B < 1 || H < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, H and N must be >= 1");
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED_D, "d must be 64 or 128");
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+        return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    const long long elems = static_cast<long long>(B) * H * N * d;
+    if (elems >= (1LL << 31)) return fail(FA_ERR_TOO_LARGE, "B*H*N*d must be < 2^31");
+    return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, float scale, int causal, int dtype, int impl, void* stream)
+{
+    int rc = check_common(B, H, N, d, scale, causal, dtype);
+    if (rc) return rc;
+    if (impl != 0 && impl != 1) return fail(FA_ERR_INVALID_ARG, "impl must be 0 or 1");
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    fa::FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    cudaError_t e;
+    if (dtype == FA_F32 || impl == 1) {
+        e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st);
+    } else {
+        if ((rc = get_encoder())) return rc;
+        CUtensorMap tq, tk, tv;
+        if ((rc = make_map(&tq, q, p.BH, N, d, 128)) || (rc = make_map(&tk, k, p.BH, N, d, 128)) ||
+            (rc = make_map(&tv, v, p.BH, N, d, 128)))
+            return rc;
+        e = fa::launch_fwd_tc(d, tq, tk, tv, p, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return FA_OK;
+}
+
+int bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+              float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+              int impl, void* stream)
+{
+    int rc = check_common(B, H, N, d, scale, causal, dtype);
+    if (rc) return rc;
+    if (impl != 0 && impl != 1) return fail(FA_ERR_INVALID_ARG, "impl must be 0 or 1");
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+        return fail(FA_ERR_INVALID_ARG, "every tensor pointer must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA_ERR_MISALIGNED, "tensors must be 16-byte aligned (lse 4-byte)");
+    const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    fa::BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.delta = reinterpret_cast<float*>(ws);
+    p.lse2 = reinterpret_cast<float*>(ws + align256(rows * 4));
+    p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    const int is_f32 = dtype == FA_F32;
+    cudaError_t e = fa::launch_bwd_preprocess(d, is_f32, p, st, di->sms);
+    if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+    if (is_f32 || impl == 1) {
+        e = fa::launch_bwd_simt(d, is_f32, p, st);
+    } else {
+        if ((rc = get_encoder())) return rc;
+        // maps: q, k, v, dout (all 128-row boxes)
+        CUtensorMap maps[4];
+        const void* srcs[4] = {q, k, v, dout};
+        for (int i = 0; i < 4; ++i)
+            if ((rc = make_map(&maps[i], srcs[i], p.BH, N, d, 128))) return rc;
+        e = fa::launch_bwd_tc(d, maps, p, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, int dtype, void* stream)
+{
+    return fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, 0, stream);
+}
+
+int fa_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, float scale, int causal, int dtype, int impl, void* stream)
+{
+    return fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, impl, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d)
+{
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    return 2 * align256(rows * 4) + 256;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+           void* stream)
+{
+    return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                     workspace, workspace_bytes, 0, stream);
+}
+
+int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                int impl, void* stream)
+{
+    return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                     workspace, workspace_bytes, impl, stream);
+}
+
+int fa_device_status(void* stream)
+{
+    DeviceInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int word = 0;
+    if ((e = cudaMemcpy(&word, di->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "reading the status word");
+    if (word == 0) return FA_OK;
+    const int zero = 0;
+    if ((e = cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(e, "clearing the status word");
+    return fail(FA_ERR_DEVICE_TIMEOUT, "bounded device wait expired at site " + std::to_string(word));
+}
+
+void fa_set_wait_limit_ns(unsigned long long ns)
+{
+    g_wait_limit_ns = ns < 1000000ull ? 1000000ull : ns;
+}
+
+const char* fa_status_string(int code)
+{
+    switch (code) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED_D: return "FA_ERR_UNSUPPORTED_D";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+        case FA_ERR_TOO_LARGE: return "FA_ERR_TOO_LARGE";
+        case FA_ERR_UNSUPPORTED_DEVICE: return "FA_ERR_UNSUPPORTED_DEVICE";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+const char* fa_last_error(void) { return t_last_error.c_str(); }
+
+int fa_causal_block_counts(int q_block, int Br, int Bc, int N, int* n_full, int* n_masked)
+{
+    if (q_block < 0 || Br < 1 || Bc < 1 || N < 1 || !n_full || !n_masked ||
+        static_cast<long long>(q_block) * Br >= N)
+        return fail(FA_ERR_INVALID_ARG, "bad block arguments");
+    const int q0 = q_block * Br, q1 = (q0 + Br < N) ? q0 + Br : N;
+    int nf = 0, nm = 0;
+    for (int k0 = 0; k0 < N; k0 += Bc) {
+        const int k1 = (k0 + Bc < N) ? k0 + Bc : N;
+        const int c = fa::causal_tile_class(q0, q1, k0, k1);
+        nf += c == fa::kTileFull;
+        nm += c == fa::kTileMasked;
+    }
+    *n_full = nf;
+    *n_masked = nm;
+    return FA_OK;
+}
+
+const char* fa_version(void) { return "fa-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,417 @@
+// Forward attention on sm_103a tensor cores: TMA-staged Q/K/V tiles, tcgen05.mma into
+// Tensor Memory, warp-specialised producer / MMA / softmax roles, online softmax in fp32
+// with exp2, un-scaled accumulation and one final 1/l, causal two-stage split, ragged tails.
+//
+// One CTA owns NT = 2 query tiles of 128 rows of one head (the FlashAttention-2 Q-outer
+// loop order, "FA2·FA3" section of "Flash Attention IO-awareness principle") and streams
+// the key/value blocks of 128 keys through a shared-memory ring.  Roles (12 warps):
+//   warps 0-3   softmax of query tile 0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax of query tile 1
+//   warp  8     TMA producer (one lane)
+//   warp  9     TMEM allocator + MMA issuer (one lane)
+//   warps 10-11 idle (kept so the softmax warpgroups sit on warpgroup boundaries)
+// TMEM columns: S_t at [128t, 128t+128) (fp32), P_t (bf16 pairs) aliased on the upper half
+// of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised).
+#include "fa_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct FwdCfg {
+    static constexpr int BM = 128;                 // query rows per tile
+    static constexpr int NT = 2;                   // query tiles per CTA
+    static constexpr int BN = 128;                 // keys per block
+    static constexpr int PANELS = D / 64;          // 128-byte swizzle panels per row
+    static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
+    static constexpr int STAGES = (D == 128) ? 2 : 4;
+    static constexpr int SMEM_Q = NT * TILE_BYTES;
+    static constexpr int SMEM_K = STAGES * TILE_BYTES;
+    static constexpr int SMEM_V = STAGES * TILE_BYTES;
+    static constexpr int SMEM_BYTES = SMEM_Q + SMEM_K + SMEM_V + 1024;  // + alignment slack
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P stays below 2^8
+};
+
+// All 32 lanes wait; the warp proceeds only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Watchdog& wd,
+                                          int site)
+{
+    const bool ok = mbar_wait(bar, parity, wd, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
+{
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sK = sQ + C::SMEM_Q;
+    uint8_t* sV = sK + C::SMEM_K;
+
+    __shared__ __align__(8) uint64_t bar_q;
+    __shared__ __align__(8) uint64_t bar_kfull[C::STAGES];
+    __shared__ __align__(8) uint64_t bar_vfull[C::STAGES];
+    __shared__ __align__(8) uint64_t bar_kvempty[C::STAGES];
+    __shared__ __align__(8) uint64_t bar_sfull[C::NT];
+    __shared__ __align__(8) uint64_t bar_pfull[C::NT];
+    __shared__ __align__(8) uint64_t bar_ofinal[C::NT];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = p.N;
+    const int bh = blockIdx.x;
+    const int n_qtiles = (N + C::BM - 1) / C::BM;
+    const int n_kblocks = (N + C::BN - 1) / C::BN;
+    // heaviest causal pairs first: blockIdx.y = 0 takes the last pair of every head
+    const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    const int qt0 = pair * C::NT;
+    const int nt = min(C::NT, n_qtiles - qt0);
+
+    // Key blocks visited by each query tile (a prefix 0..J_t-1 under the causal mask).
+    int J[C::NT];
+#pragma unroll
+    for (int t = 0; t < C::NT; ++t) {
+        J[t] = 0;
+        if (t < nt) {
+            if (!p.causal) {
+                J[t] = n_kblocks;
+            } else {
+                const int q0 = (qt0 + t) * C::BM, q1 = min(N, q0 + C::BM);
+                int jt = 0;
+                while (jt < n_kblocks &&
+                       causal_tile_class(q0, q1, jt * C::BN, min(N, (jt + 1) * C::BN)) != kTileSkip)
+                    ++jt;
+                J[t] = jt;
+            }
+        }
+    }
+    const int Jmax = max(J[0], J[1]);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&bar_kfull[s], 1);
+            mbar_init(&bar_vfull[s], 1);
+            mbar_init(&bar_kvempty[s], 1);
+        }
+        for (int t = 0; t < C::NT; ++t) {
+            mbar_init(&bar_sfull[t], 1);
+            mbar_init(&bar_pfull[t], C::BM);
+            mbar_init(&bar_ofinal[t], 1);
+        }
+        mbar_init(&bar_drain, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_slot;
+    const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+
+    if (warp == 8) {
+        // ------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_q, nt * C::TILE_BYTES);
+            for (int t = 0; t < nt; ++t)
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn,
+                                (qt0 + t) * C::BM, bh);
+            int issued = 0;
+            for (int j = 0; j < Jmax; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                if (!mbar_wait(&bar_kvempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
+                mbar_arrive_expect_tx(&bar_kfull[s], C::TILE_BYTES);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
+                                64 * pn, j * C::BN, bh);
+                mbar_arrive_expect_tx(&bar_vfull[s], C::TILE_BYTES);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bar_vfull[s],
+                                64 * pn, j * C::BN, bh);
+                issued = j + 1;
+            }
+            // Let no copy land after the CTA exits: wait (bounded, ignoring the abort flag)
+            // for the last loads this thread issued.
+            volatile int no_abort = 0;
+            const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
+            mbar_wait(&bar_q, 0, wd_drain, kSiteFwdDrain);
+            for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                mbar_wait(&bar_kfull[s], ph, wd_drain, kSiteFwdDrain);
+                mbar_wait(&bar_vfull[s], ph, wd_drain, kSiteFwdDrain);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, C::BN, 0, 0);  // S = Q K^T
+            constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);     // O += P V
+            const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+
+            auto issue_s = [&](int t, int s) {
+                const uint32_t d_tmem = tbase + 128u * t;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
+                    const uint64_t a = sdesc_sw128(sQa + t * C::TILE_BYTES + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(sKa + s * C::TILE_BYTES + off, 16, 1024);
+                    mma_ss(d_tmem, a, b, kIdS, ks > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool accumulate) {
+                const uint32_t d_tmem = tbase + 256u + static_cast<uint32_t>(t * D);
+                const uint32_t p_tmem = tbase + 128u * t + 64u;
+#pragma unroll
+                for (int ks = 0; ks < C::BN / 16; ++ks) {
+                    const uint64_t b =
+                        sdesc_sw128(sVa + s * C::TILE_BYTES + ks * 2048, C::PANEL_BYTES, 1024);
+                    mma_ts(d_tmem, p_tmem + 8u * ks, b, kIdPV, (accumulate || ks > 0) ? 1u : 0u);
+                }
+            };
+
+            bool ok = mbar_wait(&bar_q, 0, wd, kSiteFwdMmaQ);
+            ok = ok && mbar_wait(&bar_kfull[0], 0, wd, kSiteFwdMmaK);
+            int committed = 0;  // key blocks whose stage release was committed
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < nt; ++t) {
+                    issue_s(t, 0);
+                    mma_commit(&bar_sfull[t]);
+                }
+            }
+            for (int j = 0; ok && j < Jmax; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1;
+                const int s1 = (j + 1) % C::STAGES;
+                const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+                if (!mbar_wait(&bar_vfull[s], ph, wd, kSiteFwdMmaV)) { ok = false; break; }
+                bool k_next = false;
+                for (int t = 0; t < nt; ++t) {
+                    if (j >= J[t]) continue;
+                    if (!mbar_wait(&bar_pfull[t], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, s, j > 0);
+                    if (j + 1 == J[t]) {
+                        mma_commit(&bar_ofinal[t]);
+                    } else {
+                        if (!k_next) {
+                            if (!mbar_wait(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
+                            tc_fence_after();
+                            k_next = true;
+                        }
+                        issue_s(t, s1);
+                        mma_commit(&bar_sfull[t]);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bar_kvempty[s]);
+                committed = j + 1;
+            }
+            // Wait until every commit this thread issued has arrived, so no arrive lands on
+            // shared memory after the CTA exits (bounded; ignores the abort flag).
+            volatile int no_abort = 0;
+            const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
+            mma_commit(&bar_drain);
+            mbar_wait(&bar_drain, 0, wd_drain, kSiteFwdDrain);
+            for (int j = max(0, committed - C::STAGES); j < committed; ++j)
+                mbar_wait(&bar_kvempty[j % C::STAGES], (j / C::STAGES) & 1, wd_drain, kSiteFwdDrain);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------- softmax
+        const int t = warp >> 2;
+        const int r = threadIdx.x & 127;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_base + 128u * t;
+        const uint32_t tP = tS + 64u;
+        const uint32_t tO = tbase + lane_base + 256u + static_cast<uint32_t>(t * D);
+        const int qt = qt0 + t;
+        const int qrow = qt * C::BM + r;
+        // Softmax runs on x = S * c with c = scale*log2(e) (exp2 form).  For c <= 0 the
+        // scores are pre-multiplied so that masked entries remain -inf after scaling.
+        const float c2 = p.scale_log2;
+        const bool prescale = !(c2 > 0.0f);
+        const float cf = prescale ? 1.0f : c2;
+        float m = -INFINITY;  // running max of x (possibly stale by < threshold)
+        float l = 0.0f;       // running sum of exp2(x - m) (fp32, before bf16 rounding)
+        bool ok = t < nt;
+        for (int j = 0; ok && j < J[t]; ++j) {
+            if (!warp_wait(&bar_sfull[t], j & 1, wd, kSiteFwdSoftmaxS)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld32(tS + 0, sr);
+            tmem_ld32(tS + 32, sr + 32);
+            tmem_ld32(tS + 64, sr + 64);
+            tmem_ld32(tS + 96, sr + 96);
+            tmem_wait_ld();
+            reg_fence32(sr);
+            reg_fence32(sr + 32);
+            reg_fence32(sr + 64);
+            reg_fence32(sr + 96);
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+            if (prescale) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) x[c] *= c2;
+            }
+            // Element-wise mask only on the diagonal block and on the ragged last block.
+            const bool diag = p.causal && j == qt;
+            const bool tail = (j == n_kblocks - 1) && (N % C::BN) != 0;
+            if (diag || tail) {
+                int lim = N - 1 - j * C::BN;  // last valid key column in this block
+                if (diag) lim = min(lim, qrow - j * C::BN);
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > lim) x[c] = -INFINITY;
+            }
+            float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, x[c]);
+                mx1 = fmaxf(mx1, x[c + 1]);
+                mx2 = fmaxf(mx2, x[c + 2]);
+                mx3 = fmaxf(mx3, x[c + 3]);
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cf;
+            // Rescale only when the max grew by more than the threshold: l and O then keep
+            // sharing the same (stale) reference m, so the result stays exact.
+            float alpha = 1.0f;
+            const bool need = mt > m + C::RESCALE_THRESHOLD;
+            if (need) {
+                alpha = ex2(m - mt);  // m = -inf on the first block gives 0
+                m = mt;
+                l *= alpha;
+            }
+            const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+            float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const float p0 = ex2(fmaf(x[cb * 32 + c + 0], cf, neg_m));
+                    const float p1 = ex2(fmaf(x[cb * 32 + c + 1], cf, neg_m));
+                    const float p2 = ex2(fmaf(x[cb * 32 + c + 2], cf, neg_m));
+                    const float p3 = ex2(fmaf(x[cb * 32 + c + 3], cf, neg_m));
+                    ls0 += p0;
+                    ls1 += p1;
+                    ls2 += p2;
+                    ls3 += p3;
+                    pk[c / 2] = pack_bf16x2(p0, p1);
+                    pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+                }
+                tmem_st16(tP + 16u * cb, pk);
+            }
+            l += (ls0 + ls1) + (ls2 + ls3);
+            // O still holds the sum up to block j-1 (the commit that signalled S for block j
+            // also covers the P V product of block j-1).
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32u * ch, o);
+                    tmem_wait_ld();
+                    reg_fence32(o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st32(tO + 32u * ch, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar_pfull[t]);
+        }
+        // ------------------------------------------------------------- epilogue
+        if (ok && J[t] > 0) {
+            if (warp_wait(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
+                tc_fence_after();
+                const float inv_l = 1.0f / l;
+                __nv_bfloat16* orow =
+                    static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32u * ch, o);
+                    tmem_wait_ld();
+                    reg_fence32(o);
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        packed[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                                __uint_as_float(o[2 * c + 1]) * inv_l);
+                    if (qrow < N) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                                packed[4 * c + 3]);
+                    }
+                }
+                if (qrow < N && p.lse != nullptr)
+                    p.lse[static_cast<size_t>(bh) * N + qrow] = (m + __log2f(l)) * kLn2;
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
+{
+    using C = FwdCfg<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const int n_qtiles = (p.N + C::BM - 1) / C::BM;
+    const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
+    dim3 grid(p.BH, n_pairs);
+    fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
+{
+    if (d == 64) return launch_fwd_tc_impl<64>(tq, tk, tv, p, st);
+    return launch_fwd_tc_impl<128>(tq, tk, tv, p, st);
+}
+
+}  // namespace fa

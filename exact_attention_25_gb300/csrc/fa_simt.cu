@@ -1,0 +1,403 @@
+// Portable SIMT kernels (CUDA cores, fp32 math):
+//   - forward with the tiled online softmax (the fp32 path; also a cross-check for bf16),
+//   - backward preprocess Delta_i = rowsum(dO_i o O_i) and the base-2 LSE (used by every
+//     backward path),
+//   - backward as the two loops of "Backward 구현" in "Triton 06: Flash Attention v2":
+//     a dK/dV kernel (outer loop over key rows, inner over query blocks) and a dQ kernel
+//     (outer loop over query rows, inner over key blocks).  No atomics: deterministic.
+// One warp owns 4 rows; a CTA of 4 warps owns 16 rows and stages 32-row tiles of the other
+// operands in shared memory.
+#include "fa_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace fa {
+
+constexpr int kSimtWarps = 4;
+constexpr int kSimtRowsPerWarp = 4;
+constexpr int kSimtRows = kSimtWarps * kSimtRowsPerWarp;  // rows owned by one CTA
+constexpr int kSimtTile = 32;                              // rows of a staged tile
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p)
+{
+    return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void st_elem(T* p, float v);
+template <>
+__device__ __forceinline__ void st_elem<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void st_elem<__nv_bfloat16>(__nv_bfloat16* p, float v)
+{
+    *p = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Stage rows [row0, row0+rows) of one head into shared memory as fp32 with row stride ld;
+// rows at or beyond N are zero.
+template <typename T, int D>
+__device__ __forceinline__ void stage_rows(float* dst, int ld, const T* head, int row0, int rows,
+                                           int N)
+{
+    for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
+        const int r = e / D, c = e % D;
+        const int g = row0 + r;
+        dst[r * ld + c] = (g < N) ? ld_elem(head + static_cast<size_t>(g) * D + c) : 0.0f;
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// Forward: O and LSE for 16 query rows per CTA.
+// ----------------------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
+{
+    constexpr int DL = D / 32;  // output columns per lane
+    extern __shared__ float sm[];
+    float* Qs = sm;                          // [16][D]
+    float* Ks = Qs + kSimtRows * D;          // [32][D+1]
+    float* Vs = Ks + kSimtTile * (D + 1);    // [32][D]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.N, bh = blockIdx.y;
+    const int row_base = blockIdx.x * kSimtRows;
+    const size_t hoff = static_cast<size_t>(bh) * N * D;
+    const T* q = static_cast<const T*>(p.q) + hoff;
+    const T* k = static_cast<const T*>(p.k) + hoff;
+    const T* v = static_cast<const T*>(p.v) + hoff;
+    stage_rows<T, D>(Qs, D, q, row_base, kSimtRows, N);
+
+    const float c2 = p.scale_log2;
+    float m[kSimtRowsPerWarp], l[kSimtRowsPerWarp], o[kSimtRowsPerWarp][DL];
+#pragma unroll
+    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+        m[rr] = -INFINITY;
+        l[rr] = 0.0f;
+#pragma unroll
+        for (int t = 0; t < DL; ++t) o[rr][t] = 0.0f;
+    }
+    const int last_row = min(N - 1, row_base + kSimtRows - 1);
+    const int n_tiles = p.causal ? (last_row / kSimtTile + 1) : (N + kSimtTile - 1) / kSimtTile;
+    for (int kt = 0; kt < n_tiles; ++kt) {
+        __syncthreads();
+        stage_rows<T, D>(Ks, D + 1, k, kt * kSimtTile, kSimtTile, N);
+        stage_rows<T, D>(Vs, D, v, kt * kSimtTile, kSimtTile, N);
+        __syncthreads();
+        const int key = kt * kSimtTile + lane;
+#pragma unroll
+        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+            const int lr = warp * kSimtRowsPerWarp + rr;
+            const int row = row_base + lr;
+            float s = 0.0f;
+#pragma unroll 8
+            for (int c = 0; c < D; ++c) s = fmaf(Qs[lr * D + c], Ks[lane * (D + 1) + c], s);
+            const bool valid = key < N && (!p.causal || key <= row);
+            const float x = valid ? s * c2 : -INFINITY;
+            const float mnew = fmaxf(m[rr], warp_max(x));
+            if (mnew == -INFINITY) continue;  // nothing visible yet (uniform across the warp)
+            const float alpha = ex2(m[rr] - mnew);
+            const float pr = ex2(x - mnew);
+            l[rr] = l[rr] * alpha + warp_sum(pr);
+            m[rr] = mnew;
+#pragma unroll
+            for (int t = 0; t < DL; ++t) o[rr][t] *= alpha;
+#pragma unroll 4
+            for (int c = 0; c < kSimtTile; ++c) {
+                const float pc = __shfl_sync(0xffffffffu, pr, c);
+#pragma unroll
+                for (int t = 0; t < DL; ++t) o[rr][t] = fmaf(pc, Vs[c * D + lane + 32 * t], o[rr][t]);
+            }
+        }
+    }
+    T* out = static_cast<T*>(p.o) + hoff;
+#pragma unroll
+    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+        const int row = row_base + warp * kSimtRowsPerWarp + rr;
+        if (row >= N) continue;
+        const float inv = 1.0f / l[rr];
+#pragma unroll
+        for (int t = 0; t < DL; ++t)
+            st_elem(out + static_cast<size_t>(row) * D + lane + 32 * t, o[rr][t] * inv);
+        if (lane == 0 && p.lse) p.lse[static_cast<size_t>(bh) * N + row] = (m[rr] + __log2f(l[rr])) * kLn2;
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// Backward preprocess: Delta_i = sum_c dO_ic O_ic (fp32 accumulation) and lse2_i = lse_i *
+// log2(e).  D/8 threads per row, 16-byte loads for bf16 (D/4 threads, 16 B, for fp32).
+// ----------------------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams p)
+{
+    constexpr int EPV = 16 / sizeof(T);  // elements per 16-byte vector
+    constexpr int TPR = D / EPV;         // threads per row (8, 16 or 32)
+    constexpr int RPW = 32 / TPR;        // rows per warp and iteration
+    const size_t rows = static_cast<size_t>(p.BH) * p.N;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % TPR;
+    const size_t warps_total = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
+    const size_t gw = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    // The loop bound is uniform across the warp, so the shuffles below see all 32 lanes.
+    for (size_t base = gw * RPW; base < rows; base += warps_total * RPW) {
+        const size_t row = base + lane / TPR;
+        const bool valid = row < rows;
+        float acc = 0.0f;
+        if (valid) {
+            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + row * D)[sub];
+            const uint4 b =
+                reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + row * D)[sub];
+            const T* ea = reinterpret_cast<const T*>(&a);
+            const T* eb = reinterpret_cast<const T*>(&b);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc = fmaf(ld_elem(ea + e), ld_elem(eb + e), acc);
+        }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+        if (valid && sub == 0) {
+            p.delta[row] = acc;
+            p.lse2[row] = p.lse[row] * kLog2e;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// Backward dQ (outer loop over query rows, inner over key tiles).
+// ----------------------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) fa_bwd_dq_simt_kernel(const BwdParams p)
+{
+    constexpr int DL = D / 32;
+    extern __shared__ float sm[];
+    float* Qs = sm;                          // [16][D]
+    float* Gs = Qs + kSimtRows * D;          // dO rows [16][D]
+    float* Ks = Gs + kSimtRows * D;          // [32][D+1]
+    float* Vs = Ks + kSimtTile * (D + 1);    // [32][D+1]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.N, bh = blockIdx.y;
+    const int row_base = blockIdx.x * kSimtRows;
+    const size_t hoff = static_cast<size_t>(bh) * N * D;
+    const T* q = static_cast<const T*>(p.q) + hoff;
+    const T* k = static_cast<const T*>(p.k) + hoff;
+    const T* v = static_cast<const T*>(p.v) + hoff;
+    const T* g = static_cast<const T*>(p.dout) + hoff;
+    stage_rows<T, D>(Qs, D, q, row_base, kSimtRows, N);
+    stage_rows<T, D>(Gs, D, g, row_base, kSimtRows, N);
+    float L2[kSimtRowsPerWarp], Dl[kSimtRowsPerWarp], acc[kSimtRowsPerWarp][DL];
+#pragma unroll
+    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+        const int row = row_base + warp * kSimtRowsPerWarp + rr;
+        const size_t ri = static_cast<size_t>(bh) * N + min(row, N - 1);
+        L2[rr] = p.lse2[ri];
+        Dl[rr] = p.delta[ri];
+#pragma unroll
+        for (int t = 0; t < DL; ++t) acc[rr][t] = 0.0f;
+    }
+    const float c2 = p.scale_log2;
+    const int last_row = min(N - 1, row_base + kSimtRows - 1);
+    const int n_tiles = p.causal ? (last_row / kSimtTile + 1) : (N + kSimtTile - 1) / kSimtTile;
+    for (int kt = 0; kt < n_tiles; ++kt) {
+        __syncthreads();
+        stage_rows<T, D>(Ks, D + 1, k, kt * kSimtTile, kSimtTile, N);
+        stage_rows<T, D>(Vs, D + 1, v, kt * kSimtTile, kSimtTile, N);
+        __syncthreads();
+        const int key = kt * kSimtTile + lane;
+#pragma unroll
+        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+            const int lr = warp * kSimtRowsPerWarp + rr;
+            const int row = row_base + lr;
+            float s = 0.0f, dp = 0.0f;
+#pragma unroll 8
+            for (int c = 0; c < D; ++c) {
+                s = fmaf(Qs[lr * D + c], Ks[lane * (D + 1) + c], s);
+                dp = fmaf(Gs[lr * D + c], Vs[lane * (D + 1) + c], dp);
+            }
+            const bool valid = key < N && row < N && (!p.causal || key <= row);
+            const float pr = valid ? ex2(s * c2 - L2[rr]) : 0.0f;
+            const float ds = pr * (dp - Dl[rr]);
+#pragma unroll 4
+            for (int c = 0; c < kSimtTile; ++c) {
+                const float dc = __shfl_sync(0xffffffffu, ds, c);
+#pragma unroll
+                for (int t = 0; t < DL; ++t) acc[rr][t] = fmaf(dc, Ks[c * (D + 1) + lane + 32 * t], acc[rr][t]);
+            }
+        }
+    }
+    T* dq = static_cast<T*>(p.dq) + hoff;
+#pragma unroll
+    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+        const int row = row_base + warp * kSimtRowsPerWarp + rr;
+        if (row >= N) continue;
+#pragma unroll
+        for (int t = 0; t < DL; ++t)
+            st_elem(dq + static_cast<size_t>(row) * D + lane + 32 * t, acc[rr][t] * p.scale);
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// Backward dK, dV (outer loop over key rows, inner over query tiles).
+// ----------------------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) fa_bwd_dkv_simt_kernel(const BwdParams p)
+{
+    constexpr int DL = D / 32;
+    extern __shared__ float sm[];
+    float* Kw = sm;                          // own key rows [16][D]
+    float* Vw = Kw + kSimtRows * D;          // own value rows [16][D]
+    float* Qs = Vw + kSimtRows * D;          // [32][D+1]
+    float* Gs = Qs + kSimtTile * (D + 1);    // dO tile [32][D+1]
+    float* Ls = Gs + kSimtTile * (D + 1);    // lse2 of the tile [32]
+    float* Ds = Ls + kSimtTile;              // Delta of the tile [32]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.N, bh = blockIdx.y;
+    const int key_base = blockIdx.x * kSimtRows;
+    const size_t hoff = static_cast<size_t>(bh) * N * D;
+    const T* q = static_cast<const T*>(p.q) + hoff;
+    const T* k = static_cast<const T*>(p.k) + hoff;
+    const T* v = static_cast<const T*>(p.v) + hoff;
+    const T* g = static_cast<const T*>(p.dout) + hoff;
+    stage_rows<T, D>(Kw, D, k, key_base, kSimtRows, N);
+    stage_rows<T, D>(Vw, D, v, key_base, kSimtRows, N);
+    float dk[kSimtRowsPerWarp][DL], dv[kSimtRowsPerWarp][DL];
+#pragma unroll
+    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr)
+#pragma unroll
+        for (int t = 0; t < DL; ++t) dk[rr][t] = dv[rr][t] = 0.0f;
+    const float c2 = p.scale_log2;
+    const int first_tile = p.causal ? key_base / kSimtTile : 0;
+    const int n_tiles = (N + kSimtTile - 1) / kSimtTile;
+    for (int it = first_tile; it < n_tiles; ++it) {
+        __syncthreads();
+        stage_rows<T, D>(Qs, D + 1, q, it * kSimtTile, kSimtTile, N);
+        stage_rows<T, D>(Gs, D + 1, g, it * kSimtTile, kSimtTile, N);
+        if (threadIdx.x < kSimtTile) {
+            const int i = it * kSimtTile + threadIdx.x;
+            Ls[threadIdx.x] = (i < N) ? p.lse2[static_cast<size_t>(bh) * N + i] : INFINITY;
+            Ds[threadIdx.x] = (i < N) ? p.delta[static_cast<size_t>(bh) * N + i] : 0.0f;
+        }
+        __syncthreads();
+        const int qi = it * kSimtTile + lane;
+#pragma unroll
+        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+            const int lk = warp * kSimtRowsPerWarp + rr;
+            const int key = key_base + lk;
+            float s = 0.0f, dp = 0.0f;
+#pragma unroll 8
+            for (int c = 0; c < D; ++c) {
+                s = fmaf(Qs[lane * (D + 1) + c], Kw[lk * D + c], s);
+                dp = fmaf(Gs[lane * (D + 1) + c], Vw[lk * D + c], dp);
+            }
+            const bool valid = qi < N && key < N && (!p.causal || key <= qi);
+            const float pr = valid ? ex2(s * c2 - Ls[lane]) : 0.0f;
+            const float ds = pr * (dp - Ds[lane]);
+#pragma unroll 4
+            for (int c = 0; c < kSimtTile; ++c) {
+                const float pc = __shfl_sync(0xffffffffu, pr, c);
+                const float dc = __shfl_sync(0xffffffffu, ds, c);
+#pragma unroll
+                for (int t = 0; t < DL; ++t) {
+                    dv[rr][t] = fmaf(pc, Gs[c * (D + 1) + lane + 32 * t], dv[rr][t]);
+                    dk[rr][t] = fmaf(dc, Qs[c * (D + 1) + lane + 32 * t], dk[rr][t]);
+                }
+            }
+        }
+    }
+    T* dK = static_cast<T*>(p.dk) + hoff;
+    T* dV = static_cast<T*>(p.dv) + hoff;
+#pragma unroll
+    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+        const int key = key_base + warp * kSimtRowsPerWarp + rr;
+        if (key >= N) continue;
+#pragma unroll
+        for (int t = 0; t < DL; ++t) {
+            st_elem(dK + static_cast<size_t>(key) * D + lane + 32 * t, dk[rr][t] * p.scale);
+            st_elem(dV + static_cast<size_t>(key) * D + lane + 32 * t, dv[rr][t]);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// Launchers.
+// ----------------------------------------------------------------------------------------
+template <typename K>
+static cudaError_t set_smem(K kernel, int bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <typename T, int D>
+static cudaError_t fwd_simt(const FwdParams& p, cudaStream_t st)
+{
+    const int smem = (kSimtRows * D + kSimtTile * (D + 1) + kSimtTile * D) * 4;
+    cudaError_t e = set_smem(fa_fwd_simt_kernel<T, D>, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + kSimtRows - 1) / kSimtRows, p.BH);
+    fa_fwd_simt_kernel<T, D><<<grid, 128, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t st)
+{
+    if (is_f32) return d == 64 ? fwd_simt<float, 64>(p, st) : fwd_simt<float, 128>(p, st);
+    return d == 64 ? fwd_simt<__nv_bfloat16, 64>(p, st) : fwd_simt<__nv_bfloat16, 128>(p, st);
+}
+
+template <typename T, int D>
+static cudaError_t bwd_pre(const BwdParams& p, cudaStream_t st, int num_sms)
+{
+    constexpr int TPR = D / (16 / sizeof(T));
+    const long rows = static_cast<long>(p.BH) * p.N;
+    const int rows_per_block = 256 / TPR;
+    long blocks = (rows + rows_per_block - 1) / rows_per_block;
+    const long cap = static_cast<long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    fa_bwd_preprocess_kernel<T, D><<<static_cast<int>(blocks), 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_preprocess(int d, int is_f32, const BwdParams& p, cudaStream_t st, int num_sms)
+{
+    if (is_f32) return d == 64 ? bwd_pre<float, 64>(p, st, num_sms) : bwd_pre<float, 128>(p, st, num_sms);
+    return d == 64 ? bwd_pre<__nv_bfloat16, 64>(p, st, num_sms)
+                   : bwd_pre<__nv_bfloat16, 128>(p, st, num_sms);
+}
+
+template <typename T, int D>
+static cudaError_t bwd_simt(const BwdParams& p, cudaStream_t st)
+{
+    const int smem_dq = (2 * kSimtRows * D + 2 * kSimtTile * (D + 1)) * 4;
+    const int smem_dkv = (2 * kSimtRows * D + 2 * kSimtTile * (D + 1) + 2 * kSimtTile) * 4;
+    cudaError_t e = set_smem(fa_bwd_dq_simt_kernel<T, D>, smem_dq);
+    if (e != cudaSuccess) return e;
+    e = set_smem(fa_bwd_dkv_simt_kernel<T, D>, smem_dkv);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + kSimtRows - 1) / kSimtRows, p.BH);
+    fa_bwd_dkv_simt_kernel<T, D><<<grid, 128, smem_dkv, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    fa_bwd_dq_simt_kernel<T, D><<<grid, 128, smem_dq, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st)
+{
+    if (is_f32) return d == 64 ? bwd_simt<float, 64>(p, st) : bwd_simt<float, 128>(p, st);
+    return d == 64 ? bwd_simt<__nv_bfloat16, 64>(p, st) : bwd_simt<__nv_bfloat16, 128>(p, st);
+}
+
+}  // namespace fa

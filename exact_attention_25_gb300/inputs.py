@@ -1,0 +1,108 @@
+"""Seeded synthetic inputs and the named workloads.  Random numbers and shapes only: this
+module holds none of the attention arithmetic, so both the library's tests/benchmark and the
+oracle can draw their inputs from it.
+
+Recipe (every workload): a CPU ``torch.Generator`` seeded with ``seed`` draws float32
+standard-normal tensors shaped [B, H, N, d] in the order Q, K, V, then (if the workload asks
+for it) the index set of "hot" query rows, then dO, then the sampled (head, row) pairs.
+Multiplicative factors are applied in float32 before the cast to the workload dtype
+(round-to-nearest-even for bfloat16).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str            # "bf16" or "fp32"
+    causal: bool
+    fwd: bool = True
+    bwd: bool = False
+    in_scale: float = 1.0         # multiplies Q, K, V
+    hot_rows_frac: float = 0.0    # fraction of query rows multiplied by hot_rows_mult
+    hot_rows_mult: float = 1.0
+    n_samples: int = 0            # (head, query-row) samples for oracle checks at full size
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def fwd_flops(self) -> float:
+        """4 B H N^2 d, halved under the causal mask."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f * 0.5 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """2.5 x the forward count."""
+        return 2.5 * self.fwd_flops()
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("fp32_b1h1_n512_d64", 1, 1, 512, 64, "fp32", False),
+        Workload("bf16_b4h16_n4096_d64_hotrows", 4, 16, 4096, 64, "bf16", False,
+                 hot_rows_frac=0.01, hot_rows_mult=10.0),
+        Workload("bf16_b2h32_n8192_d128_causal", 2, 32, 8192, 128, "bf16", True, in_scale=0.5),
+        Workload("bf16_b4h16_n4096_d128_causal_bwd", 4, 16, 4096, 128, "bf16", True, fwd=True,
+                 bwd=True),
+        Workload("bf16_b1h32_n32000_d128_causal_fwdbwd", 1, 32, 32000, 128, "bf16", True,
+                 fwd=True, bwd=True, n_samples=64),
+    )
+}
+# Order of the five workloads of the problem statement.
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+def generate(w: Workload, seed: int = 0, need_grad_out: bool | None = None) -> dict:
+    """Seeded CPU tensors for workload ``w``: q, k, v (w's dtype), do (if backward),
+    hot_rows (flattened (b,h,i) indices), samples (list of (h, i))."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (w.B, w.H, w.N, w.d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    if w.in_scale != 1.0:
+        q.mul_(w.in_scale)
+        k.mul_(w.in_scale)
+        v.mul_(w.in_scale)
+    hot = None
+    if w.hot_rows_frac > 0:
+        rows = w.B * w.H * w.N
+        hot = torch.randperm(rows, generator=g)[: int(round(w.hot_rows_frac * rows))]
+        q.view(rows, w.d)[hot] *= w.hot_rows_mult
+    out = {"q": q.to(w.torch_dtype), "k": k.to(w.torch_dtype), "v": v.to(w.torch_dtype),
+           "hot_rows": hot}
+    if need_grad_out if need_grad_out is not None else w.bwd:
+        out["do"] = torch.randn(shape, generator=g, dtype=torch.float32).to(w.torch_dtype)
+    if w.n_samples:
+        hs = torch.randint(0, w.H, (w.n_samples,), generator=g)
+        ids = torch.randint(0, w.N, (w.n_samples,), generator=g)
+        out["samples"] = [(int(h), int(i)) for h, i in zip(hs, ids)]
+    return out
+
+
+def random_qkv(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: int = 0,
+               in_scale: float = 1.0, with_do: bool = True) -> dict:
+    """Seeded standard-normal q, k, v (and do) for ad-hoc shapes (tail sweeps, edge cases)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, N, d)
+    out = {n: (torch.randn(shape, generator=g) * in_scale).to(dtype) for n in ("q", "k", "v")}
+    if with_do:
+        out["do"] = torch.randn(shape, generator=g).to(dtype)
+    return out

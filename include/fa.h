@@ -1,0 +1,111 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * What it computes.  Exact scaled-dot-product attention for each of B*H independent heads:
+ *     S = scale * Q K^T,  P = softmax(S) row-wise (optionally with the causal mask),  O = P V,
+ * as in "Standard Attention Implementation" (Algorithm 0) of the review "[논문 리뷰]
+ * FlashAttention: Fast and Memory-Efficient Exact Attention with IO-Awareness", computed
+ * tile by tile with the online softmax of its Algorithm 1 and of the "Tiling" section of
+ * "Flash Attention IO-awareness principle", so S and P never reach device memory.  The
+ * backward pass follows "Backward 구현" of "Triton 06: Flash Attention v2": Delta =
+ * rowsum(dO o O), then dK, dV and dQ recomputed from the stored log-sum-exp.
+ *
+ * Conventions shared by every entry point.
+ *   - Layout: every tensor is contiguous row-major [B, H, N, d]; lse is [B, H, N] float32.
+ *   - dtype: FA_BF16 (bfloat16 q/k/v/o/dout/dq/dk/dv, fp32 accumulation) or FA_F32 (all fp32).
+ *   - d (head dimension) is 64 or 128.  N >= 1, B >= 1, H >= 1, B*H*N*d < 2^31.
+ *   - Causal mask: key index j <= query index i (top-left aligned, square), the condition
+ *     offs_m >= offs_n of "개선 3" in "Triton 06: Flash Attention v2".
+ *   - lse receives, per query row, the natural log of sum_j exp(scale * q_i . k_j) over the
+ *     visible keys (the base-2 value the kernels keep is converted, as that post describes).
+ *   - Pointers are device pointers, 16-byte aligned.  The caller allocates and owns every
+ *     buffer; the library allocates no device memory on these paths.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous on it.
+ *   - Return value: FA_OK (0) or a negative FA_ERR_* code.  Argument errors are detected on
+ *     the host before anything is launched; nothing throws across the ABI.  Device-side
+ *     watchdog failures are reported by fa_device_status().
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum fa_dtype { FA_BF16 = 0, FA_F32 = 1 };
+
+enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,     /* null pointer, non-positive size, bad flag or dtype     */
+    FA_ERR_UNSUPPORTED_D = -2,   /* head dimension other than 64 or 128                    */
+    FA_ERR_MISALIGNED = -3,      /* a pointer is not 16-byte aligned                       */
+    FA_ERR_WORKSPACE = -4,       /* workspace missing or smaller than fa_bwd_workspace_bytes */
+    FA_ERR_LAUNCH = -5,          /* a CUDA call failed; fa_last_error() has its text       */
+    FA_ERR_DEVICE_TIMEOUT = -6,  /* a bounded on-device wait expired (watchdog)            */
+    FA_ERR_TOO_LARGE = -7,       /* a tensor has 2^31 or more elements                     */
+    FA_ERR_UNSUPPORTED_DEVICE = -8 /* bf16 tensor-core path needs compute capability 10.3 */
+};
+
+/* Forward.  q, k, v: inputs [B,H,N,d]; o: output [B,H,N,d] (same dtype); lse: output
+ * [B,H,N] fp32 (may be NULL when the caller does not need it).  scale is any finite float
+ * (1/sqrt(d) in the usual case).  causal is 0 or 1. */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, int dtype, void* stream);
+
+/* Bytes of device workspace fa_bwd needs for this shape (Delta and a base-2 copy of lse,
+ * both fp32 [B,H,N], plus alignment).  Returns 0 for invalid sizes. */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Backward of fa_fwd.  q, k, v, o, dout: [B,H,N,d] inputs (o and lse from fa_fwd with the
+ * same q, k, v, scale, causal); dq, dk, dv: outputs [B,H,N,d]; workspace: caller-owned
+ * device buffer of at least fa_bwd_workspace_bytes(B,H,N,d) bytes, overwritten.
+ * Gradients are of L = sum(dout o O): dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO with
+ * dS = P o (dP - Delta), dP = dO V^T, Delta = rowsum(dO o O).  Deterministic. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+           void* stream);
+
+/* Same as fa_fwd but forces an implementation: 0 = default dispatch, 1 = the portable SIMT
+ * kernel (fp32 math; accepts bf16 or fp32 tensors).  For cross-checking the tensor-core
+ * path on the device; the default path is what fa_fwd runs. */
+int fa_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, float scale, int causal, int dtype, int impl, void* stream);
+
+/* Same as fa_bwd but forces an implementation (0 = default, 1 = portable SIMT kernels). */
+int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                int impl, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device status word that bounded waits
+ * inside the kernels write when they give up.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (the
+ * wait site is appended to fa_last_error()) or FA_ERR_LAUNCH if the synchronisation failed. */
+int fa_device_status(void* stream);
+
+/* Upper bound, in nanoseconds, on every on-device wait (default 2e9).  Values below 1e6 are
+ * clamped to 1e6.  Applies to launches made after the call. */
+void fa_set_wait_limit_ns(unsigned long long ns);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(int code);
+
+/* Text of the last error seen by this thread (empty string if none). */
+const char* fa_last_error(void);
+
+/* Causal block schedule of query block `q_block` (rows [q_block*Br, min(N,(q_block+1)*Br)))
+ * against key blocks of Bc keys: number of blocks visited without a mask (*n_full) and with
+ * the element-wise mask (*n_masked); the rest are skipped.  This is the host copy of the
+ * classification every kernel uses ("개선 3", two-stage causal split).  Host-only. */
+int fa_causal_block_counts(int q_block, int Br, int Bc, int N, int* n_full, int* n_masked);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

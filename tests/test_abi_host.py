@@ -1,0 +1,147 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every symbol the
+header declares, rejects bad arguments with the documented codes before touching CUDA, and
+its causal block schedule matches the counts printed in the Triton FA2 write-up."""
+import ctypes
+import json
+import math
+import os
+import re
+
+import pytest
+
+from exact_attention_25_gb300 import _lib, build, perfmodel
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_device_status"} <= set(names)
+    assert set(names) == set(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+P = ctypes.c_void_p
+A = P(0x10000)  # aligned dummy pointers: validation must reject before dereferencing
+A2 = P(0x20000)
+MIS = P(0x10008)
+
+
+def fwd(lib, q=A, k=A, v=A, o=A2, lse=A2, B=1, H=1, N=8, d=64, scale=0.125, causal=0, dtype=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), -2), (dict(d=32), -2), (dict(N=0), -1), (dict(B=0), -1), (dict(H=-1), -1),
+    (dict(q=None), -1), (dict(o=None), -1), (dict(dtype=5), -1), (dict(causal=2), -1),
+    (dict(scale=math.inf), -1), (dict(scale=math.nan), -1), (dict(q=MIS), -3), (dict(o=MIS), -3),
+    (dict(B=1024, H=1024, N=1024, d=128), -7),
+])
+def test_forward_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert fwd(lib, **kw) == code
+    assert lib.fa_last_error().decode() != ""
+
+
+def bwd(lib, ws=A, ws_bytes=None, **kw):
+    args = dict(B=1, H=2, N=100, d=128, scale=0.1, causal=1, dtype=0)
+    args.update(kw)
+    if ws_bytes is None:
+        ws_bytes = lib.fa_bwd_workspace_bytes(args["B"], args["H"], args["N"], args["d"])
+    return lib.fa_bwd(A, A, A, A, A, A, A2, A2, A2, args["B"], args["H"], args["N"], args["d"],
+                      ctypes.c_float(args["scale"]), args["causal"], args["dtype"], ws, ws_bytes,
+                      None)
+
+
+def test_backward_rejects_bad_arguments(lib):
+    assert bwd(lib, d=80) == -2
+    assert bwd(lib, N=0) == -1
+    assert bwd(lib, ws=None) == -4
+    need = lib.fa_bwd_workspace_bytes(1, 2, 100, 128)
+    assert need >= 2 * 200 * 4
+    assert bwd(lib, ws_bytes=need - 1) == -4
+    assert bwd(lib, ws=MIS) == -3
+
+
+def test_workspace_size_contract(lib):
+    assert lib.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
+    for (B, H, N) in [(1, 1, 1), (4, 16, 4096), (1, 32, 32000)]:
+        assert lib.fa_bwd_workspace_bytes(B, H, N, 128) >= 2 * B * H * N * 4
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.fa_status_string(code).decode() == name
+    assert lib.fa_version().decode().startswith("fa-gb300")
+
+
+def counts(lib, q_block, Br, Bc, N):
+    nf, nm = ctypes.c_int(), ctypes.c_int()
+    rc = lib.fa_causal_block_counts(q_block, Br, Bc, N, ctypes.byref(nf), ctypes.byref(nm))
+    assert rc == 0
+    return nf.value, nm.value
+
+
+def test_causal_schedule_matches_the_printed_counts(lib):
+    g = json.load(open(os.path.join(GOLDEN, "causal_blocks.json")))
+    for c in g["cases"]:
+        assert counts(lib, c["q_block"], c["Br"], c["Bc"], c["N"]) == (c["n_full"], c["n_masked"]), c
+
+
+@pytest.mark.parametrize("Br,Bc,N", [(128, 128, 1000), (64, 128, 777), (128, 64, 4096), (256, 128, 2000),
+                                     (128, 128, 1), (7, 5, 100)])
+def test_causal_schedule_against_brute_force(lib, Br, Bc, N):
+    """Block classes against a per-element scan of the key <= query mask."""
+    for qb in range((N + Br - 1) // Br):
+        q0, q1 = qb * Br, min(N, (qb + 1) * Br)
+        nf = nm = 0
+        for k0 in range(0, N, Bc):
+            k1 = min(N, k0 + Bc)
+            vis = [[j <= i for j in range(k0, k1)] for i in range(q0, q1)]
+            flat = [x for r in vis for x in r]
+            if all(flat):
+                nf += 1
+            elif any(flat):
+                nm += 1
+        assert counts(lib, qb, Br, Bc, N) == (nf, nm), (qb, Br, Bc, N)
+    assert lib.fa_causal_block_counts((N + Br - 1) // Br, Br, Bc, N, ctypes.byref(ctypes.c_int()),
+                                      ctypes.byref(ctypes.c_int())) == -1
+
+
+def test_hbm_models_match_the_printed_tables():
+    g = json.load(open(os.path.join(GOLDEN, "hbm_models.json")))
+    sa = g["standard_attention_fp16"]
+    for N, b in sa["rows"]:
+        assert abs(perfmodel.standard_attention_intermediate_bytes(N, 2) - b) <= sa["rel_tol"] * b
+    l6 = g["lesson06_fp32_d64"]
+    for N, naive_mib, flash_mib in l6["rows"]:
+        naive, flash = perfmodel.lesson06_hbm_elements(N, l6["d"])
+        assert abs(naive * 4 / 2**20 - naive_mib) <= l6["rel_tol"] * naive_mib + 0.05
+        assert abs(flash * 4 / 2**20 - flash_mib) <= l6["rel_tol"] * flash_mib
+    t = g["tiling_example"]
+    assert t["Br"] * t["d"] * t["elem_bytes"] == t["tile_kb"] * 1024
+    assert 5 * t["tile_kb"] == t["total_kb"]
+    assert math.ceil(t["N"] / t["Br"]) == t["Tr"] and math.ceil(t["N"] / t["Bc"]) == t["Tc"]
+
+
+def test_flop_convention():
+    assert perfmodel.fwd_flops(1, 1, 512, 64, False) == 4 * 512 * 512 * 64
+    assert perfmodel.fwd_flops(2, 32, 8192, 128, True) == pytest.approx(1.0995e12, rel=1e-4)
+    assert perfmodel.bwd_flops(4, 16, 4096, 128, True) == pytest.approx(6.872e11, rel=1e-3)
