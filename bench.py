@@ -1,0 +1,371 @@
+"""Benchmark: one step = the whole hot path (forward, then backward) of exact attention on the
+long-sequence workload B=1, H=32, N=32000, d=128, causal, bf16 (inputs of 262 MB per tensor,
+larger than the 129 MB L2, so no flush is needed between steps).
+
+Prints ONE JSON line.  ``value`` is attention TFLOP/s (forward 4BHN^2d/2 + backward 2.5x) with
+inputs resident in HBM; ``e2e`` is the same metric through the public API with the inputs
+copied from pinned host memory and the results read back inside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle (the only baseline that exists for this
+method) on a bounded sample of the same workload.  Under torchrun each rank runs an
+independent replica (weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "bf16_b1h32_n32000_d128_causal_fwdbwd"
+METRIC = "attention TFLOP/s (fwd; fwd+bwd) on 1 GB300 and % of dense BF16 TC peak"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def run_gpu(args):
+    import torch
+
+    import exact_attention_25_gb300 as fa
+    from exact_attention_25_gb300 import perfmodel
+    from exact_attention_25_gb300.inputs import WORKLOADS, generate
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[WORKLOAD]
+    x = generate(w, seed=rank)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    scale = w.scale
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, scale, w.causal, stream)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, w.causal, wsp, stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    fa.fa_device_status(stream)
+
+    # ---- device-resident timing: per-phase events on the launching stream ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            fa.fa_fwd(q, k, v, o, lse, scale, w.causal, stream)
+            ev[i][1].record(stream)
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, w.causal, wsp, stream)
+            ev[i][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    fa.fa_device_status(stream)
+    total_ms = t0.elapsed_time(t1)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if ws > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    f_fwd = perfmodel.fwd_flops(B, H, N, d, w.causal)
+    f_bwd = perfmodel.bwd_flops(B, H, N, d, w.causal)
+    value = ws * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    clocks = clk.summary()
+
+    # ---- end to end through the public API: pinned host in, results back out ----
+    hq, hk, hv, hdo = (t.pin_memory() for t in (x["q"], x["k"], x["v"], x["do"]))
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            fa.fa_fwd(q, k, v, o, lse, scale, w.causal, stream)
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, w.causal, wsp, stream)
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    if ws > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fwd_med = statistics.median(fwd_ms)
+    bwd_med = statistics.median(bwd_ms)
+    fwd_tflops = f_fwd / (fwd_med * 1e-3) / 1e12
+    bwd_tflops = f_bwd / (bwd_med * 1e-3) / 1e12
+    # Dominant kernel: the one with the largest share of the step (from the launch list).
+    dom = "fa_fwd_tc_kernel<128>" if fwd_med >= bwd_med else "backward kernels"
+    dom_tflops = fwd_tflops if fwd_med >= bwd_med else bwd_tflops
+    peak = peaks.get("bf16_tflops_sustained", 1692.4)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
+        "config": {
+            "workload": "long-sequence causal attention forward+backward, B=1 H=32 N=32000 d=128 bf16",
+            "B": B, "H": H, "N": N, "d": d, "causal": True, "scale": scale,
+            "l2": "inputs (262 MB per tensor) larger than the 129 MB L2; no flush",
+            "parallelism": f"replicas{ws}" if ws > 1 else "single GPU",
+        },
+        "phases": {
+            "fwd_ms": round(fwd_med, 4), "fwd_tflops": round(fwd_tflops, 2),
+            "bwd_ms": round(bwd_med, 4), "bwd_tflops": round(bwd_tflops, 2),
+            "fwd_frac_of_bf16_burst": round(fwd_tflops / peaks.get("bf16_tflops", 1885.6), 4),
+        },
+        "roofline": {
+            "kernel": dom,
+            "bound": "tensor",
+            "achieved": round(dom_tflops, 2),
+            "peak": peak,
+            "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+            "unit": "TFLOP/s",
+            "frac": round(dom_tflops / peak, 4),
+            "traffic": None,
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps * 4,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def cpu_baseline(target_s: float = 15.0) -> dict:
+    """The fp64 oracle, as it stands, on a bounded sample of the same workload: full forward +
+    backward of the first N_s tokens (an exact causal sub-problem) of as many heads as there
+    are host cores, timed on the host.  Reported in the metric's unit."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_25_gb300 import perfmodel
+    from exact_attention_25_gb300.inputs import WORKLOADS, generate
+
+    w = WORKLOADS[WORKLOAD]
+    cores = os.cpu_count() or 1
+    heads = min(cores, w.H)
+    n_s = 1024
+    x = generate(w, seed=0)
+    # grow the sample until one run takes a meaningful fraction of the target time
+    while True:
+        q, k, v, do = (x[n][:, :heads, :n_s] for n in ("q", "k", "v", "do"))
+        t = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, w.scale, w.causal, nthreads=cores)
+        el = time.perf_counter() - t
+        if el > target_s / 4 or n_s >= 8192:
+            break
+        n_s *= 2
+    flops = (perfmodel.fwd_flops(1, heads, n_s, w.d, True) + perfmodel.bwd_flops(1, heads, n_s, w.d, True))
+    del np
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": round(el, 3),
+            "sample": f"fp64 oracle forward+backward of the first {n_s} tokens of {heads} heads "
+                      f"(causal prefix, d=128) of the workload; FLOPs by the causal convention"}
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from exact_attention_25_gb300 import perfmodel
+    from exact_attention_25_gb300.inputs import WORKLOADS, generate
+
+    w = WORKLOADS[WORKLOAD]
+    cores = os.cpu_count() or 1
+    heads = min(cores, w.H)
+    n_s = 2048
+    x = generate(w, seed=0)
+    q, k, v, do = (x[n][:, :heads, :n_s] for n in ("q", "k", "v", "do"))
+    for _ in range(args.warmup):
+        oracle.attention_bwd(q[:, :1, :256], k[:, :1, :256], v[:, :1, :256], do[:, :1, :256],
+                             w.scale, w.causal, nthreads=1)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, w.scale, w.causal, nthreads=cores)
+        times.append(time.perf_counter() - t)
+    el = statistics.median(times)
+    flops = perfmodel.fwd_flops(1, heads, n_s, w.d, True) + perfmodel.bwd_flops(1, heads, n_s, w.d, True)
+    value = flops / el / 1e12
+    sample = (f"fp64 oracle forward+backward of the first {n_s} tokens of {heads} heads (causal "
+              f"prefix, d=128) of the workload per step")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long-sequence causal attention forward+backward, B=1 H=32 N=32000 "
+                               "d=128 (bounded CPU sample)", "B": 1, "H": heads, "N": n_s, "d": w.d,
+                   "causal": True},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
