@@ -1,13 +1,365 @@
-// Backward attention on sm_103a tensor cores (placeholder entry: routes to the SIMT kernels
-// until the tensor-core kernels land).
+// Backward attention on sm_103a tensor cores, in the two-loop structure of "Backward 구현" /
+// "Forward/Backward 전체 흐름 요약" of "Triton 06: Flash Attention v2" (after the Delta
+// preprocess): a dK/dV kernel whose CTA owns one block of 128 keys and sweeps the query
+// blocks, and a dQ kernel whose CTA owns one block of 128 queries and sweeps the key blocks.
+// S and P are recomputed from Q, K and the stored base-2 LSE (recomputation section of
+// "Flash Attention IO-awareness principle"); nothing N x N touches device memory and no
+// atomics are used, so the result is deterministic.
+//
+// One template serves both kernels.  With X, Y the resident tiles and A, B the streamed ones:
+//   dK/dV (KV = true):  X = K_j, Y = V_j, A = Q_i, B = dO_i
+//       T1 = X A^T = S^T, T2 = Y B^T = dP^T               (tcgen05, operands in smem)
+//       P^T = exp2(c S^T - L2), dS^T = P^T o (dP^T - Delta)  (elementwise warpgroup)
+//       acc1 += P^T B = dV,  acc2 += dS^T A = dK / scale   (tcgen05, first operand in TMEM)
+//   dQ (KV = false):    X = Q_i, Y = dO_i, A = K_j, B = V_j
+//       T1 = S, T2 = dP, dS = P o (dP - Delta), acc2 += dS A = dQ / scale
+// Roles (6 warps): warps 0-3 elementwise + epilogue (thread = row of X = TMEM lane),
+// warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
+// TMEM columns: T1 [0,128), T2 [128,256), acc1 [256,256+d), acc2 [256+d,256+2d); the bf16
+// operands P^T / dS^T are written over the first 64 columns of T1 / T2.
 #include "fa_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st);
+
+template <int D>
+struct BwdCfg {
+    static constexpr int BR = 128;                 // rows of the resident block
+    static constexpr int BS = 128;                 // rows of a streamed block
+    static constexpr int PANELS = D / 64;
+    static constexpr int PANEL_BYTES = 128 * 128;
+    static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;  // 128 rows x D bf16
+    static constexpr int STAGES = 2;
+    static constexpr int SMEM_RES = 2 * TILE_BYTES;           // X, Y
+    static constexpr int SMEM_STREAM = STAGES * 2 * TILE_BYTES;  // (A, B) per stage
+    static constexpr int SMEM_BYTES = SMEM_RES + SMEM_STREAM + 1024;
+    static constexpr int THREADS = 192;
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <int D, bool KV>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_y,
+                     const __grid_constant__ CUtensorMap tm_a,
+                     const __grid_constant__ CUtensorMap tm_b, const BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sX = smem;
+    uint8_t* sY = sX + C::TILE_BYTES;
+    uint8_t* sAB = sY + C::TILE_BYTES;  // stage s: A at sAB + s*2*TILE, B right after
+
+    __shared__ __align__(8) uint64_t bar_res;
+    __shared__ __align__(8) uint64_t bar_full[C::STAGES];
+    __shared__ __align__(8) uint64_t bar_empty[C::STAGES];
+    __shared__ __align__(8) uint64_t bar_t;     // T1, T2 ready
+    __shared__ __align__(8) uint64_t bar_e;     // bf16 operands written by the elementwise WG
+    __shared__ __align__(8) uint64_t bar_acc;   // accumulators final
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ float sL2[2][128];
+    __shared__ float sDl[2][128];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = p.N;
+    const int bh = blockIdx.x;
+    const int nblk = (N + 127) / 128;
+    // Heaviest blocks first: for dK/dV the first key blocks see the most query blocks under
+    // the causal mask; for dQ the last query blocks see the most key blocks.
+    const int xb = KV ? static_cast<int>(blockIdx.y)
+                      : static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    const int x0 = xb * 128, x1 = min(N, x0 + 128);
+    // Streamed blocks visited: a contiguous range [s_begin, s_end).
+    int s_begin = 0, s_end = nblk;
+    if (p.causal) {
+        if (KV) {  // query blocks that see any key of [x0, x1)
+            while (s_begin < nblk &&
+                   causal_tile_class(s_begin * 128, min(N, s_begin * 128 + 128), x0, x1) == kTileSkip)
+                ++s_begin;
+        } else {   // key blocks seen by any query of [x0, x1)
+            s_end = 0;
+            while (s_end < nblk &&
+                   causal_tile_class(x0, x1, s_end * 128, min(N, s_end * 128 + 128)) != kTileSkip)
+                ++s_end;
+        }
+    }
+    const int n_it = s_end - s_begin;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_res, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        mbar_init(&bar_t, 1);
+        mbar_init(&bar_e, 128);
+        mbar_init(&bar_acc, 1);
+        mbar_init(&bar_drain, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_y);
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_slot;
+    const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+
+    if (warp == 4) {
+        // ------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_res, 2 * C::TILE_BYTES);
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                tma_load_3d(sX + pn * C::PANEL_BYTES, &tm_x, &bar_res, 64 * pn, x0, bh);
+                tma_load_3d(sY + pn * C::PANEL_BYTES, &tm_y, &bar_res, 64 * pn, x0, bh);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                if (!mbar_wait(&bar_empty[s], ph ^ 1, wd, kSiteBwdLoadEmpty)) break;
+                uint8_t* sA = sAB + s * 2 * C::TILE_BYTES;
+                uint8_t* sB = sA + C::TILE_BYTES;
+                const int row = (s_begin + it) * 128;
+                mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE_BYTES);
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    tma_load_3d(sA + pn * C::PANEL_BYTES, &tm_a, &bar_full[s], 64 * pn, row, bh);
+                    tma_load_3d(sB + pn * C::PANEL_BYTES, &tm_b, &bar_full[s], 64 * pn, row, bh);
+                }
+                issued = it + 1;
+            }
+            volatile int no_abort = 0;
+            const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
+            mbar_wait(&bar_res, 0, wd_drain, kSiteBwdDrain);
+            for (int it = max(0, issued - C::STAGES); it < issued; ++it)
+                mbar_wait(&bar_full[it % C::STAGES], (it / C::STAGES) & 1, wd_drain, kSiteBwdDrain);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdT = idesc_bf16_f32(128, 128, 0, 0);  // T = X A^T
+            constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);  // acc += (TMEM) * (MN-major)
+            const uint32_t sXa = smem_u32(sX), sYa = smem_u32(sY), sABa = smem_u32(sAB);
+            const uint32_t tT1 = tbase, tT2 = tbase + 128u;
+            const uint32_t tAcc1 = tbase + 256u, tAcc2 = tbase + 256u + D;
+            bool ok = mbar_wait(&bar_res, 0, wd, kSiteBwdMmaKV);
+            int committed = 0;
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1;
+                if (!mbar_wait(&bar_full[s], ph, wd, kSiteBwdMmaQ)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sA = sABa + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
+                    mma_ss(tT1, sdesc_sw128(sXa + off, 16, 1024), sdesc_sw128(sA + off, 16, 1024),
+                           kIdT, ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
+                    mma_ss(tT2, sdesc_sw128(sYa + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
+                           kIdT, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_t);
+                if (!mbar_wait(&bar_e, it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
+                tc_fence_after();
+                if (KV) {  // dV += P^T dO
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tAcc1, tT1 + 8u * ks,
+                               sdesc_sw128(sB + ks * 2048, C::PANEL_BYTES, 1024), kIdAcc,
+                               (it > 0 || ks > 0) ? 1u : 0u);
+                }
+                // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(tAcc2, tT2 + 8u * ks, sdesc_sw128(sA + ks * 2048, C::PANEL_BYTES, 1024),
+                           kIdAcc, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&bar_empty[s]);
+                committed = it + 1;
+            }
+            if (ok) mma_commit(&bar_acc);
+            volatile int no_abort = 0;
+            const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
+            mma_commit(&bar_drain);
+            mbar_wait(&bar_drain, 0, wd_drain, kSiteBwdDrain);
+            for (int it = max(0, committed - C::STAGES); it < committed; ++it)
+                mbar_wait(&bar_empty[it % C::STAGES], (it / C::STAGES) & 1, wd_drain, kSiteBwdDrain);
+            if (ok) mbar_wait(&bar_acc, 0, wd_drain, kSiteBwdDrain);
+        }
+    } else {
+        // ------------------------------------------------------------- elementwise (warps 0-3)
+        const int r = threadIdx.x;  // row of the resident block = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tT1 = tbase + lane_base, tT2 = tbase + lane_base + 128u;
+        const uint32_t tAcc1 = tbase + lane_base + 256u, tAcc2 = tbase + lane_base + 256u + D;
+        const float c2 = p.scale_log2;
+        const size_t row_base = static_cast<size_t>(bh) * N;
+        const int xrow = x0 + r;
+        // dQ kernel: the row statistics of this thread's query row are fixed.
+        float L2_self = 0.0f, D_self = 0.0f;
+        if (!KV && xrow < N) {
+            L2_self = p.lse2[row_base + xrow];
+            D_self = p.delta[row_base + xrow];
+        }
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int sb = s_begin + it;
+            const int s0 = sb * 128;  // first row of the streamed block
+            if (KV) {  // stage L2 / Delta of the 128 query rows of this block
+                const int qi = s0 + r;
+                sL2[it & 1][r] = (qi < N) ? p.lse2[row_base + qi] : INFINITY;
+                sDl[it & 1][r] = (qi < N) ? p.delta[row_base + qi] : 0.0f;
+                named_bar_sync(1, 128);
+            }
+            if (!warp_wait_all(&bar_t, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
+            tc_fence_after();
+            // element-wise mask: causal diagonal block, and (dQ kernel) keys beyond N
+            const bool diag = p.causal &&
+                              causal_tile_class(KV ? s0 : x0, KV ? min(N, s0 + 128) : x1,
+                                                KV ? x0 : s0, KV ? x1 : min(N, s0 + 128)) == kTileMasked;
+            const bool tail = !KV && (s0 + 128 > N);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(tT1 + 32u * ch, sv);
+                tmem_ld32(tT2 + 32u * ch, dpv);
+                tmem_wait_ld();
+                reg_fence32(sv);
+                reg_fence32(dpv);
+                uint32_t pkP[16], pkS[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 32 * ch + e + u;
+                        const float L2 = KV ? sL2[it & 1][col] : L2_self;
+                        const float Dl = KV ? sDl[it & 1][col] : D_self;
+                        float pv = ex2(fmaf(__uint_as_float(sv[e + u]), c2, -L2));
+                        if (diag || tail) {
+                            const int key = KV ? xrow : s0 + col;
+                            const int qry = KV ? s0 + col : xrow;
+                            if ((diag && key > qry) || (tail && key >= N)) pv = 0.0f;
+                        }
+                        pr[u] = pv;
+                        ds[u] = pv * (__uint_as_float(dpv[e + u]) - Dl);
+                    }
+                    pkP[e / 2] = pack_bf16x2(pr[0], pr[1]);
+                    pkS[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                }
+                if (KV) tmem_st16(tT1 + 16u * ch, pkP);
+                tmem_st16(tT2 + 16u * ch, pkS);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar_e);
+        }
+        // ------------------------------------------------------------- epilogue
+        if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
+            tc_fence_after();
+            __nv_bfloat16* out2 = static_cast<__nv_bfloat16*>(KV ? p.dk : p.dq);
+            __nv_bfloat16* out1 = static_cast<__nv_bfloat16*>(p.dv);
+#pragma unroll 1
+            for (int which = KV ? 0 : 1; which < 2; ++which) {
+                const uint32_t tAcc = which == 0 ? tAcc1 : tAcc2;
+                const float mul = which == 0 ? 1.0f : p.scale;
+                __nv_bfloat16* dst_row = (which == 0 ? out1 : out2) + (row_base + xrow) * D;
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t a[32];
+                    tmem_ld32(tAcc + 32u * ch, a);
+                    tmem_wait_ld();
+                    reg_fence32(a);
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
+                                                __uint_as_float(a[2 * c + 1]) * mul);
+                    if (xrow < N) {
+                        uint4* dst = reinterpret_cast<uint4*>(dst_row + ch * 32);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                                packed[4 * c + 3]);
+                    }
+                }
+            }
+        } else if (n_it == 0 && xrow < N) {
+            // a block that no streamed block touches has zero gradient (cannot occur for
+            // square causal attention, kept for completeness)
+            __nv_bfloat16* out2 = static_cast<__nv_bfloat16*>(KV ? p.dk : p.dq);
+            for (int c = 0; c < D; ++c) out2[(row_base + xrow) * D + c] = __float2bfloat16_rn(0.0f);
+            if (KV)
+                for (int c = 0; c < D; ++c)
+                    static_cast<__nv_bfloat16*>(p.dv)[(row_base + xrow) * D + c] = __float2bfloat16_rn(0.0f);
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool KV>
+static cudaError_t launch_one(const CUtensorMap& x, const CUtensorMap& y, const CUtensorMap& a,
+                              const CUtensorMap& b, const BwdParams& p, cudaStream_t st)
+{
+    using C = BwdCfg<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_tc_kernel<D, KV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid(p.BH, (p.N + 127) / 128);
+    fa_bwd_tc_kernel<D, KV><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(x, y, a, b, p);
+    return cudaGetLastError();
+}
+
+// maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
+cudaError_t launch_bwd_tc_stage(int d, int stage, const CUtensorMap* maps, const BwdParams& p,
+                                cudaStream_t st)
+{
+    const CUtensorMap &q = maps[0], &k = maps[1], &v = maps[2], &g = maps[3];
+    if (stage == 1)
+        return d == 64 ? launch_one<64, true>(k, v, q, g, p, st) : launch_one<128, true>(k, v, q, g, p, st);
+    return d == 64 ? launch_one<64, false>(q, g, k, v, p, st) : launch_one<128, false>(q, g, k, v, p, st);
+}
 
 cudaError_t launch_bwd_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
 {
-    (void)maps;
-    return launch_bwd_simt(d, 0, p, st);
+    cudaError_t e = launch_bwd_tc_stage(d, 1, maps, p, st);
+    if (e != cudaSuccess) return e;
+    return launch_bwd_tc_stage(d, 2, maps, p, st);
 }
+
 }  // namespace fa

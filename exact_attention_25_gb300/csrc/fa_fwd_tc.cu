@@ -35,14 +35,6 @@ struct FwdCfg {
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P stays below 2^8
 };
 
-// All 32 lanes wait; the warp proceeds only if every lane saw the phase complete.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Watchdog& wd,
-                                          int site)
-{
-    const bool ok = mbar_wait(bar, parity, wd, site);
-    return __all_sync(0xffffffffu, ok);
-}
-
 template <int D>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -256,10 +248,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const bool prescale = !(c2 > 0.0f);
         const float cf = prescale ? 1.0f : c2;
         float m = -INFINITY;  // running max of x (possibly stale by < threshold)
-        float l = 0.0f;       // running sum of exp2(x - m) (fp32, before bf16 rounding)
+        float l = 0.0f;       // running sum of the bf16-rounded exp2(x - m), in fp32
         bool ok = t < nt;
         for (int j = 0; ok && j < J[t]; ++j) {
-            if (!warp_wait(&bar_sfull[t], j & 1, wd, kSiteFwdSoftmaxS)) { ok = false; break; }
+            if (!warp_wait_all(&bar_sfull[t], j & 1, wd, kSiteFwdSoftmaxS)) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld32(tS + 0, sr);
@@ -317,12 +309,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     const float p1 = ex2(fmaf(x[cb * 32 + c + 1], cf, neg_m));
                     const float p2 = ex2(fmaf(x[cb * 32 + c + 2], cf, neg_m));
                     const float p3 = ex2(fmaf(x[cb * 32 + c + 3], cf, neg_m));
-                    ls0 += p0;
-                    ls1 += p1;
-                    ls2 += p2;
-                    ls3 += p3;
-                    pk[c / 2] = pack_bf16x2(p0, p1);
-                    pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+                    const uint32_t w01 = pack_bf16x2(p0, p1);
+                    const uint32_t w23 = pack_bf16x2(p2, p3);
+                    // l sums the bf16-rounded weights that the P V product uses, so that
+                    // O = sum(P V) / l is an exact convex combination of the rounded weights.
+                    ls0 += __uint_as_float(w01 << 16);
+                    ls1 += __uint_as_float(w01 & 0xFFFF0000u);
+                    ls2 += __uint_as_float(w23 << 16);
+                    ls3 += __uint_as_float(w23 & 0xFFFF0000u);
+                    pk[c / 2] = w01;
+                    pk[c / 2 + 1] = w23;
                 }
                 tmem_st16(tP + 16u * cb, pk);
             }
@@ -347,7 +343,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         // ------------------------------------------------------------- epilogue
         if (ok && J[t] > 0) {
-            if (warp_wait(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
+            if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
                 tc_fence_after();
                 const float inv_l = 1.0f / l;
                 __nv_bfloat16* orow =

@@ -92,6 +92,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return mbar_wait_slow(bar, parity, wd, site);
 }
 
+// All 32 lanes of the warp wait; the warp proceeds only if every lane saw the phase
+// complete, so warp-collective tcgen05 instructions after it stay converged.
+__device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, const Watchdog& wd,
+                                              int site)
+{
+    const bool ok = mbar_wait(bar, parity, wd, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------------------------
 // TMA: 3-D tiled load global -> shared, completion counted on an mbarrier (bytes).
 // Coordinates are {x (innermost, elements), y (rows), z}.  x must be a multiple of 8 for

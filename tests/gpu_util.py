@@ -27,8 +27,10 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
-def check_fwd(o, lse, o_ref, lse_ref, dtype, what=""):
-    """Element-wise comparison of O and LSE against the oracle; returns the statistics."""
+def check_fwd(o, lse, o_ref, lse_ref, dtype, what="", check_mean=True):
+    """Element-wise comparison of O and LSE against the oracle; returns the statistics.
+    The mean bound is a property of a whole output tensor; sampled rows pass
+    check_mean=False and are held to the max bounds only."""
     o, lse, o_ref, lse_ref = f64(o), f64(lse), f64(o_ref), f64(lse_ref)
     assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
     assert np.isfinite(o).all() and np.isfinite(lse).all(), f"non-finite output {what}"
@@ -50,7 +52,8 @@ def check_fwd(o, lse, o_ref, lse_ref, dtype, what=""):
         stats["max_ulp_large"] = float((err[big] / bf16_ulp(o_ref[big])).max())
         assert stats["max_ulp_large"] <= 1.0, (what, stats)
     assert stats["max_abs_o_small"] <= TOL_BF16_O_MAX, (what, stats)
-    assert stats["mean_abs_o"] <= TOL_BF16_O_MEAN, (what, stats)
+    if check_mean:
+        assert stats["mean_abs_o"] <= TOL_BF16_O_MEAN, (what, stats)
     assert stats["max_abs_lse"] <= TOL_BF16_LSE, (what, stats)
     return stats
 

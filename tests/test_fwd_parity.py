@@ -120,14 +120,19 @@ def test_workload_full_size_sampled_heads(name, n_heads):
         print(name, b, h, stats)
     if w.hot_rows_frac:
         # every hot row of the whole batch, one row at a time
-        rows = x["hot_rows"][:256].tolist()
-        for r in rows[:64]:
+        got_o, got_l, ref_o, ref_l = [], [], [], []
+        for r in x["hot_rows"][:64].tolist():
             bh, i = divmod(r, w.N)
             b, h = divmod(bh, w.H)
             res = oracle.attention_rows_head(x["q"][b, h], x["k"][b, h], x["v"][b, h],
                                              torch.zeros(w.N, w.d), w.scale, w.causal, [i], [])
-            check_fwd(o_cpu[b, h, i:i + 1], lse_cpu[b, h, i:i + 1], res["o"], res["lse"],
-                      torch.bfloat16, f"hot row {r}")
+            got_o.append(f64(o_cpu[b, h, i:i + 1]))
+            got_l.append(f64(lse_cpu[b, h, i:i + 1]))
+            ref_o.append(res["o"])
+            ref_l.append(res["lse"])
+        stats = check_fwd(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o),
+                          np.concatenate(ref_l), torch.bfloat16, "hot rows", check_mean=False)
+        print("hot rows (x10 queries)", stats)
 
 
 def test_workload_long_sequence_sampled_rows():
@@ -142,4 +147,4 @@ def test_workload_long_sequence_sampled_rows():
         res = oracle.attention_rows_head(x["q"][0, h], x["k"][0, h], x["v"][0, h],
                                          torch.zeros(w.N, w.d), w.scale, w.causal, rows, [])
         check_fwd(o_cpu[0, h, rows], lse_cpu[0, h, rows], res["o"], res["lse"], torch.bfloat16,
-                  f"N=32000 h={h}")
+                  f"N=32000 h={h}", check_mean=False)
