@@ -13,7 +13,7 @@ from . import _lib
 from ._lib import FA_BF16, FA_F32, FaError, check, load
 
 __all__ = [
-    "FA_BF16", "FA_F32", "FaError", "load", "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes",
+    "FA_BF16", "FA_F32", "FaError", "load", "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_causal_block_counts", "forward", "backward",
 ]
 
@@ -84,6 +84,18 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspac
         check(lib.fa_bwd_impl(*args, int(impl), _stream(stream)))
     else:
         check(lib.fa_bwd(*args, _stream(stream)))
+
+
+def fa_bwd_stage(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspace,
+                 stage: int, stream=None) -> None:
+    """C ``fa_bwd_stage``: 0 = preprocess, 1 = dK/dV, 2 = dQ (0, 1, 2 in order = fa_bwd)."""
+    _check_tensors(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, H, N, d = _shape(q)
+    nbytes = workspace.numel() * workspace.element_size()
+    check(load().fa_bwd_stage(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _ptr(workspace), nbytes,
+        int(stage), _stream(stream)))
 
 
 def fa_device_status(stream=None) -> None:

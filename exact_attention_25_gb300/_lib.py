@@ -19,7 +19,7 @@ STATUS = {
 }
 # Every symbol include/fa.h declares (tests check the library exports all of them).
 EXPORTS = (
-    "fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_fwd_impl", "fa_bwd_impl",
+    "fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_stage", "fa_fwd_impl", "fa_bwd_impl",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_status_string", "fa_last_error",
     "fa_causal_block_counts", "fa_version",
 )
@@ -54,6 +54,8 @@ def load(path: str | None = None):
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
         lib.fa_bwd_impl.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp,
                                     sz, i, vp]
+        lib.fa_bwd_stage.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp,
+                                     sz, i, vp]
         lib.fa_device_status.argtypes = [vp]
         lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.fa_set_wait_limit_ns.restype = None
@@ -63,7 +65,7 @@ def load(path: str | None = None):
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_causal_block_counts.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
         lib.fa_version.restype = ctypes.c_char_p
-        for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_device_status",
+        for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_bwd_stage", "fa_device_status",
                    "fa_causal_block_counts"):
             getattr(lib, fn).restype = ctypes.c_int
         if path is None:

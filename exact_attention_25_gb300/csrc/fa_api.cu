@@ -17,6 +17,8 @@ cudaError_t launch_bwd_preprocess(int d, int is_f32, const BwdParams& p, cudaStr
                                   int num_sms);
 cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st);
 cudaError_t launch_bwd_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_tc_stage(int d, int stage, const CUtensorMap* maps, const BwdParams& p,
+                                cudaStream_t st);
 
 // Device status word written by bounded waits that give up (0 = fine).
 __device__ int g_status_word;
@@ -159,11 +161,14 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dout,
               const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
               float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
-              int impl, void* stream)
+              int impl, int stage, void* stream)
 {
     int rc = check_common(B, H, N, d, scale, causal, dtype);
     if (rc) return rc;
     if (impl != 0 && impl != 1) return fail(FA_ERR_INVALID_ARG, "impl must be 0 or 1");
+    if (stage < -1 || stage > 2) return fail(FA_ERR_INVALID_ARG, "stage must be 0, 1 or 2");
+    if (stage >= 0 && (dtype != FA_BF16 || impl != 0))
+        return fail(FA_ERR_INVALID_ARG, "staged backward is the bf16 tensor-core path only");
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
         return fail(FA_ERR_INVALID_ARG, "every tensor pointer must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
@@ -187,8 +192,12 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     const int is_f32 = dtype == FA_F32;
-    cudaError_t e = fa::launch_bwd_preprocess(d, is_f32, p, st, di->sms);
-    if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+    cudaError_t e = cudaSuccess;
+    if (stage <= 0) {
+        e = fa::launch_bwd_preprocess(d, is_f32, p, st, di->sms);
+        if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+        if (stage == 0) return FA_OK;
+    }
     if (is_f32 || impl == 1) {
         e = fa::launch_bwd_simt(d, is_f32, p, st);
     } else {
@@ -198,7 +207,8 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
         const void* srcs[4] = {q, k, v, dout};
         for (int i = 0; i < 4; ++i)
             if ((rc = make_map(&maps[i], srcs[i], p.BH, N, d, 128))) return rc;
-        e = fa::launch_bwd_tc(d, maps, p, st);
+        e = stage < 0 ? fa::launch_bwd_tc(d, maps, p, st)
+                      : fa::launch_bwd_tc_stage(d, stage, maps, p, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return FA_OK;
@@ -233,7 +243,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* stream)
 {
     return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
-                     workspace, workspace_bytes, 0, stream);
+                     workspace, workspace_bytes, 0, -1, stream);
 }
 
 int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -242,7 +252,17 @@ int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, cons
                 int impl, void* stream)
 {
     return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
-                     workspace, workspace_bytes, impl, stream);
+                     workspace, workspace_bytes, impl, -1, stream);
+}
+
+int fa_bwd_stage(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                 int stage, void* stream)
+{
+    if (stage < 0 || stage > 2) return fail(FA_ERR_INVALID_ARG, "stage must be 0, 1 or 2");
+    return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                     workspace, workspace_bytes, 0, stage, stream);
 }
 
 int fa_device_status(void* stream)

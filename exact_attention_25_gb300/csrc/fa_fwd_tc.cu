@@ -4,12 +4,11 @@
 //
 // One CTA owns NT = 2 query tiles of 128 rows of one head (the FlashAttention-2 Q-outer
 // loop order, "FA2·FA3" section of "Flash Attention IO-awareness principle") and streams
-// the key/value blocks of 128 keys through a shared-memory ring.  Roles (12 warps):
+// the key/value blocks of 128 keys through a shared-memory ring.  Roles (10 warps):
 //   warps 0-3   softmax of query tile 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax of query tile 1
 //   warp  8     TMA producer (one lane)
 //   warp  9     TMEM allocator + MMA issuer (one lane)
-//   warps 10-11 idle (kept so the softmax warpgroups sit on warpgroup boundaries)
 // TMEM columns: S_t at [128t, 128t+128) (fp32), P_t (bf16 pairs) aliased on the upper half
 // of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised).
 #include "fa_common.cuh"
@@ -30,13 +29,13 @@ struct FwdCfg {
     static constexpr int SMEM_K = STAGES * TILE_BYTES;
     static constexpr int SMEM_V = STAGES * TILE_BYTES;
     static constexpr int SMEM_BYTES = SMEM_Q + SMEM_K + SMEM_V + 1024;  // + alignment slack
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 320;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P stays below 2^8
 };
 
 template <int D>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+__global__ void __maxnreg__(200)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
@@ -248,7 +247,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const bool prescale = !(c2 > 0.0f);
         const float cf = prescale ? 1.0f : c2;
         float m = -INFINITY;  // running max of x (possibly stale by < threshold)
-        float l = 0.0f;       // running sum of the bf16-rounded exp2(x - m), in fp32
+        float l = 0.0f;       // running sum of exp2(x - m) (fp32, before rounding): the LSE
+        float lr = 0.0f;      // running sum of the bf16-rounded exp2(x - m): normalises O
         bool ok = t < nt;
         for (int j = 0; ok && j < J[t]; ++j) {
             if (!warp_wait_all(&bar_sfull[t], j & 1, wd, kSiteFwdSoftmaxS)) { ok = false; break; }
@@ -297,9 +297,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 alpha = ex2(m - mt);  // m = -inf on the first block gives 0
                 m = mt;
                 l *= alpha;
+                lr *= alpha;
             }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+            float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t pk[16];
@@ -311,18 +312,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     const float p3 = ex2(fmaf(x[cb * 32 + c + 3], cf, neg_m));
                     const uint32_t w01 = pack_bf16x2(p0, p1);
                     const uint32_t w23 = pack_bf16x2(p2, p3);
-                    // l sums the bf16-rounded weights that the P V product uses, so that
-                    // O = sum(P V) / l is an exact convex combination of the rounded weights.
-                    ls0 += __uint_as_float(w01 << 16);
-                    ls1 += __uint_as_float(w01 & 0xFFFF0000u);
-                    ls2 += __uint_as_float(w23 << 16);
-                    ls3 += __uint_as_float(w23 & 0xFFFF0000u);
+                    ls0 += p0 + p1;
+                    ls1 += p2 + p3;
+                    // lr sums the bf16-rounded weights that the P V product uses, so that
+                    // O = sum(P V) / lr is an exact convex combination of those weights.
+                    lr0 += __uint_as_float(w01 << 16) + __uint_as_float(w01 & 0xFFFF0000u);
+                    lr1 += __uint_as_float(w23 << 16) + __uint_as_float(w23 & 0xFFFF0000u);
                     pk[c / 2] = w01;
                     pk[c / 2 + 1] = w23;
                 }
                 tmem_st16(tP + 16u * cb, pk);
             }
-            l += (ls0 + ls1) + (ls2 + ls3);
+            l += ls0 + ls1;
+            lr += lr0 + lr1;
             // O still holds the sum up to block j-1 (the commit that signalled S for block j
             // also covers the P V product of block j-1).
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (ok && J[t] > 0) {
             if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
                 tc_fence_after();
-                const float inv_l = 1.0f / l;
+                const float inv_l = 1.0f / lr;
                 __nv_bfloat16* orow =
                     static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll 1

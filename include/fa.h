@@ -68,6 +68,16 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
            void* stream);
 
+/* One stage of fa_bwd, for callers that schedule or time the stages separately:
+ * stage 0 = preprocess (Delta and the base-2 LSE into the workspace), 1 = dK and dV,
+ * 2 = dQ.  Running stages 0, 1, 2 in order on one stream is exactly fa_bwd; stages 1 and 2
+ * read the workspace stage 0 wrote and may run in either order after it.  Arguments and
+ * errors as fa_bwd, plus FA_ERR_INVALID_ARG for another stage value.  bf16 only. */
+int fa_bwd_stage(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                 int stage, void* stream);
+
 /* Same as fa_fwd but forces an implementation: 0 = default dispatch, 1 = the portable SIMT
  * kernel (fp32 math; accepts bf16 or fp32 tensors).  For cross-checking the tensor-core
  * path on the device; the default path is what fa_fwd runs. */
