@@ -35,7 +35,7 @@ struct FwdCfg {
 };
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
