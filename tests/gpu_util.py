@@ -84,16 +84,19 @@ def check_grads(got: dict, ref: dict, dtype, what=""):
 
 
 def guarded_empty(shape, dtype, device="cuda", pad=4096):
-    """A tensor inside a larger buffer whose margins hold a NaN sentinel; returns
-    (view, check) where check() asserts that the margins are untouched."""
+    """A tensor inside a larger buffer whose margins hold a sentinel (NaN for floating
+    types, 0xAB for bytes); returns (view, check) where check() asserts that the margins
+    are untouched."""
     n = int(np.prod(shape))
-    buf = torch.full((n + 2 * pad,), float("nan"), dtype=dtype, device=device)
+    floating = dtype.is_floating_point
+    fill = float("nan") if floating else 0xAB
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device=device)
     view = buf[pad:pad + n].view(shape)
     view.zero_()
 
     def check():
-        head = buf[:pad].float().cpu()
-        tail = buf[pad + n:].float().cpu()
-        assert torch.isnan(head).all() and torch.isnan(tail).all(), "write outside the output"
+        for part in (buf[:pad].cpu(), buf[pad + n:].cpu()):
+            ok = torch.isnan(part.float()).all() if floating else (part == 0xAB).all()
+            assert ok, "write outside the output"
 
     return view, check
