@@ -20,6 +20,7 @@ STATUS = {
 # Every symbol include/fa.h declares (tests check the library exports all of them).
 EXPORTS = (
     "fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_stage", "fa_fwd_impl", "fa_bwd_impl",
+    "fa_bwd_noalloc",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_status_string", "fa_last_error",
     "fa_causal_block_counts", "fa_version",
 )
@@ -56,6 +57,8 @@ def load(path: str | None = None):
                                     sz, i, vp]
         lib.fa_bwd_stage.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp,
                                      sz, i, vp]
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_noalloc.restype = ctypes.c_int
         lib.fa_device_status.argtypes = [vp]
         lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.fa_set_wait_limit_ns.restype = None

@@ -326,3 +326,58 @@ int fa_causal_block_counts(int q_block, int Br, int Bc, int N, int* n_full, int*
 const char* fa_version(void) { return "fa-gb300 0.1 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// fa_bwd_noalloc: the backward with its scratch in a fixed device array of this library.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr long long kNoallocMaxRows = 1LL << 20;  // largest B*H*N accepted
+constexpr size_t kNoallocBytes = 2 * static_cast<size_t>(kNoallocMaxRows) * 4 + 256;
+
+// Delta and the base-2 LSE for up to kNoallocMaxRows rows, in the layout of fa_bwd's
+// workspace.  Every device that loads the library holds these 8 MiB until the process exits.
+static __device__ __align__(256) unsigned char g_bwd_scratch[kNoallocBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_dev_ptr[64] = {};
+
+// Device address of g_bwd_scratch on the current device, looked up once per device.  In host
+// code the symbol names a host-side shadow, not device memory, so it is never passed as is.
+int scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(FA_ERR_LAUNCH, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_dev_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+        if (e != cudaSuccess || ptr == nullptr)
+            return cuda_fail(e, "cudaGetSymbolAddress(backward scratch)");
+        g_scratch_dev_ptr[dev] = ptr;
+    }
+    *out = g_scratch_dev_ptr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal, int dtype,
+                              void* stream)
+{
+    int rc = check_common(B, H, N, d, scale, causal, dtype);
+    if (rc) return rc;
+    const long long rows = static_cast<long long>(B) * H * N;
+    if (rows > kNoallocMaxRows)
+        return fail(FA_ERR_TOO_LARGE, "fa_bwd_noalloc supports B*H*N <= " +
+                                          std::to_string(kNoallocMaxRows) + " rows (got " +
+                                          std::to_string(rows) + "); use fa_bwd with a workspace");
+    void* scratch = nullptr;
+    if ((rc = scratch_address(&scratch))) return rc;
+    return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                     scratch, kNoallocBytes, 0, -1, stream);
+}

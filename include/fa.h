@@ -90,6 +90,26 @@ int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, cons
                 float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
                 int impl, void* stream);
 
+/* Backward for callers that cannot allocate device memory.  This entry point has no
+ * counterpart on the pages; it exists for code that is not allowed to call cudaMalloc or any
+ * allocating routine, for example a plugin running inside a host framework that owns every
+ * byte of device memory, or a latency-critical loop that must not take the device-wide
+ * synchronisation an allocation can imply.  It computes exactly what fa_bwd computes, with
+ * the same arguments except the workspace: its scratch (Delta and the base-2 LSE) lives in a
+ * fixed 8 MiB array inside the library, which every GPU that loads the library holds until
+ * the process exits.
+ *   - Limit: B*H*N <= 1048576 rows (1 << 20); larger shapes return FA_ERR_TOO_LARGE and must
+ *     use fa_bwd with a workspace.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     once per device, with that device current); make that first call before any stream
+ *     capture.  The call allocates nothing.
+ *   - Every call shares the one array and overwrites all of it that it uses before reading
+ *     it, so nothing carries over between calls; calls that overlap on the GPU (for example
+ *     on two streams at once) race on the array and must be serialised by the caller. */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, int dtype, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word that bounded waits
  * inside the kernels write when they give up.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (the
  * wait site is appended to fa_last_error()) or FA_ERR_LAUNCH if the synchronisation failed. */
