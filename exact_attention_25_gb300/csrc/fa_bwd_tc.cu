@@ -9,14 +9,19 @@
 // One template serves both kernels.  With X, Y the resident tiles and A, B the streamed ones:
 //   dK/dV (KV = true):  X = K_j, Y = V_j, A = Q_i, B = dO_i
 //       T1 = X A^T = S^T, T2 = Y B^T = dP^T               (tcgen05, operands in smem)
-//       P^T = exp2(c S^T - L2), dS^T = P^T o (dP^T - Delta)  (elementwise warpgroup)
+//       P^T = exp2(c S^T - L2), dS^T = P^T o (dP^T - Delta)  (elementwise warpgroups)
 //       acc1 += P^T B = dV,  acc2 += dS^T A = dK / scale   (tcgen05, first operand in TMEM)
 //   dQ (KV = false):    X = Q_i, Y = dO_i, A = K_j, B = V_j
 //       T1 = S, T2 = dP, dS = P o (dP - Delta), acc2 += dS A = dQ / scale
-// Roles (6 warps): warps 0-3 elementwise + epilogue (thread = row of X = TMEM lane),
-// warp 4 TMA producer, warp 5 TMEM allocator + MMA issuer.
-// TMEM columns: T1 [0,128), T2 [128,256), acc1 [256,256+d), acc2 [256+d,256+2d); the bf16
-// operands P^T / dS^T are written over the first 64 columns of T1 / T2.
+// Roles (10 warps): two elementwise warpgroups (warps 0-3 and 4-7; thread = row of X = TMEM
+// lane), each owning one half (64 columns = 64 streamed rows) of T1/T2; warp 8 TMA producer;
+// warp 9 TMEM allocator + MMA issuer.  The products that read the bf16 operands from TMEM are
+// issued per half, as soon as that half's warpgroup is done, so one half's products overlap
+// the other half's elementwise work, and two warps per SM sub-partition hide each other's
+// TMEM-load and exp latency.
+// TMEM columns: T1 [0,128), T2 [128,256), acc1 [256,256+d), acc2 [256+d,256+2d).  Half h of
+// P^T / dS^T (bf16 pairs, 32 columns) is written over columns [64h, 64h+32) of T1 / T2, inside
+// the half's own fp32 columns, after the warpgroup has loaded them.
 #include "fa_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -24,16 +29,14 @@ namespace fa {
 
 template <int D>
 struct BwdCfg {
-    static constexpr int BR = 128;                 // rows of the resident block
-    static constexpr int BS = 128;                 // rows of a streamed block
     static constexpr int PANELS = D / 64;
     static constexpr int PANEL_BYTES = 128 * 128;
-    static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;  // 128 rows x D bf16
+    static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;      // 128 rows x D bf16
     static constexpr int STAGES = 2;
-    static constexpr int SMEM_RES = 2 * TILE_BYTES;           // X, Y
+    static constexpr int SMEM_RES = 2 * TILE_BYTES;              // X, Y
     static constexpr int SMEM_STREAM = STAGES * 2 * TILE_BYTES;  // (A, B) per stage
     static constexpr int SMEM_BYTES = SMEM_RES + SMEM_STREAM + 1024;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 320;
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -61,11 +64,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_full[C::STAGES];
     __shared__ __align__(8) uint64_t bar_empty[C::STAGES];
     __shared__ __align__(8) uint64_t bar_t;     // T1, T2 ready
-    __shared__ __align__(8) uint64_t bar_e;     // bf16 operands written by the elementwise WG
+    __shared__ __align__(8) uint64_t bar_e[2];  // half h of the bf16 operands written
     __shared__ __align__(8) uint64_t bar_acc;   // accumulators final
     __shared__ __align__(8) uint64_t bar_drain;
-    __shared__ float sL2[2][128];
-    __shared__ float sDl[2][128];
+    __shared__ __align__(16) float sL2[2][128];
+    __shared__ __align__(16) float sDl[2][128];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -102,17 +105,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mbar_init(&bar_empty[s], 1);
         }
         mbar_init(&bar_t, 1);
-        mbar_init(&bar_e, 128);
+        mbar_init(&bar_e[0], 128);
+        mbar_init(&bar_e[1], 128);
         mbar_init(&bar_acc, 1);
         mbar_init(&bar_drain, 1);
         abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_y);
         tma_prefetch_desc(&tm_a);
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------- TMA producer
         if (lane == 0) {
             mbar_arrive_expect_tx(&bar_res, 2 * C::TILE_BYTES);
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             for (int it = max(0, issued - C::STAGES); it < issued; ++it)
                 mbar_wait(&bar_full[it % C::STAGES], (it / C::STAGES) & 1, wd_drain, kSiteBwdDrain);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdT = idesc_bf16_f32(128, 128, 0, 0);  // T = X A^T
@@ -182,20 +186,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                            kIdT, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_t);
-                if (!mbar_wait(&bar_e, it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
-                tc_fence_after();
-                if (KV) {  // dV += P^T dO
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait(&bar_e[h], it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
+                    tc_fence_after();
+                    // half h: streamed rows [64h, 64h+64) = 4 k-steps of 16
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tAcc1, tT1 + 8u * ks,
-                               sdesc_sw128(sB + ks * 2048, C::PANEL_BYTES, 1024), kIdAcc,
-                               (it > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t acc = (it > 0 || h > 0 || ks > 0) ? 1u : 0u;
+                        const uint32_t brow = (4 * h + ks) * 2048;  // 16 rows x 128 B
+                        if (KV)  // dV += P^T dO
+                            mma_ts(tAcc1, tT1 + 64u * h + 8u * ks,
+                                   sdesc_sw128(sB + brow, C::PANEL_BYTES, 1024), kIdAcc, acc);
+                        // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
+                        mma_ts(tAcc2, tT2 + 64u * h + 8u * ks,
+                               sdesc_sw128(sA + brow, C::PANEL_BYTES, 1024), kIdAcc, acc);
+                    }
                 }
-                // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tAcc2, tT2 + 8u * ks, sdesc_sw128(sA + ks * 2048, C::PANEL_BYTES, 1024),
-                           kIdAcc, (it > 0 || ks > 0) ? 1u : 0u);
+                if (!ok) break;
                 mma_commit(&bar_empty[s]);
                 committed = it + 1;
             }
@@ -209,9 +216,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             if (ok) mbar_wait(&bar_acc, 0, wd_drain, kSiteBwdDrain);
         }
     } else {
-        // ------------------------------------------------------------- elementwise (warps 0-3)
-        const int r = threadIdx.x;  // row of the resident block = TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        // ------------------------------------------------------------- elementwise (warps 0-7)
+        const int h = warp >> 2;           // half of the streamed block this warpgroup owns
+        const int r = threadIdx.x & 127;   // row of the resident block = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tT1 = tbase + lane_base, tT2 = tbase + lane_base + 128u;
         const uint32_t tAcc1 = tbase + lane_base + 256u, tAcc2 = tbase + lane_base + 256u + D;
         const float c2 = p.scale_log2;
@@ -225,13 +233,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int sb = s_begin + it;
-            const int s0 = sb * 128;  // first row of the streamed block
-            if (KV) {  // stage L2 / Delta of the 128 query rows of this block
-                const int qi = s0 + r;
-                sL2[it & 1][r] = (qi < N) ? p.lse2[row_base + qi] : INFINITY;
-                sDl[it & 1][r] = (qi < N) ? p.delta[row_base + qi] : 0.0f;
-                named_bar_sync(1, 128);
+            const int s0 = (s_begin + it) * 128;  // first row of the streamed block
+            if (KV) {  // stage L2 / Delta of this half's 64 query rows
+                if (r < 64) {
+                    const int qi = s0 + 64 * h + r;
+                    sL2[it & 1][64 * h + r] = (qi < N) ? p.lse2[row_base + qi] : INFINITY;
+                    sDl[it & 1][64 * h + r] = (qi < N) ? p.delta[row_base + qi] : 0.0f;
+                }
+                named_bar_sync(1 + h, 128);
             }
             if (!warp_wait_all(&bar_t, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
@@ -241,10 +250,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                                                 KV ? x0 : s0, KV ? x1 : min(N, s0 + 128)) == kTileMasked;
             const bool tail = !KV && (s0 + 128 > N);
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
+                const int col0 = 64 * h + 32 * ch;
                 uint32_t sv[32], dpv[32];
-                tmem_ld32(tT1 + 32u * ch, sv);
-                tmem_ld32(tT2 + 32u * ch, dpv);
+                tmem_ld32(tT1 + col0, sv);
+                tmem_ld32(tT2 + col0, dpv);
                 tmem_wait_ld();
                 reg_fence32(sv);
                 reg_fence32(dpv);
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     float pr[2], ds[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int col = 32 * ch + e + u;
+                        const int col = col0 + e + u;
                         const float L2 = KV ? sL2[it & 1][col] : L2_self;
                         const float Dl = KV ? sDl[it & 1][col] : D_self;
                         float pv = ex2(fmaf(__uint_as_float(sv[e + u]), c2, -L2));
@@ -269,14 +279,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     pkP[e / 2] = pack_bf16x2(pr[0], pr[1]);
                     pkS[e / 2] = pack_bf16x2(ds[0], ds[1]);
                 }
-                if (KV) tmem_st16(tT1 + 16u * ch, pkP);
-                tmem_st16(tT2 + 16u * ch, pkS);
+                // columns [64h + 16ch, 64h + 16ch + 16): already loaded by this warpgroup
+                if (KV) tmem_st16(tT1 + 64u * h + 16u * ch, pkP);
+                tmem_st16(tT2 + 64u * h + 16u * ch, pkS);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bar_e);
+            mbar_arrive(&bar_e[h]);
         }
         // ------------------------------------------------------------- epilogue
+        // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
         if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
             tc_fence_after();
             __nv_bfloat16* out2 = static_cast<__nv_bfloat16*>(KV ? p.dk : p.dq);
@@ -287,9 +299,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 const float mul = which == 0 ? 1.0f : p.scale;
                 __nv_bfloat16* dst_row = (which == 0 ? out1 : out2) + (row_base + xrow) * D;
 #pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    const int c0 = h * (D / 2) + 32 * ch;
                     uint32_t a[32];
-                    tmem_ld32(tAcc + 32u * ch, a);
+                    tmem_ld32(tAcc + c0, a);
                     tmem_wait_ld();
                     reg_fence32(a);
                     uint32_t packed[16];
@@ -298,7 +311,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                         packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
                                                 __uint_as_float(a[2 * c + 1]) * mul);
                     if (xrow < N) {
-                        uint4* dst = reinterpret_cast<uint4*>(dst_row + ch * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
                             dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
@@ -310,16 +323,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             // a block that no streamed block touches has zero gradient (cannot occur for
             // square causal attention, kept for completeness)
             __nv_bfloat16* out2 = static_cast<__nv_bfloat16*>(KV ? p.dk : p.dq);
-            for (int c = 0; c < D; ++c) out2[(row_base + xrow) * D + c] = __float2bfloat16_rn(0.0f);
-            if (KV)
-                for (int c = 0; c < D; ++c)
-                    static_cast<__nv_bfloat16*>(p.dv)[(row_base + xrow) * D + c] = __float2bfloat16_rn(0.0f);
+            for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c) {
+                out2[(row_base + xrow) * D + c] = __float2bfloat16_rn(0.0f);
+                if (KV) static_cast<__nv_bfloat16*>(p.dv)[(row_base + xrow) * D + c] = __float2bfloat16_rn(0.0f);
+            }
         }
         tc_fence_before();
     }
 
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);
     }
