@@ -14,14 +14,19 @@
 //   dQ (KV = false):    X = Q_i, Y = dO_i, A = K_j, B = V_j
 //       T1 = S, T2 = dP, dS = P o (dP - Delta), acc2 += dS A = dQ / scale
 // Roles (10 warps): two elementwise warpgroups (warps 0-3 and 4-7; thread = row of X = TMEM
-// lane), each owning one half (64 columns = 64 streamed rows) of T1/T2; warp 8 TMA producer;
-// warp 9 TMEM allocator + MMA issuer.  The products that read the bf16 operands from TMEM are
-// issued per half, as soon as that half's warpgroup is done, so one half's products overlap
-// the other half's elementwise work, and two warps per SM sub-partition hide each other's
-// TMEM-load and exp latency.
-// TMEM columns: T1 [0,128), T2 [128,256), acc1 [256,256+d), acc2 [256+d,256+2d).  Half h of
-// P^T / dS^T (bf16 pairs, 32 columns) is written over columns [64h, 64h+32) of T1 / T2, inside
-// the half's own fp32 columns, after the warpgroup has loaded them.
+// lane), warpgroup h owning half h (streamed rows [64h, 64h+64)) of every block; warp 8 TMA
+// producer; warp 9 TMEM allocator + MMA issuer.
+// Pipeline: the T1/T2 products are issued per half (N = 64), and half h of block i+1 is issued
+// right after the accumulating products of half h of block i.  The tensor pipe therefore
+// always has the other half's products queued while a warpgroup runs its elementwise pass:
+//   TC:  acc(i,0) | T(i+1,0) | acc(i,1) | T(i+1,1) | acc(i+1,0) | ...
+//   WG0:             elementwise(i+1, 0) .........|
+//   WG1:                        elementwise(i+1, 1) ..........|
+// TMEM columns: half h: T1 [128h, 128h+64), T2 [128h+64, 128h+128); acc1 [256, 256+d),
+// acc2 [256+d, 256+2d).  The bf16 P^T / dS^T of half h (32 columns of packed pairs) overwrite
+// the first 32 columns of that half's T1 / T2, chunk by chunk, after they were loaded.
+#include <type_traits>
+
 #include "fa_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -63,12 +68,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_res;
     __shared__ __align__(8) uint64_t bar_full[C::STAGES];
     __shared__ __align__(8) uint64_t bar_empty[C::STAGES];
-    __shared__ __align__(8) uint64_t bar_t;     // T1, T2 ready
+    __shared__ __align__(8) uint64_t bar_t[2];  // half h of T1, T2 ready
     __shared__ __align__(8) uint64_t bar_e[2];  // half h of the bf16 operands written
     __shared__ __align__(8) uint64_t bar_acc;   // accumulators final
     __shared__ __align__(8) uint64_t bar_drain;
-    __shared__ __align__(16) float sL2[2][128];
-    __shared__ __align__(16) float sDl[2][128];
+    __shared__ __align__(16) float sL2[2][2][64];  // -L2 per streamed row [half][parity][row]
+    __shared__ __align__(16) float sDl[2][2][64];  // -Delta per streamed row
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -104,9 +109,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
         }
-        mbar_init(&bar_t, 1);
-        mbar_init(&bar_e[0], 128);
-        mbar_init(&bar_e[1], 128);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bar_t[h], 1);
+            mbar_init(&bar_e[h], 4);  // one elected arrive per warp of the warpgroup
+        }
         mbar_init(&bar_acc, 1);
         mbar_init(&bar_drain, 1);
         abort_flag = 0;
@@ -160,51 +166,82 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdT = idesc_bf16_f32(128, 128, 0, 0);  // T = X A^T
+            constexpr uint32_t kIdT = idesc_bf16_f32(128, 64, 0, 0);   // T_h = X A_h^T
             constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);  // acc += (TMEM) * (MN-major)
             const uint32_t sXa = smem_u32(sX), sYa = smem_u32(sY), sABa = smem_u32(sAB);
-            const uint32_t tT1 = tbase, tT2 = tbase + 128u;
             const uint32_t tAcc1 = tbase + 256u, tAcc2 = tbase + 256u + D;
+
+            // T1, T2 of half h of streamed block `it` (streamed rows [64h, 64h+64)).
+            auto issue_t = [&](int it, int h) {
+                const int s = it % C::STAGES;
+                const uint32_t sA = sABa + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
+                const uint32_t tT1 = tbase + 128u * h, tT2 = tT1 + 64u;
+                const uint32_t hrow = 64u * 128u * h;  // 64 rows of 128 B into every panel
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
+                    mma_ss(tT1, sdesc_sw128(sXa + off, 16, 1024),
+                           sdesc_sw128(sA + off + hrow, 16, 1024), kIdT, ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
+                    mma_ss(tT2, sdesc_sw128(sYa + off, 16, 1024),
+                           sdesc_sw128(sB + off + hrow, 16, 1024), kIdT, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_t[h]);
+            };
+            // Accumulating products of half h of streamed block `it` (4 k-steps of 16 rows).
+            auto issue_acc = [&](int it, int h) {
+                const int s = it % C::STAGES;
+                const uint32_t sA = sABa + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
+                const uint32_t tT1 = tbase + 128u * h, tT2 = tT1 + 64u;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t acc = (it > 0 || h > 0 || ks > 0) ? 1u : 0u;
+                    const uint32_t brow = (4 * h + ks) * 2048;  // 16 rows x 128 B
+                    if (KV)  // dV += P^T dO
+                        mma_ts(tAcc1, tT1 + 8u * ks, sdesc_sw128(sB + brow, C::PANEL_BYTES, 1024),
+                               kIdAcc, acc);
+                    // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
+                    mma_ts(tAcc2, tT2 + 8u * ks, sdesc_sw128(sA + brow, C::PANEL_BYTES, 1024),
+                           kIdAcc, acc);
+                }
+            };
+
             bool ok = mbar_wait(&bar_res, 0, wd, kSiteBwdMmaKV);
             int committed = 0;
+            if (ok && n_it > 0) {
+                ok = mbar_wait(&bar_full[0], 0, wd, kSiteBwdMmaQ);
+                if (ok) {
+                    tc_fence_after();
+                    issue_t(0, 0);
+                    issue_t(0, 1);
+                }
+            }
             for (int it = 0; ok && it < n_it; ++it) {
-                const int s = it % C::STAGES;
-                const uint32_t ph = (it / C::STAGES) & 1;
-                if (!mbar_wait(&bar_full[s], ph, wd, kSiteBwdMmaQ)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t sA = sABa + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(tT1, sdesc_sw128(sXa + off, 16, 1024), sdesc_sw128(sA + off, 16, 1024),
-                           kIdT, ks > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(tT2, sdesc_sw128(sYa + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
-                           kIdT, ks > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_t);
+                const bool more = it + 1 < n_it;
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait(&bar_e[h], it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
                     tc_fence_after();
-                    // half h: streamed rows [64h, 64h+64) = 4 k-steps of 16
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint32_t acc = (it > 0 || h > 0 || ks > 0) ? 1u : 0u;
-                        const uint32_t brow = (4 * h + ks) * 2048;  // 16 rows x 128 B
-                        if (KV)  // dV += P^T dO
-                            mma_ts(tAcc1, tT1 + 64u * h + 8u * ks,
-                                   sdesc_sw128(sB + brow, C::PANEL_BYTES, 1024), kIdAcc, acc);
-                        // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
-                        mma_ts(tAcc2, tT2 + 64u * h + 8u * ks,
-                               sdesc_sw128(sA + brow, C::PANEL_BYTES, 1024), kIdAcc, acc);
+                    issue_acc(it, h);
+                    if (h == 1) {
+                        mma_commit(&bar_empty[it % C::STAGES]);
+                        committed = it + 1;
+                    }
+                    if (more) {
+                        if (h == 0) {
+                            const int s1 = (it + 1) % C::STAGES;
+                            if (!mbar_wait(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd, kSiteBwdMmaQ)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        // half h of T is free: its readers (issue_acc above) precede in issue order
+                        issue_t(it + 1, h);
                     }
                 }
-                if (!ok) break;
-                mma_commit(&bar_empty[s]);
-                committed = it + 1;
             }
             if (ok) mma_commit(&bar_acc);
             volatile int no_abort = 0;
@@ -220,7 +257,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int h = warp >> 2;           // half of the streamed block this warpgroup owns
         const int r = threadIdx.x & 127;   // row of the resident block = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tT1 = tbase + lane_base, tT2 = tbase + lane_base + 128u;
+        const uint32_t tT1 = tbase + lane_base + 128u * h, tT2 = tT1 + 64u;
         const uint32_t tAcc1 = tbase + lane_base + 256u, tAcc2 = tbase + lane_base + 256u + D;
         const float c2 = p.scale_log2;
         const size_t row_base = static_cast<size_t>(bh) * N;
@@ -235,14 +272,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int it = 0; it < n_it; ++it) {
             const int s0 = (s_begin + it) * 128;  // first row of the streamed block
             if (KV) {  // stage L2 / Delta of this half's 64 query rows
-                if (r < 64) {
+                if (r < 64) {  // stored negated, so the pass below is fma / add only
                     const int qi = s0 + 64 * h + r;
-                    sL2[it & 1][64 * h + r] = (qi < N) ? p.lse2[row_base + qi] : INFINITY;
-                    sDl[it & 1][64 * h + r] = (qi < N) ? p.delta[row_base + qi] : 0.0f;
+                    sL2[h][it & 1][r] = (qi < N) ? -p.lse2[row_base + qi] : -INFINITY;
+                    sDl[h][it & 1][r] = (qi < N) ? -p.delta[row_base + qi] : 0.0f;
                 }
                 named_bar_sync(1 + h, 128);
             }
-            if (!warp_wait_all(&bar_t, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
+            if (!warp_wait_all(&bar_t[h], it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
             // element-wise mask: causal diagonal block, and (dQ kernel) keys beyond N
             const bool diag = p.causal &&
@@ -251,41 +288,69 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             const bool tail = !KV && (s0 + 128 > N);
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {
-                const int col0 = 64 * h + 32 * ch;
+                const int col0 = 64 * h + 32 * ch;  // streamed row of the first column
                 uint32_t sv[32], dpv[32];
-                tmem_ld32(tT1 + col0, sv);
-                tmem_ld32(tT2 + col0, dpv);
+                tmem_ld32(tT1 + 32u * ch, sv);
+                tmem_ld32(tT2 + 32u * ch, dpv);
                 tmem_wait_ld();
                 reg_fence32(sv);
                 reg_fence32(dpv);
                 uint32_t pkP[16], pkS[16];
+                const uint64_t c2x2 = f2_make(c2, c2);
+                const float* nl2 = KV ? &sL2[h][it & 1][32 * ch] : nullptr;
+                const float* ndl = KV ? &sDl[h][it & 1][32 * ch] : nullptr;
+                auto pass = [&](auto mask_tag) {
+                constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pr[2], ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = col0 + e + u;
-                        const float L2 = KV ? sL2[it & 1][col] : L2_self;
-                        const float Dl = KV ? sDl[it & 1][col] : D_self;
-                        float pv = ex2(fmaf(__uint_as_float(sv[e + u]), c2, -L2));
-                        if (diag || tail) {
-                            const int key = KV ? xrow : s0 + col;
-                            const int qry = KV ? s0 + col : xrow;
-                            if ((diag && key > qry) || (tail && key >= N)) pv = 0.0f;
-                        }
-                        pr[u] = pv;
-                        ds[u] = pv * (__uint_as_float(dpv[e + u]) - Dl);
+                for (int e = 0; e < 32; e += 4) {
+                    // per-column (dK/dV) or per-row (dQ) statistics for 4 columns
+                    float4 nl, nd;
+                    if (KV) {
+                        nl = *reinterpret_cast<const float4*>(nl2 + e);
+                        nd = *reinterpret_cast<const float4*>(ndl + e);
+                    } else {
+                        nl = make_float4(-L2_self, -L2_self, -L2_self, -L2_self);
+                        nd = make_float4(-D_self, -D_self, -D_self, -D_self);
                     }
-                    pkP[e / 2] = pack_bf16x2(pr[0], pr[1]);
-                    pkS[e / 2] = pack_bf16x2(ds[0], ds[1]);
+#pragma unroll
+                    for (int u = 0; u < 4; u += 2) {
+                        const float nla = u ? nl.z : nl.x, nlb = u ? nl.w : nl.y;
+                        const float nda = u ? nd.z : nd.x, ndb = u ? nd.w : nd.y;
+                        const uint64_t x2 =
+                            f2_fma(f2_make(__uint_as_float(sv[e + u]), __uint_as_float(sv[e + u + 1])),
+                                   c2x2, f2_make(nla, nlb));
+                        float xa, xb;
+                        f2_split(x2, xa, xb);
+                        float pa = ex2(xa), pb = ex2(xb);
+                        if (MASK) {
+                            const int col = col0 + e + u;
+                            const int keya = KV ? xrow : s0 + col, qrya = KV ? s0 + col : xrow;
+                            const int keyb = KV ? xrow : s0 + col + 1, qryb = KV ? s0 + col + 1 : xrow;
+                            if ((diag && keya > qrya) || (tail && keya >= N)) pa = 0.0f;
+                            if ((diag && keyb > qryb) || (tail && keyb >= N)) pb = 0.0f;
+                        }
+                        const uint64_t t2 = f2_add(
+                            f2_make(__uint_as_float(dpv[e + u]), __uint_as_float(dpv[e + u + 1])),
+                            f2_make(nda, ndb));
+                        float da, db;
+                        f2_split(f2_mul(f2_make(pa, pb), t2), da, db);
+                        pkP[(e + u) / 2] = pack_bf16x2(pa, pb);
+                        pkS[(e + u) / 2] = pack_bf16x2(da, db);
+                    }
                 }
-                // columns [64h + 16ch, 64h + 16ch + 16): already loaded by this warpgroup
-                if (KV) tmem_st16(tT1 + 64u * h + 16u * ch, pkP);
-                tmem_st16(tT2 + 64u * h + 16u * ch, pkS);
+                };
+                if (diag || tail)
+                    pass(std::true_type{});
+                else
+                    pass(std::false_type{});
+                // columns [16ch, 16ch + 16) of this half: loaded already (chunk 0 is 0..31)
+                if (KV) tmem_st16(tT1 + 16u * ch, pkP);
+                tmem_st16(tT2 + 16u * ch, pkS);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bar_e[h]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_e[h]);
         }
         // ------------------------------------------------------------- epilogue
         // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.

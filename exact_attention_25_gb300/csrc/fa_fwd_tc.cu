@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         for (int t = 0; t < C::NT; ++t) {
             mbar_init(&bar_sfull[t], 1);
-            mbar_init(&bar_pfull[t], C::BM);
+            mbar_init(&bar_pfull[t], 4);  // one elected arrive per softmax warp
             mbar_init(&bar_ofinal[t], 1);
         }
         mbar_init(&bar_drain, 1);
@@ -341,7 +341,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bar_pfull[t]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_pfull[t]);
         }
         // ------------------------------------------------------------- epilogue
         if (ok && J[t] > 0) {
