@@ -15,16 +15,14 @@
 //       T1 = S, T2 = dP, dS = P o (dP - Delta), acc2 += dS A = dQ / scale
 // Roles (10 warps): two elementwise warpgroups (warps 0-3 and 4-7; thread = row of X = TMEM
 // lane), warpgroup h owning half h (streamed rows [64h, 64h+64)) of every block; warp 8 TMA
-// producer; warp 9 TMEM allocator + MMA issuer.
-// Pipeline: the T1/T2 products are issued per half (N = 64), and half h of block i+1 is issued
-// right after the accumulating products of half h of block i.  The tensor pipe therefore
-// always has the other half's products queued while a warpgroup runs its elementwise pass:
-//   TC:  acc(i,0) | T(i+1,0) | acc(i,1) | T(i+1,1) | acc(i+1,0) | ...
-//   WG0:             elementwise(i+1, 0) .........|
-//   WG1:                        elementwise(i+1, 1) ..........|
-// TMEM columns: half h: T1 [128h, 128h+64), T2 [128h+64, 128h+128); acc1 [256, 256+d),
-// acc2 [256+d, 256+2d).  The bf16 P^T / dS^T of half h (32 columns of packed pairs) overwrite
-// the first 32 columns of that half's T1 / T2, chunk by chunk, after they were loaded.
+// producer; warp 9 TMEM allocator + MMA issuer.  Per streamed block the MMA warp issues the
+// T products (N = 128), waits for each half's elementwise pass and issues that half's
+// accumulating products, then issues the next block's T products.  Shared-memory descriptors
+// are built once per stage and only advanced per MMA, so one thread issues at tensor-core
+// speed.
+// TMEM columns: T1 [0,128), T2 [128,256), acc1 [256,256+d), acc2 [256+d,256+2d).  The bf16
+// P^T / dS^T of half h (32 columns of packed pairs) overwrite columns [64h, 64h+32) of T1 /
+// T2, chunk by chunk, after the warpgroup loaded them.
 #include <type_traits>
 
 #include "fa_common.cuh"
@@ -166,46 +164,53 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdT = idesc_bf16_f32(128, 64, 0, 0);   // T_h = X A_h^T
+            constexpr uint32_t kIdT = idesc_bf16_f32(128, 128, 0, 0);  // T = X A^T
             constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);  // acc += (TMEM) * (MN-major)
-            const uint32_t sXa = smem_u32(sX), sYa = smem_u32(sY), sABa = smem_u32(sAB);
+            const uint32_t tT1 = tbase, tT2 = tbase + 128u;
             const uint32_t tAcc1 = tbase + 256u, tAcc2 = tbase + 256u + D;
+            // Descriptors are built once; each MMA only advances the start address by a
+            // compile-time byte offset (keeps the single issuing thread off the critical path).
+            const uint64_t dX = sdesc_sw128(smem_u32(sX), 16, 1024);
+            const uint64_t dY = sdesc_sw128(smem_u32(sY), 16, 1024);
+            uint64_t dA[C::STAGES], dB[C::STAGES], mA[C::STAGES], mB[C::STAGES];
+#pragma unroll
+            for (int s = 0; s < C::STAGES; ++s) {
+                const uint32_t sA = smem_u32(sAB) + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
+                dA[s] = sdesc_sw128(sA, 16, 1024);              // K-major (T products)
+                dB[s] = sdesc_sw128(sB, 16, 1024);
+                mA[s] = sdesc_sw128(sA, C::PANEL_BYTES, 1024);  // MN-major (accumulating products)
+                mB[s] = sdesc_sw128(sB, C::PANEL_BYTES, 1024);
+            }
 
-            // T1, T2 of half h of streamed block `it` (streamed rows [64h, 64h+64)).
-            auto issue_t = [&](int it, int h) {
+            // T1 = X A^T and T2 = Y B^T of streamed block `it` (N = 128).
+            auto issue_t = [&](int it) {
                 const int s = it % C::STAGES;
-                const uint32_t sA = sABa + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
-                const uint32_t tT1 = tbase + 128u * h, tT2 = tT1 + 64u;
-                const uint32_t hrow = 64u * 128u * h;  // 64 rows of 128 B into every panel
+                const uint64_t a = s ? dA[1] : dA[0], b = s ? dB[1] : dB[0];
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(tT1, sdesc_sw128(sXa + off, 16, 1024),
-                           sdesc_sw128(sA + off + hrow, 16, 1024), kIdT, ks > 0 ? 1u : 0u);
+                    mma_ss(tT1, sdesc_adv(dX, off), sdesc_adv(a, off), kIdT, ks > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(tT2, sdesc_sw128(sYa + off, 16, 1024),
-                           sdesc_sw128(sB + off + hrow, 16, 1024), kIdT, ks > 0 ? 1u : 0u);
+                    mma_ss(tT2, sdesc_adv(dY, off), sdesc_adv(b, off), kIdT, ks > 0 ? 1u : 0u);
                 }
-                mma_commit(&bar_t[h]);
+                mma_commit(&bar_t[0]);
+                mma_commit(&bar_t[1]);
             };
             // Accumulating products of half h of streamed block `it` (4 k-steps of 16 rows).
             auto issue_acc = [&](int it, int h) {
                 const int s = it % C::STAGES;
-                const uint32_t sA = sABa + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
-                const uint32_t tT1 = tbase + 128u * h, tT2 = tT1 + 64u;
+                const uint64_t a = s ? mA[1] : mA[0], b = s ? mB[1] : mB[0];
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t acc = (it > 0 || h > 0 || ks > 0) ? 1u : 0u;
                     const uint32_t brow = (4 * h + ks) * 2048;  // 16 rows x 128 B
                     if (KV)  // dV += P^T dO
-                        mma_ts(tAcc1, tT1 + 8u * ks, sdesc_sw128(sB + brow, C::PANEL_BYTES, 1024),
-                               kIdAcc, acc);
+                        mma_ts(tAcc1, tT1 + 64u * h + 8u * ks, sdesc_adv(b, brow), kIdAcc, acc);
                     // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
-                    mma_ts(tAcc2, tT2 + 8u * ks, sdesc_sw128(sA + brow, C::PANEL_BYTES, 1024),
-                           kIdAcc, acc);
+                    mma_ts(tAcc2, tT2 + 64u * h + 8u * ks, sdesc_adv(a, brow), kIdAcc, acc);
                 }
             };
 
@@ -215,32 +220,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 ok = mbar_wait(&bar_full[0], 0, wd, kSiteBwdMmaQ);
                 if (ok) {
                     tc_fence_after();
-                    issue_t(0, 0);
-                    issue_t(0, 1);
+                    issue_t(0);
                 }
             }
             for (int it = 0; ok && it < n_it; ++it) {
-                const bool more = it + 1 < n_it;
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait(&bar_e[h], it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
                     tc_fence_after();
                     issue_acc(it, h);
-                    if (h == 1) {
-                        mma_commit(&bar_empty[it % C::STAGES]);
-                        committed = it + 1;
+                }
+                if (!ok) break;
+                mma_commit(&bar_empty[it % C::STAGES]);
+                committed = it + 1;
+                if (it + 1 < n_it) {
+                    const int s1 = (it + 1) % C::STAGES;
+                    if (!mbar_wait(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd, kSiteBwdMmaQ)) {
+                        ok = false;
+                        break;
                     }
-                    if (more) {
-                        if (h == 0) {
-                            const int s1 = (it + 1) % C::STAGES;
-                            if (!mbar_wait(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd, kSiteBwdMmaQ)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        // half h of T is free: its readers (issue_acc above) precede in issue order
-                        issue_t(it + 1, h);
-                    }
+                    tc_fence_after();
+                    // T1/T2 are free: their readers (issue_acc above) precede in issue order
+                    issue_t(it + 1);
                 }
             }
             if (ok) mma_commit(&bar_acc);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int h = warp >> 2;           // half of the streamed block this warpgroup owns
         const int r = threadIdx.x & 127;   // row of the resident block = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tT1 = tbase + lane_base + 128u * h, tT2 = tT1 + 64u;
+        const uint32_t tT1 = tbase + lane_base + 64u * h, tT2 = tT1 + 128u;
         const uint32_t tAcc1 = tbase + lane_base + 256u, tAcc2 = tbase + lane_base + 256u + D;
         const float c2 = p.scale_log2;
         const size_t row_base = static_cast<size_t>(bh) * N;
@@ -286,29 +286,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                               causal_tile_class(KV ? s0 : x0, KV ? min(N, s0 + 128) : x1,
                                                 KV ? x0 : s0, KV ? x1 : min(N, s0 + 128)) == kTileMasked;
             const bool tail = !KV && (s0 + 128 > N);
-#pragma unroll 1
-            for (int ch = 0; ch < 2; ++ch) {
-                const int col0 = 64 * h + 32 * ch;  // streamed row of the first column
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(tT1 + 32u * ch, sv);
-                tmem_ld32(tT2 + 32u * ch, dpv);
-                tmem_wait_ld();
-                reg_fence32(sv);
-                reg_fence32(dpv);
-                uint32_t pkP[16], pkS[16];
-                const uint64_t c2x2 = f2_make(c2, c2);
-                const float* nl2 = KV ? &sL2[h][it & 1][32 * ch] : nullptr;
-                const float* ndl = KV ? &sDl[h][it & 1][32 * ch] : nullptr;
-                auto pass = [&](auto mask_tag) {
+            // 64 columns in 4 chunks of 16, software-pipelined: the TMEM load of chunk c+1 is
+            // in flight while chunk c is computed and stored.  bf16 results of chunk c go to
+            // columns [8c, 8c+8), which chunks 0..c have already loaded.
+            const uint64_t c2x2 = f2_make(c2, c2);
+            auto chunk = [&](auto mask_tag, int c, const uint32_t* sv, const uint32_t* dpv) {
                 constexpr bool MASK = decltype(mask_tag)::value;
+                uint32_t pkP[8], pkS[8];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    // per-column (dK/dV) or per-row (dQ) statistics for 4 columns
+                for (int e = 0; e < 16; e += 4) {
                     float4 nl, nd;
-                    if (KV) {
-                        nl = *reinterpret_cast<const float4*>(nl2 + e);
-                        nd = *reinterpret_cast<const float4*>(ndl + e);
-                    } else {
+                    if (KV) {  // per-column statistics (negated) for 4 columns
+                        nl = *reinterpret_cast<const float4*>(&sL2[h][it & 1][16 * c + e]);
+                        nd = *reinterpret_cast<const float4*>(&sDl[h][it & 1][16 * c + e]);
+                    } else {   // per-row statistics of this thread's query row
                         nl = make_float4(-L2_self, -L2_self, -L2_self, -L2_self);
                         nd = make_float4(-D_self, -D_self, -D_self, -D_self);
                     }
@@ -323,7 +314,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                         f2_split(x2, xa, xb);
                         float pa = ex2(xa), pb = ex2(xb);
                         if (MASK) {
-                            const int col = col0 + e + u;
+                            const int col = 64 * h + 16 * c + e + u;  // streamed row offset
                             const int keya = KV ? xrow : s0 + col, qrya = KV ? s0 + col : xrow;
                             const int keyb = KV ? xrow : s0 + col + 1, qryb = KV ? s0 + col + 1 : xrow;
                             if ((diag && keya > qrya) || (tail && keya >= N)) pa = 0.0f;
@@ -338,15 +329,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                         pkS[(e + u) / 2] = pack_bf16x2(da, db);
                     }
                 }
-                };
-                if (diag || tail)
-                    pass(std::true_type{});
-                else
-                    pass(std::false_type{});
-                // columns [16ch, 16ch + 16) of this half: loaded already (chunk 0 is 0..31)
-                if (KV) tmem_st16(tT1 + 16u * ch, pkP);
-                tmem_st16(tT2 + 16u * ch, pkS);
-            }
+                if (KV) tmem_st8(tT1 + 8u * c, pkP);
+                tmem_st8(tT2 + 8u * c, pkS);
+            };
+            auto half_pass = [&](auto mask_tag) {
+                uint32_t s0v[16], d0v[16], s1v[16], d1v[16];
+                tmem_ld16(tT1, s0v);
+                tmem_ld16(tT2, d0v);
+                tmem_wait_ld();
+                reg_fence16(s0v);
+                reg_fence16(d0v);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t* cs = (c & 1) ? s1v : s0v;
+                    uint32_t* cd = (c & 1) ? d1v : d0v;
+                    uint32_t* ns = (c & 1) ? s0v : s1v;
+                    uint32_t* nd = (c & 1) ? d0v : d1v;
+                    if (c + 1 < 4) {
+                        tmem_ld16(tT1 + 16u * (c + 1), ns);
+                        tmem_ld16(tT2 + 16u * (c + 1), nd);
+                    }
+                    chunk(mask_tag, c, cs, cd);
+                    if (c + 1 < 4) {
+                        tmem_wait_ld();
+                        reg_fence16(ns);
+                        reg_fence16(nd);
+                    }
+                }
+            };
+            if (diag || tail)
+                half_pass(std::true_type{});
+            else
+                half_pass(std::false_type{});
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();

@@ -161,27 +161,40 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, C::BN, 0, 0);  // S = Q K^T
             constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);     // O += P V
-            const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+            // Descriptors are built once; each MMA only advances the start address by a
+            // compile-time byte offset (keeps the single issuing thread off the critical path).
+            uint64_t dQd[C::NT], dK[C::STAGES], dV[C::STAGES];
+#pragma unroll
+            for (int t = 0; t < C::NT; ++t) dQd[t] = sdesc_sw128(smem_u32(sQ) + t * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+            for (int s = 0; s < C::STAGES; ++s) {
+                dK[s] = sdesc_sw128(smem_u32(sK) + s * C::TILE_BYTES, 16, 1024);
+                dV[s] = sdesc_sw128(smem_u32(sV) + s * C::TILE_BYTES, C::PANEL_BYTES, 1024);
+            }
+            auto pick = [](const uint64_t* arr, int i) {
+                uint64_t r = arr[0];
+#pragma unroll
+                for (int k = 1; k < C::STAGES; ++k) r = (i == k) ? arr[k] : r;
+                return r;
+            };
 
             auto issue_s = [&](int t, int s) {
                 const uint32_t d_tmem = tbase + 128u * t;
+                const uint64_t a0 = t ? dQd[1] : dQd[0], b0 = pick(dK, s);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    const uint64_t a = sdesc_sw128(sQa + t * C::TILE_BYTES + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sKa + s * C::TILE_BYTES + off, 16, 1024);
-                    mma_ss(d_tmem, a, b, kIdS, ks > 0 ? 1u : 0u);
+                    mma_ss(d_tmem, sdesc_adv(a0, off), sdesc_adv(b0, off), kIdS, ks > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int s, bool accumulate) {
                 const uint32_t d_tmem = tbase + 256u + static_cast<uint32_t>(t * D);
                 const uint32_t p_tmem = tbase + 128u * t + 64u;
+                const uint64_t b0 = pick(dV, s);
 #pragma unroll
-                for (int ks = 0; ks < C::BN / 16; ++ks) {
-                    const uint64_t b =
-                        sdesc_sw128(sVa + s * C::TILE_BYTES + ks * 2048, C::PANEL_BYTES, 1024);
-                    mma_ts(d_tmem, p_tmem + 8u * ks, b, kIdPV, (accumulate || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < C::BN / 16; ++ks)
+                    mma_ts(d_tmem, p_tmem + 8u * ks, sdesc_adv(b0, ks * 2048), kIdPV,
+                           (accumulate || ks > 0) ? 1u : 0u);
             };
 
             bool ok = mbar_wait(&bar_q, 0, wd, kSiteFwdMmaQ);

@@ -174,6 +174,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Advance a shared-memory descriptor by `bytes` (a multiple of 16): only the 14-bit start
+// address field changes, and it cannot carry because shared addresses stay below 256 KB.
+__device__ __forceinline__ uint64_t sdesc_adv(uint64_t d, uint32_t bytes)
+{
+    const uint32_t lo = static_cast<uint32_t>(d) + (bytes >> 4);
+    return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
 //   [4,6) D format (1 = f32)  [7,10) A format (1 = bf16)  [10,13) B format (1 = bf16)
 //   15 A major (0 = K-major, 1 = MN-major)  16 B major  [17,23) N >> 3  [24,29) M >> 4
@@ -297,6 +305,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r)
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
         : "memory");
 }
 
