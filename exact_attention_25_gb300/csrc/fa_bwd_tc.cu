@@ -48,6 +48,34 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// T = X A^T for one 128-row streamed tile: D/16 k-steps of 16 (N = 128), first overwrites.
+template <int D, int PANEL>
+__device__ __forceinline__ void bwd_issue_t(uint32_t d_tmem, uint64_t xdesc, uint64_t adesc,
+                                            uint32_t idesc)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks / 4) * PANEL + (ks % 4) * 32;
+        mma_ss(d_tmem, sdesc_adv(xdesc, off), sdesc_adv(adesc, off), idesc, ks > 0 ? 1u : 0u);
+    }
+}
+
+// Accumulating products of one 64-row half: 4 k-steps of 16 streamed rows.
+// acc1 += T1(bf16) * B (dK/dV kernel only), acc2 += T2(bf16) * A; MN-major B / A descriptors
+// already point at the half's first row.
+template <bool KV>
+__device__ __forceinline__ void bwd_issue_acc(uint32_t acc1, uint32_t acc2, uint32_t t1,
+                                              uint32_t t2, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t acc_first)
+{
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t acc = ks > 0 ? 1u : acc_first;
+        if (KV) mma_ts(acc1, t1 + 8u * ks, sdesc_adv(bdesc, ks * 2048), idesc, acc);
+        mma_ts(acc2, t2 + 8u * ks, sdesc_adv(adesc, ks * 2048), idesc, acc);
+    }
+}
+
 template <int D, bool KV>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -168,50 +196,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);  // acc += (TMEM) * (MN-major)
             const uint32_t tT1 = tbase, tT2 = tbase + 128u;
             const uint32_t tAcc1 = tbase + 256u, tAcc2 = tbase + 256u + D;
-            // Descriptors are built once; each MMA only advances the start address by a
-            // compile-time byte offset (keeps the single issuing thread off the critical path).
+            // Everything the issue loop needs lives in scalar registers: base descriptors are
+            // built once and advanced by byte offsets (stage, half, k-step), so the single
+            // issuing thread keeps pace with the tensor core.
             const uint64_t dX = sdesc_sw128(smem_u32(sX), 16, 1024);
             const uint64_t dY = sdesc_sw128(smem_u32(sY), 16, 1024);
-            uint64_t dA[C::STAGES], dB[C::STAGES], mA[C::STAGES], mB[C::STAGES];
-#pragma unroll
-            for (int s = 0; s < C::STAGES; ++s) {
-                const uint32_t sA = smem_u32(sAB) + s * 2 * C::TILE_BYTES, sB = sA + C::TILE_BYTES;
-                dA[s] = sdesc_sw128(sA, 16, 1024);              // K-major (T products)
-                dB[s] = sdesc_sw128(sB, 16, 1024);
-                mA[s] = sdesc_sw128(sA, C::PANEL_BYTES, 1024);  // MN-major (accumulating products)
-                mB[s] = sdesc_sw128(sB, C::PANEL_BYTES, 1024);
-            }
-
-            // T1 = X A^T and T2 = Y B^T of streamed block `it` (N = 128).
-            auto issue_t = [&](int it) {
-                const int s = it % C::STAGES;
-                const uint64_t a = s ? dA[1] : dA[0], b = s ? dB[1] : dB[0];
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(tT1, sdesc_adv(dX, off), sdesc_adv(a, off), kIdT, ks > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(tT2, sdesc_adv(dY, off), sdesc_adv(b, off), kIdT, ks > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_t[0]);
-                mma_commit(&bar_t[1]);
+            const uint64_t dA0 = sdesc_sw128(smem_u32(sAB), 16, 1024);           // K-major
+            const uint64_t mA0 = sdesc_sw128(smem_u32(sAB), C::PANEL_BYTES, 1024);  // MN-major
+            auto issue_t = [=](int it) {
+                const uint32_t so = (it % C::STAGES) * 2 * C::TILE_BYTES;
+                bwd_issue_t<D, C::PANEL_BYTES>(tT1, dX, sdesc_adv(dA0, so), kIdT);
+                bwd_issue_t<D, C::PANEL_BYTES>(tT2, dY, sdesc_adv(dA0, so + C::TILE_BYTES), kIdT);
             };
-            // Accumulating products of half h of streamed block `it` (4 k-steps of 16 rows).
-            auto issue_acc = [&](int it, int h) {
-                const int s = it % C::STAGES;
-                const uint64_t a = s ? mA[1] : mA[0], b = s ? mB[1] : mB[0];
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t acc = (it > 0 || h > 0 || ks > 0) ? 1u : 0u;
-                    const uint32_t brow = (4 * h + ks) * 2048;  // 16 rows x 128 B
-                    if (KV)  // dV += P^T dO
-                        mma_ts(tAcc1, tT1 + 64u * h + 8u * ks, sdesc_adv(b, brow), kIdAcc, acc);
-                    // dK += dS^T Q  (KV)   or   dQ += dS K  (dQ kernel)
-                    mma_ts(tAcc2, tT2 + 64u * h + 8u * ks, sdesc_adv(a, brow), kIdAcc, acc);
-                }
+            auto issue_acc = [=](int it, int h) {
+                const uint32_t so = (it % C::STAGES) * 2 * C::TILE_BYTES;
+                bwd_issue_acc<KV>(tAcc1, tAcc2, tT1 + 64u * h, tT2 + 64u * h,
+                                  sdesc_adv(mA0, so + h * 8192), sdesc_adv(mA0, so + C::TILE_BYTES + h * 8192),
+                                  kIdAcc, (it > 0 || h > 0) ? 1u : 0u);
             };
 
             bool ok = mbar_wait(&bar_res, 0, wd, kSiteBwdMmaKV);
@@ -221,6 +222,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 if (ok) {
                     tc_fence_after();
                     issue_t(0);
+                    mma_commit(&bar_t[0]);
+                    mma_commit(&bar_t[1]);
                 }
             }
             for (int it = 0; ok && it < n_it; ++it) {
@@ -241,6 +244,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     tc_fence_after();
                     // T1/T2 are free: their readers (issue_acc above) precede in issue order
                     issue_t(it + 1);
+                    mma_commit(&bar_t[0]);
+                    mma_commit(&bar_t[1]);
                 }
             }
             if (ok) mma_commit(&bar_acc);

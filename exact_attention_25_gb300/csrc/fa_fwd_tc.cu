@@ -34,6 +34,28 @@ struct FwdCfg {
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P stays below 2^8
 };
 
+// S = Q K^T for one 128-row query tile: D/16 k-steps of 16, the first overwriting D.
+template <int D, int PANEL>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc,
+                                         uint32_t idesc)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks / 4) * PANEL + (ks % 4) * 32;
+        mma_ss(d_tmem, sdesc_adv(qdesc, off), sdesc_adv(kdesc, off), idesc, ks > 0 ? 1u : 0u);
+    }
+}
+
+// O += P V: P (bf16) from TMEM, V (MN-major) from shared memory; BN/16 k-steps over keys.
+template <int BN>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
+                                         uint32_t idesc, uint32_t acc_first)
+{
+#pragma unroll
+    for (int ks = 0; ks < BN / 16; ++ks)
+        mma_ts(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc, ks > 0 ? 1u : acc_first);
+}
+
 template <int D>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -161,50 +183,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, C::BN, 0, 0);  // S = Q K^T
             constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);     // O += P V
-            // Descriptors are built once; each MMA only advances the start address by a
-            // compile-time byte offset (keeps the single issuing thread off the critical path).
-            uint64_t dQd[C::NT], dK[C::STAGES], dV[C::STAGES];
-#pragma unroll
-            for (int t = 0; t < C::NT; ++t) dQd[t] = sdesc_sw128(smem_u32(sQ) + t * C::TILE_BYTES, 16, 1024);
-#pragma unroll
-            for (int s = 0; s < C::STAGES; ++s) {
-                dK[s] = sdesc_sw128(smem_u32(sK) + s * C::TILE_BYTES, 16, 1024);
-                dV[s] = sdesc_sw128(smem_u32(sV) + s * C::TILE_BYTES, C::PANEL_BYTES, 1024);
-            }
-            auto pick = [](const uint64_t* arr, int i) {
-                uint64_t r = arr[0];
-#pragma unroll
-                for (int k = 1; k < C::STAGES; ++k) r = (i == k) ? arr[k] : r;
-                return r;
-            };
-
-            auto issue_s = [&](int t, int s) {
-                const uint32_t d_tmem = tbase + 128u * t;
-                const uint64_t a0 = t ? dQd[1] : dQd[0], b0 = pick(dK, s);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * C::PANEL_BYTES + (ks % 4) * 32;
-                    mma_ss(d_tmem, sdesc_adv(a0, off), sdesc_adv(b0, off), kIdS, ks > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int s, bool accumulate) {
-                const uint32_t d_tmem = tbase + 256u + static_cast<uint32_t>(t * D);
-                const uint32_t p_tmem = tbase + 128u * t + 64u;
-                const uint64_t b0 = pick(dV, s);
-#pragma unroll
-                for (int ks = 0; ks < C::BN / 16; ++ks)
-                    mma_ts(d_tmem, p_tmem + 8u * ks, sdesc_adv(b0, ks * 2048), kIdPV,
-                           (accumulate || ks > 0) ? 1u : 0u);
-            };
+            // Everything the issue loop needs lives in scalar registers: base descriptors are
+            // built once and advanced by byte offsets (stage, tile, k-step), so the single
+            // issuing thread keeps pace with the tensor core.
+            const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(sV), C::PANEL_BYTES, 1024);
+            const int J0 = J[0], J1 = J[1];
+            const uint32_t tS0 = tbase, tS1 = tbase + 128u;
+            const uint32_t tO0 = tbase + 256u, tO1 = tbase + 256u + D;
 
             bool ok = mbar_wait(&bar_q, 0, wd, kSiteFwdMmaQ);
             ok = ok && mbar_wait(&bar_kfull[0], 0, wd, kSiteFwdMmaK);
             int committed = 0;  // key blocks whose stage release was committed
             if (ok) {
                 tc_fence_after();
-                for (int t = 0; t < nt; ++t) {
-                    issue_s(t, 0);
-                    mma_commit(&bar_sfull[t]);
+                issue_qk<D, C::PANEL_BYTES>(tS0, dq0, dk0, kIdS);
+                mma_commit(&bar_sfull[0]);
+                if (nt > 1) {
+                    issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), dk0, kIdS);
+                    mma_commit(&bar_sfull[1]);
                 }
             }
             for (int j = 0; ok && j < Jmax; ++j) {
@@ -212,26 +210,42 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 const uint32_t ph = (j / C::STAGES) & 1;
                 const int s1 = (j + 1) % C::STAGES;
                 const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+                const uint64_t vd = sdesc_adv(dv0, s * C::TILE_BYTES);
+                const uint64_t kd1 = sdesc_adv(dk0, s1 * C::TILE_BYTES);
+                const uint32_t acc_first = j > 0 ? 1u : 0u;
                 if (!mbar_wait(&bar_vfull[s], ph, wd, kSiteFwdMmaV)) { ok = false; break; }
                 bool k_next = false;
-                for (int t = 0; t < nt; ++t) {
-                    if (j >= J[t]) continue;
-                    if (!mbar_wait(&bar_pfull[t], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
+                // query tile 0
+                if (j < J0) {
+                    if (!mbar_wait(&bar_pfull[0], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                    if (j + 1 == J[t]) {
-                        mma_commit(&bar_ofinal[t]);
+                    issue_pv<C::BN>(tO0, tS0 + 64u, vd, kIdPV, acc_first);
+                    if (j + 1 == J0) {
+                        mma_commit(&bar_ofinal[0]);
+                    } else {
+                        if (!mbar_wait(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
+                        tc_fence_after();
+                        k_next = true;
+                        issue_qk<D, C::PANEL_BYTES>(tS0, dq0, kd1, kIdS);
+                        mma_commit(&bar_sfull[0]);
+                    }
+                }
+                // query tile 1
+                if (j < J1) {
+                    if (!mbar_wait(&bar_pfull[1], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv<C::BN>(tO1, tS1 + 64u, vd, kIdPV, acc_first);
+                    if (j + 1 == J1) {
+                        mma_commit(&bar_ofinal[1]);
                     } else {
                         if (!k_next) {
                             if (!mbar_wait(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
                             tc_fence_after();
-                            k_next = true;
                         }
-                        issue_s(t, s1);
-                        mma_commit(&bar_sfull[t]);
+                        issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), kd1, kIdS);
+                        mma_commit(&bar_sfull[1]);
                     }
                 }
-                if (!ok) break;
                 mma_commit(&bar_kvempty[s]);
                 committed = j + 1;
             }
@@ -263,7 +277,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         float l = 0.0f;       // running sum of exp2(x - m) (fp32, before rounding): the LSE
         float lr = 0.0f;      // running sum of the bf16-rounded exp2(x - m): normalises O
         bool ok = t < nt;
-        for (int j = 0; ok && j < J[t]; ++j) {
+        const int Jt = t ? J[1] : J[0];
+        for (int j = 0; ok && j < Jt; ++j) {
             if (!warp_wait_all(&bar_sfull[t], j & 1, wd, kSiteFwdSoftmaxS)) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[128];
@@ -358,7 +373,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (lane == 0) mbar_arrive(&bar_pfull[t]);
         }
         // ------------------------------------------------------------- epilogue
-        if (ok && J[t] > 0) {
+        if (ok && Jt > 0) {
             if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
                 tc_fence_after();
                 const float inv_l = 1.0f / lr;
