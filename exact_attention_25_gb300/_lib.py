@@ -20,7 +20,7 @@ STATUS = {
 # Every symbol include/fa.h declares (tests check the library exports all of them).
 EXPORTS = (
     "fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_stage", "fa_fwd_impl", "fa_bwd_impl",
-    "fa_bwd_noalloc",
+    "fa_bwd_noalloc", "fa_debug_set_flags",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_status_string", "fa_last_error",
     "fa_causal_block_counts", "fa_version",
 )
@@ -62,6 +62,8 @@ def load(path: str | None = None):
         lib.fa_device_status.argtypes = [vp]
         lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.fa_set_wait_limit_ns.restype = None
+        lib.fa_debug_set_flags.argtypes = [i]
+        lib.fa_debug_set_flags.restype = None
         lib.fa_status_string.argtypes = [i]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_error.argtypes = []

@@ -28,6 +28,7 @@ namespace {
 
 thread_local std::string t_last_error;
 unsigned long long g_wait_limit_ns = 2000000000ull;
+int g_debug_flags = 0;
 
 int fail(int code, const std::string& what)
 {
@@ -143,6 +144,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
     cudaError_t e;
     if (dtype == FA_F32 || impl == 1) {
         e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st);
@@ -191,6 +193,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.lse2 = reinterpret_cast<float*>(ws + align256(rows * 4));
     p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
     const int is_f32 = dtype == FA_F32;
     cudaError_t e = cudaSuccess;
     if (stage <= 0) {
@@ -286,6 +289,8 @@ void fa_set_wait_limit_ns(unsigned long long ns)
 {
     g_wait_limit_ns = ns < 1000000ull ? 1000000ull : ns;
 }
+
+void fa_debug_set_flags(int flags) { g_debug_flags = flags; }
 
 const char* fa_status_string(int code)
 {

@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE_BYTES);
                 for (int pn = 0; pn < C::PANELS; ++pn) {
                     tma_load_3d(sA + pn * C::PANEL_BYTES, &tm_a, &bar_full[s], 64 * pn, row, bh);
-                    tma_load_3d(sB + pn * C::PANEL_BYTES, &tm_b, &bar_full[s], 64 * pn, row, bh);
+                    if (!(it == 0 && (p.debug_flags & kDebugDropFirstLoad)))
+                        tma_load_3d(sB + pn * C::PANEL_BYTES, &tm_b, &bar_full[s], 64 * pn, row, bh);
                 }
                 issued = it + 1;
             }

@@ -33,6 +33,11 @@ enum WaitSite : int {
     kSiteBwdDrain,
 };
 
+// Test hook: the producer announces the bytes of its first streamed tile but never issues
+// the copy, so the barrier guarding that tile never completes and every bounded wait on it
+// must expire (watchdog test).  Never set in normal operation.
+constexpr int kDebugDropFirstLoad = 1;
+
 // Causal mask (key index <= query index, top-left aligned): classification of the key
 // block [k0, k1) against the query block [q0, q1), following the two-stage split of the
 // FlashAttention-2 Triton write-up ("개선 3: Causal Mask 2-Stage"):
@@ -62,6 +67,7 @@ struct FwdParams {
     int causal;
     int* status;       // device status word (watchdog)
     unsigned long long wait_limit_ns;
+    int debug_flags;   // test hook: kDebugDropFirstLoad
 };
 
 // Parameters of the backward kernels.
@@ -84,6 +90,7 @@ struct BwdParams {
     int causal;
     int* status;
     unsigned long long wait_limit_ns;
+    int debug_flags;
 };
 
 }  // namespace fa

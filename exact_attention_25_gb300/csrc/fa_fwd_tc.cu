@@ -161,9 +161,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     tma_load_3d(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
                                 64 * pn, j * C::BN, bh);
                 mbar_arrive_expect_tx(&bar_vfull[s], C::TILE_BYTES);
-                for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bar_vfull[s],
-                                64 * pn, j * C::BN, bh);
+                if (!(j == 0 && (p.debug_flags & kDebugDropFirstLoad)))
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_3d(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
+                                    &bar_vfull[s], 64 * pn, j * C::BN, bh);
                 issued = j + 1;
             }
             // Let no copy land after the CTA exits: wait (bounded, ignoring the abort flag)

@@ -119,6 +119,13 @@ int fa_device_status(void* stream);
  * clamped to 1e6.  Applies to launches made after the call. */
 void fa_set_wait_limit_ns(unsigned long long ns);
 
+/* Test hook for the watchdog: flags = 1 makes the tensor-core kernels announce their first
+ * streamed tile without copying it, so the wait for it can only end by expiring; each CTA then
+ * aborts cleanly (frees Tensor Memory, returns) and fa_device_status() reports
+ * FA_ERR_DEVICE_TIMEOUT.  0 (the default) restores normal operation.  Not for production use;
+ * applies to launches made after the call. */
+void fa_debug_set_flags(int flags);
+
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(int code);
 
