@@ -106,12 +106,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int N = p.N;
-    const int bh = blockIdx.x;
     const int nblk = (N + 127) / 128;
-    // Heaviest blocks first: for dK/dV the first key blocks see the most query blocks under
-    // the causal mask; for dQ the last query blocks see the most key blocks.
-    const int xb = KV ? static_cast<int>(blockIdx.y)
-                      : static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    // Head-major order, so the CTAs resident at one time share one or two heads' tiles in L2.
+    // Within a head the heaviest blocks go first: for dK/dV the first key blocks see the most
+    // query blocks under the causal mask; for dQ the last query blocks see the most key blocks.
+    const int bh = static_cast<int>(blockIdx.x) / nblk;
+    const int yb = static_cast<int>(blockIdx.x) % nblk;
+    const int xb = KV ? yb : nblk - 1 - yb;
     const int x0 = xb * 128, x1 = min(N, x0 + 128);
     // Streamed blocks visited: a contiguous range [s_begin, s_end).
     int s_begin = 0, s_end = nblk;
@@ -438,7 +439,7 @@ static cudaError_t launch_one(const CUtensorMap& x, const CUtensorMap& y, const 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(p.BH, (p.N + 127) / 128);
+    dim3 grid(p.BH * ((p.N + 127) / 128));
     fa_bwd_tc_kernel<D, KV><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(x, y, a, b, p);
     return cudaGetLastError();
 }

@@ -84,11 +84,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int N = p.N;
-    const int bh = blockIdx.x;
     const int n_qtiles = (N + C::BM - 1) / C::BM;
     const int n_kblocks = (N + C::BN - 1) / C::BN;
-    // heaviest causal pairs first: blockIdx.y = 0 takes the last pair of every head
-    const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
+    // Head-major order, so the CTAs resident at one time share one or two heads' K/V in L2;
+    // within a head the heaviest causal pairs (the last ones) go first.
+    const int bh = static_cast<int>(blockIdx.x) / n_pairs;
+    const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) % n_pairs;
     const int qt0 = pair * C::NT;
     const int nt = min(C::NT, n_qtiles - qt0);
 
@@ -430,7 +432,7 @@ static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& 
     }
     const int n_qtiles = (p.N + C::BM - 1) / C::BM;
     const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
-    dim3 grid(p.BH, n_pairs);
+    dim3 grid(p.BH * n_pairs);
     fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
