@@ -56,7 +56,7 @@ __device__ __forceinline__ void bwd_issue_t(uint32_t d_tmem, uint64_t xdesc, uin
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t off = (ks / 4) * PANEL + (ks % 4) * 32;
-        mma_ss(d_tmem, sdesc_adv(xdesc, off), sdesc_adv(adesc, off), idesc, ks > 0 ? 1u : 0u);
+        mma_ss_w(d_tmem, sdesc_adv(xdesc, off), sdesc_adv(adesc, off), idesc, ks > 0 ? 1u : 0u);
     }
 }
 
@@ -71,8 +71,8 @@ __device__ __forceinline__ void bwd_issue_acc(uint32_t acc1, uint32_t acc2, uint
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
         const uint32_t acc = ks > 0 ? 1u : acc_first;
-        if (KV) mma_ts(acc1, t1 + 8u * ks, sdesc_adv(bdesc, ks * 2048), idesc, acc);
-        mma_ts(acc2, t2 + 8u * ks, sdesc_adv(adesc, ks * 2048), idesc, acc);
+        if (KV) mma_ts_w(acc1, t1 + 8u * ks, sdesc_adv(bdesc, ks * 2048), idesc, acc);
+        mma_ts_w(acc2, t2 + 8u * ks, sdesc_adv(adesc, ks * 2048), idesc, acc);
     }
 }
 
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        {  // the whole warp runs the loop (warp-uniform values); elect.sync picks the issuer
             constexpr uint32_t kIdT = idesc_bf16_f32(128, 128, 0, 0);  // T = X A^T
             constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);  // acc += (TMEM) * (MN-major)
             const uint32_t tT1 = tbase, tT2 = tbase + 128u;
@@ -217,43 +217,43 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                                   kIdAcc, (it > 0 || h > 0) ? 1u : 0u);
             };
 
-            bool ok = mbar_wait(&bar_res, 0, wd, kSiteBwdMmaKV);
+            bool ok = warp_wait_all(&bar_res, 0, wd, kSiteBwdMmaKV);
             int committed = 0;
             if (ok && n_it > 0) {
-                ok = mbar_wait(&bar_full[0], 0, wd, kSiteBwdMmaQ);
+                ok = warp_wait_all(&bar_full[0], 0, wd, kSiteBwdMmaQ);
                 if (ok) {
                     tc_fence_after();
                     issue_t(0);
-                    mma_commit(&bar_t[0]);
-                    mma_commit(&bar_t[1]);
+                    mma_commit_w(&bar_t[0]);
+                    mma_commit_w(&bar_t[1]);
                 }
             }
             for (int it = 0; ok && it < n_it; ++it) {
                 for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait(&bar_e[h], it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
+                    if (!warp_wait_all(&bar_e[h], it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
                     tc_fence_after();
                     issue_acc(it, h);
                 }
                 if (!ok) break;
-                mma_commit(&bar_empty[it % C::STAGES]);
+                mma_commit_w(&bar_empty[it % C::STAGES]);
                 committed = it + 1;
                 if (it + 1 < n_it) {
                     const int s1 = (it + 1) % C::STAGES;
-                    if (!mbar_wait(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd, kSiteBwdMmaQ)) {
+                    if (!warp_wait_all(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd, kSiteBwdMmaQ)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     // T1/T2 are free: their readers (issue_acc above) precede in issue order
                     issue_t(it + 1);
-                    mma_commit(&bar_t[0]);
-                    mma_commit(&bar_t[1]);
+                    mma_commit_w(&bar_t[0]);
+                    mma_commit_w(&bar_t[1]);
                 }
             }
-            if (ok) mma_commit(&bar_acc);
+            if (ok) mma_commit_w(&bar_acc);
             volatile int no_abort = 0;
             const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
-            mma_commit(&bar_drain);
+            mma_commit_w(&bar_drain);
             mbar_wait(&bar_drain, 0, wd_drain, kSiteBwdDrain);
             for (int it = max(0, committed - C::STAGES); it < committed; ++it)
                 mbar_wait(&bar_empty[it % C::STAGES], (it / C::STAGES) & 1, wd_drain, kSiteBwdDrain);

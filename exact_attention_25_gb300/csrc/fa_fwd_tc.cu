@@ -35,6 +35,7 @@ struct FwdCfg {
 };
 
 // S = Q K^T for one 128-row query tile: D/16 k-steps of 16, the first overwriting D.
+// Executed by the whole MMA warp; one elected lane issues each MMA.
 template <int D, int PANEL>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc,
                                          uint32_t idesc)
@@ -42,7 +43,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t off = (ks / 4) * PANEL + (ks % 4) * 32;
-        mma_ss(d_tmem, sdesc_adv(qdesc, off), sdesc_adv(kdesc, off), idesc, ks > 0 ? 1u : 0u);
+        mma_ss_w(d_tmem, sdesc_adv(qdesc, off), sdesc_adv(kdesc, off), idesc, ks > 0 ? 1u : 0u);
     }
 }
 
@@ -53,7 +54,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 {
 #pragma unroll
     for (int ks = 0; ks < BN / 16; ++ks)
-        mma_ts(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc, ks > 0 ? 1u : acc_first);
+        mma_ts_w(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc, ks > 0 ? 1u : acc_first);
 }
 
 template <int D>
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        {  // the whole warp runs the loop (warp-uniform values); elect.sync picks the issuer
             constexpr uint32_t kIdS = idesc_bf16_f32(128, C::BN, 0, 0);  // S = Q K^T
             constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);     // O += P V
             // Everything the issue loop needs lives in scalar registers: base descriptors are
@@ -196,16 +197,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const uint32_t tS0 = tbase, tS1 = tbase + 128u;
             const uint32_t tO0 = tbase + 256u, tO1 = tbase + 256u + D;
 
-            bool ok = mbar_wait(&bar_q, 0, wd, kSiteFwdMmaQ);
-            ok = ok && mbar_wait(&bar_kfull[0], 0, wd, kSiteFwdMmaK);
+            bool ok = warp_wait_all(&bar_q, 0, wd, kSiteFwdMmaQ);
+            ok = ok && warp_wait_all(&bar_kfull[0], 0, wd, kSiteFwdMmaK);
             int committed = 0;  // key blocks whose stage release was committed
             if (ok) {
                 tc_fence_after();
                 issue_qk<D, C::PANEL_BYTES>(tS0, dq0, dk0, kIdS);
-                mma_commit(&bar_sfull[0]);
+                mma_commit_w(&bar_sfull[0]);
                 if (nt > 1) {
                     issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), dk0, kIdS);
-                    mma_commit(&bar_sfull[1]);
+                    mma_commit_w(&bar_sfull[1]);
                 }
             }
             for (int j = 0; ok && j < Jmax; ++j) {
@@ -216,47 +217,47 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 const uint64_t vd = sdesc_adv(dv0, s * C::TILE_BYTES);
                 const uint64_t kd1 = sdesc_adv(dk0, s1 * C::TILE_BYTES);
                 const uint32_t acc_first = j > 0 ? 1u : 0u;
-                if (!mbar_wait(&bar_vfull[s], ph, wd, kSiteFwdMmaV)) { ok = false; break; }
+                if (!warp_wait_all(&bar_vfull[s], ph, wd, kSiteFwdMmaV)) { ok = false; break; }
                 bool k_next = false;
                 // query tile 0
                 if (j < J0) {
-                    if (!mbar_wait(&bar_pfull[0], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
+                    if (!warp_wait_all(&bar_pfull[0], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv<C::BN>(tO0, tS0 + 64u, vd, kIdPV, acc_first);
                     if (j + 1 == J0) {
-                        mma_commit(&bar_ofinal[0]);
+                        mma_commit_w(&bar_ofinal[0]);
                     } else {
-                        if (!mbar_wait(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
+                        if (!warp_wait_all(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
                         tc_fence_after();
                         k_next = true;
                         issue_qk<D, C::PANEL_BYTES>(tS0, dq0, kd1, kIdS);
-                        mma_commit(&bar_sfull[0]);
+                        mma_commit_w(&bar_sfull[0]);
                     }
                 }
                 // query tile 1
                 if (j < J1) {
-                    if (!mbar_wait(&bar_pfull[1], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
+                    if (!warp_wait_all(&bar_pfull[1], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv<C::BN>(tO1, tS1 + 64u, vd, kIdPV, acc_first);
                     if (j + 1 == J1) {
-                        mma_commit(&bar_ofinal[1]);
+                        mma_commit_w(&bar_ofinal[1]);
                     } else {
                         if (!k_next) {
-                            if (!mbar_wait(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
+                            if (!warp_wait_all(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
                             tc_fence_after();
                         }
                         issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), kd1, kIdS);
-                        mma_commit(&bar_sfull[1]);
+                        mma_commit_w(&bar_sfull[1]);
                     }
                 }
-                mma_commit(&bar_kvempty[s]);
+                mma_commit_w(&bar_kvempty[s]);
                 committed = j + 1;
             }
             // Wait until every commit this thread issued has arrived, so no arrive lands on
             // shared memory after the CTA exits (bounded; ignores the abort flag).
             volatile int no_abort = 0;
             const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
-            mma_commit(&bar_drain);
+            mma_commit_w(&bar_drain);
             mbar_wait(&bar_drain, 0, wd_drain, kSiteFwdDrain);
             for (int j = max(0, committed - C::STAGES); j < committed; ++j)
                 mbar_wait(&bar_kvempty[j % C::STAGES], (j / C::STAGES) & 1, wd_drain, kSiteFwdDrain);
