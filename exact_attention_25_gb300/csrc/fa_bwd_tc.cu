@@ -163,25 +163,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bar_res, 2 * C::TILE_BYTES);
+        {  // the whole warp runs the loop; elect.sync picks the issuing lane
+            mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
             for (int pn = 0; pn < C::PANELS; ++pn) {
-                tma_load_3d(sX + pn * C::PANEL_BYTES, &tm_x, &bar_res, 64 * pn, x0, bh);
-                tma_load_3d(sY + pn * C::PANEL_BYTES, &tm_y, &bar_res, 64 * pn, x0, bh);
+                tma_load_3d_w(sX + pn * C::PANEL_BYTES, &tm_x, &bar_res, 64 * pn, x0, bh);
+                tma_load_3d_w(sY + pn * C::PANEL_BYTES, &tm_y, &bar_res, 64 * pn, x0, bh);
             }
             int issued = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (it / C::STAGES) & 1;
-                if (!mbar_wait(&bar_empty[s], ph ^ 1, wd, kSiteBwdLoadEmpty)) break;
+                if (!warp_wait_all(&bar_empty[s], ph ^ 1, wd, kSiteBwdLoadEmpty)) break;
                 uint8_t* sA = sAB + s * 2 * C::TILE_BYTES;
                 uint8_t* sB = sA + C::TILE_BYTES;
                 const int row = (s_begin + it) * 128;
-                mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE_BYTES);
+                mbar_arrive_expect_tx_w(&bar_full[s], 2 * C::TILE_BYTES);
                 for (int pn = 0; pn < C::PANELS; ++pn) {
-                    tma_load_3d(sA + pn * C::PANEL_BYTES, &tm_a, &bar_full[s], 64 * pn, row, bh);
+                    tma_load_3d_w(sA + pn * C::PANEL_BYTES, &tm_a, &bar_full[s], 64 * pn, row, bh);
                     if (!(it == 0 && (p.debug_flags & kDebugDropFirstLoad)))
-                        tma_load_3d(sB + pn * C::PANEL_BYTES, &tm_b, &bar_full[s], 64 * pn, row, bh);
+                        tma_load_3d_w(sB + pn * C::PANEL_BYTES, &tm_b, &bar_full[s], 64 * pn, row, bh);
                 }
                 issued = it + 1;
             }

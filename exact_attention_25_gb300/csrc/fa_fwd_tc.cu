@@ -148,25 +148,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bar_q, nt * C::TILE_BYTES);
+        {  // the whole warp runs the loop; elect.sync picks the issuing lane
+            mbar_arrive_expect_tx_w(&bar_q, nt * C::TILE_BYTES);
             for (int t = 0; t < nt; ++t)
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn,
+                    tma_load_3d_w(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn,
                                 (qt0 + t) * C::BM, bh);
             int issued = 0;
             for (int j = 0; j < Jmax; ++j) {
                 const int s = j % C::STAGES;
                 const uint32_t ph = (j / C::STAGES) & 1;
-                if (!mbar_wait(&bar_kvempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
-                mbar_arrive_expect_tx(&bar_kfull[s], C::TILE_BYTES);
+                if (!warp_wait_all(&bar_kvempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
+                mbar_arrive_expect_tx_w(&bar_kfull[s], C::TILE_BYTES);
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
+                    tma_load_3d_w(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
                                 64 * pn, j * C::BN, bh);
-                mbar_arrive_expect_tx(&bar_vfull[s], C::TILE_BYTES);
+                mbar_arrive_expect_tx_w(&bar_vfull[s], C::TILE_BYTES);
                 if (!(j == 0 && (p.debug_flags & kDebugDropFirstLoad)))
                     for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
+                        tma_load_3d_w(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
                                     &bar_vfull[s], 64 * pn, j * C::BN, bh);
                 issued = j + 1;
             }
