@@ -15,14 +15,16 @@
 //       T1 = S, T2 = dP, dS = P o (dP - Delta), acc2 += dS A = dQ / scale
 // Roles (10 warps): two elementwise warpgroups (warps 0-3 and 4-7; thread = row of X = TMEM
 // lane), warpgroup h owning half h (streamed rows [64h, 64h+64)) of every block; warp 8 TMA
-// producer; warp 9 TMEM allocator + MMA issuer.  Per streamed block the MMA warp issues the
-// T products (N = 128), waits for each half's elementwise pass and issues that half's
-// accumulating products, then issues the next block's T products.  Shared-memory descriptors
-// are built once per stage and only advanced per MMA, so one thread issues at tensor-core
-// speed.
-// TMEM columns: T1 [0,128), T2 [128,256), acc1 [256,256+d), acc2 [256+d,256+2d).  The bf16
-// P^T / dS^T of half h (32 columns of packed pairs) overwrite columns [64h, 64h+32) of T1 /
-// T2, chunk by chunk, after the warpgroup loaded them.
+// producer; warp 9 TMEM allocator + MMA issuer (whole warp, one elected lane issues).
+// Pipeline: the T1/T2 products are issued per half (N = 64), and half h of block i+1 is issued
+// right after the accumulating products of half h of block i, so the tensor pipe always has
+// the other half's products queued while a warpgroup runs its elementwise pass:
+//   TC:  acc(i,0) | T(i+1,0) | acc(i,1) | T(i+1,1) | acc(i+1,0) | ...
+//   WG0:             elementwise(i+1, 0) .........|
+//   WG1:                        elementwise(i+1, 1) ..........|
+// TMEM columns: half h: T1 [128h, 128h+64), T2 [128h+64, 128h+128); acc1 [256, 256+d),
+// acc2 [256+d, 256+2d).  The bf16 P^T / dS^T of half h (32 columns of packed pairs) overwrite
+// the first 32 columns of that half's T1 / T2, chunk by chunk, after they were loaded.
 #include <type_traits>
 
 #include "fa_common.cuh"
@@ -194,9 +196,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
         {  // the whole warp runs the loop (warp-uniform values); elect.sync picks the issuer
-            constexpr uint32_t kIdT = idesc_bf16_f32(128, 128, 0, 0);  // T = X A^T
+            constexpr uint32_t kIdT = idesc_bf16_f32(128, 64, 0, 0);   // T_h = X A_h^T
             constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);  // acc += (TMEM) * (MN-major)
-            const uint32_t tT1 = tbase, tT2 = tbase + 128u;
             const uint32_t tAcc1 = tbase + 256u, tAcc2 = tbase + 256u + D;
             // Everything the issue loop needs lives in scalar registers: base descriptors are
             // built once and advanced by byte offsets (stage, half, k-step), so the single
@@ -205,16 +206,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             const uint64_t dY = sdesc_sw128(smem_u32(sY), 16, 1024);
             const uint64_t dA0 = sdesc_sw128(smem_u32(sAB), 16, 1024);           // K-major
             const uint64_t mA0 = sdesc_sw128(smem_u32(sAB), C::PANEL_BYTES, 1024);  // MN-major
-            auto issue_t = [=](int it) {
-                const uint32_t so = (it % C::STAGES) * 2 * C::TILE_BYTES;
-                bwd_issue_t<D, C::PANEL_BYTES>(tT1, dX, sdesc_adv(dA0, so), kIdT);
-                bwd_issue_t<D, C::PANEL_BYTES>(tT2, dY, sdesc_adv(dA0, so + C::TILE_BYTES), kIdT);
+            // T1, T2 of half h of streamed block `it` (streamed rows [64h, 64h+64)).
+            auto issue_t = [=](int it, int h) {
+                const uint32_t so = (it % C::STAGES) * 2 * C::TILE_BYTES + 8192u * h;
+                const uint32_t t1 = tbase + 128u * h;
+                bwd_issue_t<D, C::PANEL_BYTES>(t1, dX, sdesc_adv(dA0, so), kIdT);
+                bwd_issue_t<D, C::PANEL_BYTES>(t1 + 64u, dY, sdesc_adv(dA0, so + C::TILE_BYTES), kIdT);
             };
+            // Accumulating products of half h of streamed block `it`.
             auto issue_acc = [=](int it, int h) {
-                const uint32_t so = (it % C::STAGES) * 2 * C::TILE_BYTES;
-                bwd_issue_acc<KV>(tAcc1, tAcc2, tT1 + 64u * h, tT2 + 64u * h,
-                                  sdesc_adv(mA0, so + h * 8192), sdesc_adv(mA0, so + C::TILE_BYTES + h * 8192),
-                                  kIdAcc, (it > 0 || h > 0) ? 1u : 0u);
+                const uint32_t so = (it % C::STAGES) * 2 * C::TILE_BYTES + 8192u * h;
+                const uint32_t t1 = tbase + 128u * h;
+                bwd_issue_acc<KV>(tAcc1, tAcc2, t1, t1 + 64u, sdesc_adv(mA0, so),
+                                  sdesc_adv(mA0, so + C::TILE_BYTES), kIdAcc,
+                                  (it > 0 || h > 0) ? 1u : 0u);
             };
 
             bool ok = warp_wait_all(&bar_res, 0, wd, kSiteBwdMmaKV);
@@ -223,31 +228,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 ok = warp_wait_all(&bar_full[0], 0, wd, kSiteBwdMmaQ);
                 if (ok) {
                     tc_fence_after();
-                    issue_t(0);
+                    issue_t(0, 0);
                     mma_commit_w(&bar_t[0]);
+                    issue_t(0, 1);
                     mma_commit_w(&bar_t[1]);
                 }
             }
             for (int it = 0; ok && it < n_it; ++it) {
+                const bool more = it + 1 < n_it;
                 for (int h = 0; h < 2; ++h) {
                     if (!warp_wait_all(&bar_e[h], it & 1, wd, kSiteBwdMmaDS)) { ok = false; break; }
                     tc_fence_after();
                     issue_acc(it, h);
-                }
-                if (!ok) break;
-                mma_commit_w(&bar_empty[it % C::STAGES]);
-                committed = it + 1;
-                if (it + 1 < n_it) {
-                    const int s1 = (it + 1) % C::STAGES;
-                    if (!warp_wait_all(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd, kSiteBwdMmaQ)) {
-                        ok = false;
-                        break;
+                    if (h == 1) {
+                        mma_commit_w(&bar_empty[it % C::STAGES]);
+                        committed = it + 1;
                     }
-                    tc_fence_after();
-                    // T1/T2 are free: their readers (issue_acc above) precede in issue order
-                    issue_t(it + 1);
-                    mma_commit_w(&bar_t[0]);
-                    mma_commit_w(&bar_t[1]);
+                    if (more) {
+                        if (h == 0) {
+                            const int s1 = (it + 1) % C::STAGES;
+                            if (!warp_wait_all(&bar_full[s1], ((it + 1) / C::STAGES) & 1, wd,
+                                               kSiteBwdMmaQ)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        // half h of T is free: its readers (issue_acc above) precede in issue order
+                        issue_t(it + 1, h);
+                        mma_commit_w(&bar_t[h]);
+                    }
                 }
             }
             if (ok) mma_commit_w(&bar_acc);
@@ -264,7 +274,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int h = warp >> 2;           // half of the streamed block this warpgroup owns
         const int r = threadIdx.x & 127;   // row of the resident block = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tT1 = tbase + lane_base + 64u * h, tT2 = tT1 + 128u;
+        const uint32_t tT1 = tbase + lane_base + 128u * h, tT2 = tT1 + 64u;
         const uint32_t tAcc1 = tbase + lane_base + 256u, tAcc2 = tbase + lane_base + 256u + D;
         const float c2 = p.scale_log2;
         const size_t row_base = static_cast<size_t>(bh) * N;
