@@ -312,14 +312,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c > lim) x[c] = -INFINITY;
             }
+            // Row max: four independent chains of three-input maxima.
             float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, x[c]);
-                mx1 = fmaxf(mx1, x[c + 1]);
-                mx2 = fmaxf(mx2, x[c + 2]);
-                mx3 = fmaxf(mx3, x[c + 3]);
+            for (int c = 4; c < 124; c += 8) {
+                mx0 = fmax3(mx0, x[c], x[c + 1]);
+                mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
+                mx2 = fmax3(mx2, x[c + 4], x[c + 5]);
+                mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
             }
+            mx0 = fmax3(mx0, x[124], x[125]);
+            mx1 = fmax3(mx1, x[126], x[127]);
             const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cf;
             // Rescale only when the max grew by more than the threshold: l and O then keep
             // sharing the same (stale) reference m, so the result stays exact.
@@ -332,31 +335,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 lr *= alpha;
             }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+            // exp2(x c - m) on pairs (f32x2 fma), both row sums as f32x2 adds: the exact one
+            // over the fp32 values and the one over their bf16 roundings.
+            const uint64_t cf2 = f2_make(cf, cf), nm2 = f2_make(neg_m, neg_m);
+            uint64_t lsa = f2_make(0.f, 0.f), lsb = lsa, lra = lsa, lrb = lsa;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
-                    const float p0 = ex2(fmaf(x[cb * 32 + c + 0], cf, neg_m));
-                    const float p1 = ex2(fmaf(x[cb * 32 + c + 1], cf, neg_m));
-                    const float p2 = ex2(fmaf(x[cb * 32 + c + 2], cf, neg_m));
-                    const float p3 = ex2(fmaf(x[cb * 32 + c + 3], cf, neg_m));
+                    const int i = cb * 32 + c;
+                    float p0, p1, p2, p3;
+                    f2_split(f2_fma(f2_make(x[i], x[i + 1]), cf2, nm2), p0, p1);
+                    f2_split(f2_fma(f2_make(x[i + 2], x[i + 3]), cf2, nm2), p2, p3);
+                    p0 = ex2(p0);
+                    p1 = ex2(p1);
+                    p2 = ex2(p2);
+                    p3 = ex2(p3);
                     const uint32_t w01 = pack_bf16x2(p0, p1);
                     const uint32_t w23 = pack_bf16x2(p2, p3);
-                    ls0 += p0 + p1;
-                    ls1 += p2 + p3;
+                    lsa = f2_add(lsa, f2_make(p0, p1));
+                    lsb = f2_add(lsb, f2_make(p2, p3));
                     // lr sums the bf16-rounded weights that the P V product uses, so that
                     // O = sum(P V) / lr is an exact convex combination of those weights.
-                    lr0 += __uint_as_float(w01 << 16) + __uint_as_float(w01 & 0xFFFF0000u);
-                    lr1 += __uint_as_float(w23 << 16) + __uint_as_float(w23 & 0xFFFF0000u);
+                    lra = f2_add(lra, f2_make(__uint_as_float(w01 << 16),
+                                              __uint_as_float(w01 & 0xFFFF0000u)));
+                    lrb = f2_add(lrb, f2_make(__uint_as_float(w23 << 16),
+                                              __uint_as_float(w23 & 0xFFFF0000u)));
                     pk[c / 2] = w01;
                     pk[c / 2 + 1] = w23;
                 }
                 tmem_st16(tP + 16u * cb, pk);
             }
-            l += ls0 + ls1;
-            lr += lr0 + lr1;
+            {
+                float a0, a1, b0, b1;
+                f2_split(f2_add(lsa, lsb), a0, a1);
+                f2_split(f2_add(lra, lrb), b0, b1);
+                l += a0 + a1;
+                lr += b0 + b1;
+            }
             // O still holds the sum up to block j-1 (the commit that signalled S for block j
             // also covers the P V product of block j-1).
             if (j > 0 && __any_sync(0xffffffffu, need)) {

@@ -430,6 +430,14 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
     return d;
 }
 
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` goes to bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
