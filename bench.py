@@ -232,8 +232,8 @@ def run_gpu(args):
     # kernel 4 (S^T, dP^T, dV, dK), the dQ kernel 3 (S, dP, dQ).
     gemm = perfmodel.fwd_flops(B, H, N, d, w.causal) / 2.0
     kern_flops = {"fwd": 2 * gemm, "bwd_dkdv": 4 * gemm, "bwd_dq": 3 * gemm}
-    kern_names = {"fwd": "fa_fwd_tc_kernel<128>", "bwd_dkdv": "fa_bwd_tc_kernel<128,KV=true>",
-                  "bwd_dq": "fa_bwd_tc_kernel<128,KV=false>"}
+    kern_names = {"fwd": "fa_fwd_tc_kernel<128>", "bwd_dkdv": "fa_bwd_dkv_tc_kernel<128>",
+                  "bwd_dq": "fa_bwd_dq_tc_kernel<128>"}
     dom_key = max(kern_flops, key=lambda k: kern_ms[k])
     dom_tflops = kern_flops[dom_key] / (kern_ms[dom_key] * 1e-3) / 1e12
     # Denominator: the measured burst bf16 peak.  The timed region is well under a second

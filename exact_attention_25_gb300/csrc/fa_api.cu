@@ -16,9 +16,9 @@ cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t 
 cudaError_t launch_bwd_preprocess(int d, int is_f32, const BwdParams& p, cudaStream_t st,
                                   int num_sms);
 cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st);
-cudaError_t launch_bwd_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
-cudaError_t launch_bwd_tc_stage(int d, int stage, const CUtensorMap* maps, const BwdParams& p,
-                                cudaStream_t st);
+// maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
+cudaError_t launch_bwd_dkv_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
 
 // Device status word written by bounded waits that give up (0 = fine).
 __device__ int g_status_word;
@@ -210,8 +210,8 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
         const void* srcs[4] = {q, k, v, dout};
         for (int i = 0; i < 4; ++i)
             if ((rc = make_map(&maps[i], srcs[i], p.BH, N, d, 128))) return rc;
-        e = stage < 0 ? fa::launch_bwd_tc(d, maps, p, st)
-                      : fa::launch_bwd_tc_stage(d, stage, maps, p, st);
+        if (stage < 0 || stage == 1) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
+        if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq_tc(d, maps, p, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return FA_OK;

@@ -1,0 +1,423 @@
+// dQ of backward attention on sm_103a tensor cores: the dQ loop of "Backward 구현" in
+// "Triton 06: Flash Attention v2" (after the Delta preprocess).  A CTA owns one block of 128
+// query rows (Q_i and dO_i resident in shared memory, the row's base-2 LSE and Delta in
+// registers) and sweeps the key blocks j it sees, accumulating in Tensor Memory:
+//   S = Q_i K_j^T,  dP = dO_i V_j^T                    (tcgen05, N = 128, operands in smem)
+//   P = exp2(c S - L2_i),  dS = P o (dP - Delta_i)     (elementwise warpgroups)
+//   acc += dS K_j                                        (tcgen05, dS from TMEM)
+// and dQ_i = scale * acc.  S and P are recomputed ("Flash Attention IO-awareness principle",
+// recomputation); nothing N x N reaches device memory and there are no atomics.
+//
+// Roles (10 warps): warps 0-7 elementwise, warpgroup h owning key columns [64h, 64h+64) of
+// every block (thread = query row = TMEM lane); warp 8 TMA producer; warp 9 TMEM allocator and
+// MMA issuer (whole warp, one elected lane issues).
+//
+// TMEM: one S buffer, two dP buffers, the accumulator.  The bf16 dS of block j overwrites the
+// dP buffer it came from (j % 2), so the S buffer is free as soon as the elementwise warps have
+// loaded S(j) into registers, and dP(j+2) can be issued as soon as acc(j) has been queued.
+// Issue order, block j (tcgen05.mma operations of one CTA execute in issue order, so a
+// product that overwrites a buffer runs after the one that reads it):
+//   wait dS(j) | acc += dS(j) K_j | dP(j+2) -> dP buffer j % 2 | wait S(j+1) loaded |
+//   S(j+2) -> S buffer
+// While the elementwise warps work on block j+1 (S(j+1) and dP(j+1) were issued a block
+// earlier) the pipe runs acc(j), dP(j+2), S(j+2): three 128x128x128 products of cover.  Each
+// streamed tile is issued about two blocks before its first use, which hides the ~1 us latency
+// of a TMA load under full load: K_j is read by S(j) and last by acc(j) (3-stage ring), V_j by
+// dP(j) only (2 stages).
+// TMEM columns: S [0, 128), dP buffers [128, 256) and [256, 384), acc [384, 384 + d).
+// Within a dP buffer, warpgroup h's dS (32 columns of bf16 pairs) lands at [64h, 64h + 32),
+// the first half of the columns it loaded itself.
+#include "fa_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct DqCfg {
+    static constexpr int PANELS = D / 64;
+    static constexpr int PANEL_BYTES = 128 * 128;            // 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;  // 128 rows x D bf16
+    static constexpr int KSTAGES = 3;
+    static constexpr int VSTAGES = 2;
+    static constexpr int SMEM_BYTES = (2 + KSTAGES + VSTAGES) * TILE_BYTES + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 384;  // dP buffer b at COL_DP + 128 b
+};
+
+// D/16 k-steps of a 128 x 128 product of two K-major 128-row tiles, the first overwriting.
+template <int D, int PANEL>
+__device__ __forceinline__ void dq_issue_nt(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks / 4) * PANEL + (ks % 4) * 32;
+        mma_ss_w(d_tmem, sdesc_adv(adesc, off), sdesc_adv(bdesc, off), idesc, ks > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
+    fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_g,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const BwdParams p)
+{
+    using C = DqCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sG = sQ + C::TILE_BYTES;
+    uint8_t* sK = sG + C::TILE_BYTES;                  // KSTAGES tiles
+    uint8_t* sV = sK + C::KSTAGES * C::TILE_BYTES;     // VSTAGES tiles
+
+    __shared__ __align__(8) uint64_t bar_res;
+    __shared__ __align__(8) uint64_t bar_kfull[C::KSTAGES];
+    __shared__ __align__(8) uint64_t bar_kempty[C::KSTAGES];
+    __shared__ __align__(8) uint64_t bar_vfull[C::VSTAGES];
+    __shared__ __align__(8) uint64_t bar_vempty[C::VSTAGES];
+    __shared__ __align__(8) uint64_t bar_s;      // S of the next block landed
+    __shared__ __align__(8) uint64_t bar_sfree;  // every elementwise warp loaded S
+    __shared__ __align__(8) uint64_t bar_dp[2];  // dP landed in dP buffer b
+    __shared__ __align__(8) uint64_t bar_e[2];  // warpgroup h wrote its dS (and read S, dP)
+    __shared__ __align__(8) uint64_t bar_acc;   // accumulator final
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = p.N;
+    const int nblk = (N + 127) / 128;
+    // Head-major order; within a head the last query blocks (most key blocks under the causal
+    // mask) go first.
+    const int bh = static_cast<int>(blockIdx.x) / nblk;
+    const int qb = nblk - 1 - static_cast<int>(blockIdx.x) % nblk;
+    const int q0 = qb * 128, q1 = min(N, q0 + 128);
+    int n_it = nblk;  // key blocks [0, n_it) seen by any query of [q0, q1)
+    if (p.causal) {
+        n_it = 0;
+        while (n_it < nblk &&
+               causal_tile_class(q0, q1, n_it * 128, min(N, n_it * 128 + 128)) != kTileSkip)
+            ++n_it;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_res, 1);
+        for (int s = 0; s < C::KSTAGES; ++s) {
+            mbar_init(&bar_kfull[s], 1);
+            mbar_init(&bar_kempty[s], 1);
+        }
+        for (int s = 0; s < C::VSTAGES; ++s) {
+            mbar_init(&bar_vfull[s], 1);
+            mbar_init(&bar_vempty[s], 1);
+        }
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_sfree, 8);  // one elected arrive per elementwise warp
+        mbar_init(&bar_dp[0], 1);
+        mbar_init(&bar_dp[1], 1);
+        mbar_init(&bar_e[0], 4);  // one elected arrive per warp of the warpgroup
+        mbar_init(&bar_e[1], 4);
+        mbar_init(&bar_acc, 1);
+        mbar_init(&bar_drain, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_g);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_slot;
+    const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+
+    if (warp == 8) {
+        // ------------------------------------------------------------- TMA producer
+        mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+            tma_load_3d_w(sQ + pn * C::PANEL_BYTES, &tm_q, &bar_res, 64 * pn, q0, bh);
+            tma_load_3d_w(sG + pn * C::PANEL_BYTES, &tm_g, &bar_res, 64 * pn, q0, bh);
+        }
+        int issued_k = 0, issued_v = 0;
+        for (int it = 0; it < n_it; ++it) {
+            const int row = it * 128;
+            // V first: dP(it) is issued before S(it), and V's stage frees earlier than K's
+            const int sv = it % C::VSTAGES;
+            if (!warp_wait_all(&bar_vempty[sv], ((it / C::VSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
+                break;
+            mbar_arrive_expect_tx_w(&bar_vfull[sv], C::TILE_BYTES);
+            if (!(it == 0 && (p.debug_flags & kDebugDropFirstLoad)))
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d_w(sV + sv * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
+                                  &bar_vfull[sv], 64 * pn, row, bh);
+            issued_v = it + 1;
+            const int sk = it % C::KSTAGES;
+            if (!warp_wait_all(&bar_kempty[sk], ((it / C::KSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
+                break;
+            mbar_arrive_expect_tx_w(&bar_kfull[sk], C::TILE_BYTES);
+            for (int pn = 0; pn < C::PANELS; ++pn)
+                tma_load_3d_w(sK + sk * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[sk],
+                              64 * pn, row, bh);
+            issued_k = it + 1;
+        }
+        // drain: no copy may still be in flight when the CTA exits
+        volatile int no_abort = 0;
+        const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
+        mbar_wait(&bar_res, 0, wd_drain, kSiteBwdDrain);
+        for (int it = max(0, issued_k - C::KSTAGES); it < issued_k; ++it)
+            mbar_wait(&bar_kfull[it % C::KSTAGES], (it / C::KSTAGES) & 1, wd_drain, kSiteBwdDrain);
+        for (int it = max(0, issued_v - C::VSTAGES); it < issued_v; ++it)
+            mbar_wait(&bar_vfull[it % C::VSTAGES], (it / C::VSTAGES) & 1, wd_drain, kSiteBwdDrain);
+    } else if (warp == 9) {
+        // ------------------------------------------------------------- MMA issuer
+        constexpr uint32_t kIdNT = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: both K-major
+        constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);   // acc += (TMEM) * (MN-major)
+        const uint32_t tS = tbase + C::COL_S, tAcc = tbase + C::COL_ACC;
+        const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dGd = sdesc_sw128(smem_u32(sG), 16, 1024);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);                // K-major
+        const uint64_t mK0 = sdesc_sw128(smem_u32(sK), C::PANEL_BYTES, 1024);    // MN-major
+        const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
+        auto issue_s = [=](int it) {
+            dq_issue_nt<D, C::PANEL_BYTES>(tS, dQd,
+                                           sdesc_adv(dK0, (it % C::KSTAGES) * C::TILE_BYTES), kIdNT);
+        };
+        auto issue_dp = [=](int it) {
+            dq_issue_nt<D, C::PANEL_BYTES>(tbase + C::COL_DP + 128u * (it & 1), dGd,
+                                           sdesc_adv(dV0, (it % C::VSTAGES) * C::TILE_BYTES), kIdNT);
+        };
+        auto issue_acc = [=](int it) {
+            const uint32_t sb = tbase + C::COL_DP + 128u * (it & 1);
+            const uint64_t kb = sdesc_adv(mK0, (it % C::KSTAGES) * C::TILE_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)  // 16 keys per k-step; dS pairs of keys [16ks, +16)
+                mma_ts_w(tAcc, sb + (ks < 4 ? 8u * ks : 64u + 8u * (ks - 4)),
+                         sdesc_adv(kb, ks * 2048), kIdAcc, (it > 0 || ks > 0) ? 1u : 0u);
+        };
+        auto wait_k = [&](int it) {
+            return warp_wait_all(&bar_kfull[it % C::KSTAGES], (it / C::KSTAGES) & 1, wd,
+                                 kSiteBwdMmaQ);
+        };
+        auto wait_v = [&](int it) {
+            return warp_wait_all(&bar_vfull[it % C::VSTAGES], (it / C::VSTAGES) & 1, wd,
+                                 kSiteBwdMmaQ);
+        };
+        // dP(it) -> dP buffer it % 2, releasing V's stage when it has run
+        auto do_dp = [&](int it) {
+            if (!wait_v(it)) return false;
+            tc_fence_after();
+            issue_dp(it);
+            mma_commit_w(&bar_dp[it & 1]);
+            mma_commit_w(&bar_vempty[it % C::VSTAGES]);
+            return true;
+        };
+        // S(it) once every elementwise warp has loaded S(it - 1)
+        auto do_s = [&](int it) {
+            if (it > 0 && !warp_wait_all(&bar_sfree, (it - 1) & 1, wd, kSiteBwdMmaP)) return false;
+            if (!wait_k(it)) return false;
+            tc_fence_after();
+            issue_s(it);
+            mma_commit_w(&bar_s);
+            return true;
+        };
+
+        bool ok = warp_wait_all(&bar_res, 0, wd, kSiteBwdMmaKV);
+        int committed_k = 0, committed_v = 0;
+        if (ok && n_it > 0) {
+            ok = do_s(0) && do_dp(0);
+            committed_v = ok ? 1 : 0;
+            if (ok && n_it > 1) {
+                ok = do_dp(1);
+                committed_v = ok ? 2 : 1;
+                ok = ok && do_s(1);
+            }
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+            if (!warp_wait_all(&bar_e[0], it & 1, wd, kSiteBwdMmaDS) ||
+                !warp_wait_all(&bar_e[1], it & 1, wd, kSiteBwdMmaDS)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            issue_acc(it);
+            mma_commit_w(&bar_kempty[it % C::KSTAGES]);
+            committed_k = it + 1;
+            if (it + 2 < n_it) {  // dP buffer it % 2 is free once acc(it), queued above, ran
+                if (!do_dp(it + 2)) { ok = false; break; }
+                committed_v = it + 3;
+                if (!do_s(it + 2)) { ok = false; break; }
+            }
+        }
+        if (ok) mma_commit_w(&bar_acc);
+        volatile int no_abort = 0;
+        const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
+        mma_commit_w(&bar_drain);
+        mbar_wait(&bar_drain, 0, wd_drain, kSiteBwdDrain);
+        for (int it = max(0, committed_k - C::KSTAGES); it < committed_k; ++it)
+            mbar_wait(&bar_kempty[it % C::KSTAGES], (it / C::KSTAGES) & 1, wd_drain, kSiteBwdDrain);
+        for (int it = max(0, committed_v - C::VSTAGES); it < committed_v; ++it)
+            mbar_wait(&bar_vempty[it % C::VSTAGES], (it / C::VSTAGES) & 1, wd_drain, kSiteBwdDrain);
+        if (ok) mbar_wait(&bar_acc, 0, wd_drain, kSiteBwdDrain);
+    } else {
+        // ------------------------------------------------------------- elementwise (warps 0-7)
+        const int h = warp >> 2;          // key columns [64h, 64h + 64) of every block
+        const int r = threadIdx.x & 127;  // query row within the block = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_base + C::COL_S + 64u * h;
+        const uint32_t tDP = tbase + lane_base + C::COL_DP + 64u * h;
+        const uint32_t tAcc = tbase + lane_base + C::COL_ACC;
+        const size_t row_base = static_cast<size_t>(bh) * N;
+        const int qrow = q0 + r;
+        float nL2 = 0.0f, nDl = 0.0f;  // -L2 and -Delta of this thread's query row
+        if (qrow < N) {
+            nL2 = -p.lse2[row_base + qrow];
+            nDl = -p.delta[row_base + qrow];
+        }
+        const uint64_t c2x2 = f2_make(p.scale_log2, p.scale_log2);
+        const uint64_t nl2 = f2_make(nL2, nL2), nd2 = f2_make(nDl, nDl);
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int k0 = it * 128 + 64 * h;  // first key of this warpgroup's columns
+            const uint32_t tDPb = tDP + 128u * (it & 1);  // dP(it), then dS(it)
+            // element-wise mask: causal diagonal block (key > query) and keys beyond N
+            const bool diag = p.causal &&
+                              causal_tile_class(q0, q1, it * 128, min(N, it * 128 + 128)) == kTileMasked;
+            const bool tail = it * 128 + 128 > N;
+            // ---- phase 1: P = exp2(c S - L2) on S, which landed a block ago
+            if (!warp_wait_all(&bar_s, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t pv[64];
+            tmem_ld32(tS, pv);
+            tmem_ld32(tS + 32u, pv + 32);
+            tmem_wait_ld();
+            reg_fence32(pv);
+            reg_fence32(pv + 32);
+            tc_fence_before();  // S is in registers: the buffer may take S(it + 1)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_sfree);
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                const uint64_t x2 =
+                    f2_fma(f2_make(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), c2x2, nl2);
+                float pa, pb;
+                f2_split(x2, pa, pb);
+                pa = ex2(pa);
+                pb = ex2(pb);
+                pv[c] = __float_as_uint(pa);
+                pv[c + 1] = __float_as_uint(pb);
+            }
+            if (diag || tail) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int key = k0 + c;
+                    if ((diag && key > qrow) || key >= N) pv[c] = 0u;
+                }
+            }
+            // ---- phase 2: dS = P o (dP - Delta), bf16 pairs over the first 32 columns of dP
+            // one barrier per dP buffer: dP(it + 2) is issued only after this warpgroup's
+            // arrive for block it, so a waiter is never a full phase behind
+            if (!warp_wait_all(&bar_dp[it & 1], (it >> 1) & 1, wd, kSiteBwdEltS)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t dv[32];
+                tmem_ld32(tDPb + 32u * cb, dv);
+                tmem_wait_ld();
+                reg_fence32(dv);
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const int i = 32 * cb + c;
+                    const uint64_t t2 =
+                        f2_add(f2_make(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), nd2);
+                    float da, db;
+                    f2_split(f2_mul(f2_make(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), t2),
+                             da, db);
+                    pk[c / 2] = pack_bf16x2(da, db);
+                }
+                tmem_st16(tDPb + 16u * cb, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_e[h]);
+        }
+        // ------------------------------------------------------------- epilogue
+        // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
+        if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
+            tc_fence_after();
+            __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) + (row_base + qrow) * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 64; ++ch) {
+                const int c0 = h * (D / 2) + 32 * ch;
+                uint32_t a[32];
+                tmem_ld32(tAcc + c0, a);
+                tmem_wait_ld();
+                reg_fence32(a);
+                uint32_t packed[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale,
+                                            __uint_as_float(a[2 * c + 1]) * p.scale);
+                if (qrow < N) {
+                    uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                            packed[4 * c + 3]);
+                }
+            }
+        } else if (n_it == 0 && qrow < N) {
+            // a query block that sees no key has zero gradient (cannot occur for square causal
+            // attention, kept for completeness)
+            for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c)
+                static_cast<__nv_bfloat16*>(p.dq)[(row_base + qrow) * D + c] = __float2bfloat16_rn(0.0f);
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const CUtensorMap& k,
+                             const CUtensorMap& v, const BwdParams& p, cudaStream_t st)
+{
+    using C = DqCfg<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid(p.BH * ((p.N + 127) / 128));
+    fa_bwd_dq_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(q, g, k, v, p);
+    return cudaGetLastError();
+}
+
+// maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
+cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
+{
+    if (d == 64) return launch_dq<64>(maps[0], maps[3], maps[1], maps[2], p, st);
+    return launch_dq<128>(maps[0], maps[3], maps[1], maps[2], p, st);
+}
+
+}  // namespace fa

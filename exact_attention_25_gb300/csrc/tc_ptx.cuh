@@ -68,17 +68,20 @@ struct Watchdog {
     uint64_t limit_ns;
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const Watchdog& wd,
-                                            int site)
+// The timed part of a wait, out of line.  The watchdog's fields travel by value: a reference
+// would put the struct in local memory and give every caller a stack frame.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort_flag, int* status,
+                                                   uint64_t limit_ns, int site)
 {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
-            if (*wd.abort_flag) return false;
-            if (globaltimer_ns() - t0 > wd.limit_ns) {
-                *wd.abort_flag = 1;
-                atomicCAS(wd.status, 0, site);
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, site);
                 return false;
             }
         }
@@ -89,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
                                           int site)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, wd, site);
+    return mbar_wait_slow(bar, parity, wd.abort_flag, wd.status, wd.limit_ns, site);
 }
 
 // All 32 lanes of the warp wait; the warp proceeds only if every lane saw the phase
@@ -398,6 +401,12 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads'.
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Packed pairs of fp32 (Blackwell f32x2 arithmetic: one instruction for two lanes of math).

@@ -47,6 +47,10 @@ def main():
         ws = torch.empty(fa.fa_bwd_workspace_bytes(*shape), dtype=torch.uint8, device="cuda")
         run = {"fwd": lambda: fa.fa_fwd(q, k, v, o, lse, scale, a.causal),
                "bwd": lambda: fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, a.causal, ws)}[a.which]
+        if a.which == "bwd" and a.stage >= 0:
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, a.causal, ws)
+            run = lambda: fa.fa_bwd_stage(q, k, v, o, do, lse, dq, dk, dv, scale, a.causal, ws,  # noqa: E731
+                                          a.stage)
         for _ in range(3):
             run()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -58,6 +62,10 @@ def main():
         fa.fa_device_status()
         ms = e0.elapsed_time(e1) / a.iters
         fl = (perfmodel.fwd_flops if a.which == "fwd" else perfmodel.bwd_flops)(*shape, a.causal)
+        if a.which == "bwd" and a.stage >= 0:
+            print(f"bwd stage {a.stage} B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: "
+                  f"{ms:.4f} ms")
+            return
         print(f"{a.which} B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: {ms:.4f} ms "
               f"{fl / ms / 1e9:.1f} TFLOP/s")
         return
