@@ -81,7 +81,11 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_s;      // S of the next block landed
     __shared__ __align__(8) uint64_t bar_sfree;  // every elementwise warp loaded S
     __shared__ __align__(8) uint64_t bar_dp[2];  // dP landed in dP buffer b
-    __shared__ __align__(8) uint64_t bar_e[2];  // warpgroup h wrote its dS (and read S, dP)
+    // warpgroup h wrote the dS of a block of parity b (and read its S, dP): bar_e[h][b].  Both
+    // products of block j + 1 are issued before the MMA warp waits for dS(j), so one barrier per
+    // warpgroup could complete twice before that wait; per parity it cannot (block j + 2's dP
+    // is issued only after the wait).
+    __shared__ __align__(8) uint64_t bar_e[2][2];
     __shared__ __align__(8) uint64_t bar_acc;   // accumulator final
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_slot;
@@ -118,8 +122,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_init(&bar_sfree, 8);  // one elected arrive per elementwise warp
         mbar_init(&bar_dp[0], 1);
         mbar_init(&bar_dp[1], 1);
-        mbar_init(&bar_e[0], 4);  // one elected arrive per warp of the warpgroup
-        mbar_init(&bar_e[1], 4);
+        for (int h = 0; h < 2; ++h)
+            for (int b = 0; b < 2; ++b) mbar_init(&bar_e[h][b], 4);  // one arrive per warp
         mbar_init(&bar_acc, 1);
         mbar_init(&bar_drain, 1);
         abort_flag = 0;
@@ -243,8 +247,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             }
         }
         for (int it = 0; ok && it < n_it; ++it) {
-            if (!warp_wait_all(&bar_e[0], it & 1, wd, kSiteBwdMmaDS) ||
-                !warp_wait_all(&bar_e[1], it & 1, wd, kSiteBwdMmaDS)) {
+            if (!warp_wait_all(&bar_e[0][it & 1], (it >> 1) & 1, wd, kSiteBwdMmaDS) ||
+                !warp_wait_all(&bar_e[1][it & 1], (it >> 1) & 1, wd, kSiteBwdMmaDS)) {
                 ok = false;
                 break;
             }
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_e[h]);
+            if (lane == 0) mbar_arrive(&bar_e[h][it & 1]);
         }
         // ------------------------------------------------------------- epilogue
         // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.

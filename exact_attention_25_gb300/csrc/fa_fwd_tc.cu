@@ -4,11 +4,13 @@
 //
 // One CTA owns NT = 2 query tiles of 128 rows of one head (the FlashAttention-2 Q-outer
 // loop order, "FA2·FA3" section of "Flash Attention IO-awareness principle") and streams
-// the key/value blocks of 128 keys through a shared-memory ring.  Roles (10 warps):
+// the key/value blocks of 128 keys through shared-memory rings (K and V stages are released
+// separately: K(j) after the S products of block j, V(j) after its P V products, so the copy
+// of K(j+2) starts a block and a half before its first use).  Roles (10 warps):
 //   warps 0-3   softmax of query tile 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax of query tile 1
-//   warp  8     TMA producer (one lane)
-//   warp  9     TMEM allocator + MMA issuer (one lane)
+//   warp  8     TMA producer (whole warp, one elected lane issues)
+//   warp  9     TMEM allocator + MMA issuer (whole warp, one elected lane issues)
 // TMEM columns: S_t at [128t, 128t+128) (fp32), P_t (bf16 pairs) aliased on the upper half
 // of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised).
 #include "fa_common.cuh"
@@ -74,7 +76,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_q;
     __shared__ __align__(8) uint64_t bar_kfull[C::STAGES];
     __shared__ __align__(8) uint64_t bar_vfull[C::STAGES];
-    __shared__ __align__(8) uint64_t bar_kvempty[C::STAGES];
+    __shared__ __align__(8) uint64_t bar_kempty[C::STAGES];  // K of a block no longer read
+    __shared__ __align__(8) uint64_t bar_vempty[C::STAGES];  // V of a block no longer read
     __shared__ __align__(8) uint64_t bar_sfull[C::NT];
     __shared__ __align__(8) uint64_t bar_pfull[C::NT];
     __shared__ __align__(8) uint64_t bar_ofinal[C::NT];
@@ -120,7 +123,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&bar_kfull[s], 1);
             mbar_init(&bar_vfull[s], 1);
-            mbar_init(&bar_kvempty[s], 1);
+            mbar_init(&bar_kempty[s], 1);
+            mbar_init(&bar_vempty[s], 1);
         }
         for (int t = 0; t < C::NT; ++t) {
             mbar_init(&bar_sfull[t], 1);
@@ -158,11 +162,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             for (int j = 0; j < Jmax; ++j) {
                 const int s = j % C::STAGES;
                 const uint32_t ph = (j / C::STAGES) & 1;
-                if (!warp_wait_all(&bar_kvempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
+                // K and V stages are released separately (K after the last S product that
+                // reads it, V after the last P V product), so K runs two blocks ahead.
+                if (!warp_wait_all(&bar_kempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
                 mbar_arrive_expect_tx_w(&bar_kfull[s], C::TILE_BYTES);
                 for (int pn = 0; pn < C::PANELS; ++pn)
                     tma_load_3d_w(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
                                 64 * pn, j * C::BN, bh);
+                if (!warp_wait_all(&bar_vempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
                 mbar_arrive_expect_tx_w(&bar_vfull[s], C::TILE_BYTES);
                 if (!(j == 0 && (p.debug_flags & kDebugDropFirstLoad)))
                     for (int pn = 0; pn < C::PANELS; ++pn)
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
             bool ok = warp_wait_all(&bar_q, 0, wd, kSiteFwdMmaQ);
             ok = ok && warp_wait_all(&bar_kfull[0], 0, wd, kSiteFwdMmaK);
-            int committed = 0;  // key blocks whose stage release was committed
+            int committed_k = 0, committed_v = 0;  // key blocks whose K / V release was committed
             if (ok) {
                 tc_fence_after();
                 issue_qk<D, C::PANEL_BYTES>(tS0, dq0, dk0, kIdS);
@@ -208,6 +215,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), dk0, kIdS);
                     mma_commit_w(&bar_sfull[1]);
                 }
+                mma_commit_w(&bar_kempty[0]);  // K(0) is read by these S products only
+                committed_k = 1;
             }
             for (int j = 0; ok && j < Jmax; ++j) {
                 const int s = j % C::STAGES;
@@ -250,8 +259,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                         mma_commit_w(&bar_sfull[1]);
                     }
                 }
-                mma_commit_w(&bar_kvempty[s]);
-                committed = j + 1;
+                if (k_next) {  // K(j + 1) has been read by every S product that needs it
+                    mma_commit_w(&bar_kempty[s1]);
+                    committed_k = j + 2;
+                }
+                mma_commit_w(&bar_vempty[s]);  // V(j) has been read by the P V products
+                committed_v = j + 1;
             }
             // Wait until every commit this thread issued has arrived, so no arrive lands on
             // shared memory after the CTA exits (bounded; ignores the abort flag).
@@ -259,8 +272,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
             mma_commit_w(&bar_drain);
             mbar_wait(&bar_drain, 0, wd_drain, kSiteFwdDrain);
-            for (int j = max(0, committed - C::STAGES); j < committed; ++j)
-                mbar_wait(&bar_kvempty[j % C::STAGES], (j / C::STAGES) & 1, wd_drain, kSiteFwdDrain);
+            for (int j = max(0, committed_k - C::STAGES); j < committed_k; ++j)
+                mbar_wait(&bar_kempty[j % C::STAGES], (j / C::STAGES) & 1, wd_drain, kSiteFwdDrain);
+            for (int j = max(0, committed_v - C::STAGES); j < committed_v; ++j)
+                mbar_wait(&bar_vempty[j % C::STAGES], (j / C::STAGES) & 1, wd_drain, kSiteFwdDrain);
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------- softmax

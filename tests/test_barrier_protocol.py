@@ -1,0 +1,250 @@
+"""Host model of the mbarrier protocols of the three tensor-core kernels.
+
+Each role (TMA producer, MMA issuer, elementwise / softmax warpgroups) is written as the
+sequence of barrier operations its loop performs, in the order of the kernel source.  Arrivals
+that the hardware makes asynchronously (a TMA copy completing, a ``tcgen05.commit`` firing when
+the MMAs before it finish) become pending events that a random scheduler delivers later; commit
+arrivals of one issuer keep their order, as MMAs complete in issue order.
+
+A wait is ``mbarrier.try_wait.parity``: it passes when the barrier's current phase parity
+differs from the parity asked for.  The model flags
+  * a wait that passes while the barrier is not exactly one phase past the one the role wants
+    (a missed or an early phase: the parity test cannot tell them apart), and
+  * a schedule in which no role can move while some have not finished (deadlock).
+Random schedules explore the interleavings that the kernels' timing normally hides; the dQ
+kernel's dS barrier was one barrier per warpgroup until this model (and a variant that moved
+the K/V waits) showed that the warpgroups can complete two of its phases before the MMA warp
+waits for the first.
+"""
+from __future__ import annotations
+
+import random
+
+import pytest
+
+# ----------------------------------------------------------------------------- engine
+
+W, A, C = "wait", "arrive", "commit"  # C: asynchronous arrive (TMA completion or tcgen05.commit)
+
+
+class Hazard(AssertionError):
+    pass
+
+
+def run(progs: dict, counts: dict, rng: random.Random) -> None:
+    done = {b: 0 for b in counts}      # completed phases
+    pend = {b: 0 for b in counts}      # arrivals in the current phase
+    pc = {r: 0 for r in progs}
+    asyncq = {r: [] for r in progs}    # in-order asynchronous arrivals issued by each role
+
+    def arrive(b):
+        pend[b] += 1
+        if pend[b] == counts[b]:
+            pend[b] = 0
+            done[b] += 1
+
+    while True:
+        moves = []
+        for r, prog in progs.items():
+            if pc[r] < len(prog):
+                op, b, *k = prog[pc[r]]
+                if op != W or (done[b] & 1) != (k[0] & 1):
+                    moves.append(("step", r))
+            if asyncq[r]:
+                moves.append(("async", r))
+        if not moves:
+            stuck = {r: progs[r][pc[r]] for r in progs if pc[r] < len(progs[r])}
+            if stuck:
+                raise Hazard(f"deadlock: {stuck}")
+            return
+        kind, r = rng.choice(moves)
+        if kind == "async":
+            arrive(asyncq[r].pop(0))
+            continue
+        op, b, *k = progs[r][pc[r]]
+        pc[r] += 1
+        if op == W:
+            if done[b] != k[0] + 1:
+                raise Hazard(f"{r}: wait for phase {k[0]} of {b} passed with {done[b]} completed")
+        elif op == A:
+            arrive(b)
+        else:
+            asyncq[r].append(b)
+
+
+# ----------------------------------------------------------------------------- dQ kernel
+
+def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False):
+    """fa_bwd_dq_tc_kernel: producer (V then K per block), MMA issuer, 2 elementwise groups."""
+    prod, mma = [], []
+    for j in range(n):
+        if j >= vs:
+            prod.append((W, ("vempty", j % vs), j // vs - 1))
+        prod.append((C, ("vfull", j % vs)))
+        if j >= ks:
+            prod.append((W, ("kempty", j % ks), j // ks - 1))
+        prod.append((C, ("kfull", j % ks)))
+    wk = lambda j: (W, ("kfull", j % ks), j // ks)  # noqa: E731
+    wv = lambda j: (W, ("vfull", j % vs), j // vs)  # noqa: E731
+    ebar = (lambda h, j: (("e", h, j & 1), j >> 1)) if e_per_parity else (lambda h, j: (("e", h, 0), j))
+
+    def dp(j):
+        return [(C, ("dp", j & 1)), (C, ("vempty", j % vs))]
+
+    def s(j):
+        return ([(W, "sfree", j - 1)] if j > 0 else []) + [(C, "s")]
+
+    mma += [wk(0), wv(0)] + s(0) + dp(0)
+    if n > 1:
+        mma += [wv(1)] + dp(1) + [wk(1)] + s(1)
+    for it in range(n):
+        if kv_waits_first and it + 2 < n:
+            mma += [wv(it + 2), wk(it + 2)]
+        for h in (0, 1):
+            b, k = ebar(h, it)
+            mma.append((W, b, k))
+        mma.append((C, ("kempty", it % ks)))
+        if it + 2 < n:
+            if not kv_waits_first:
+                mma.append(wv(it + 2))
+            mma += dp(it + 2)
+            if not kv_waits_first:
+                mma += [(W, "sfree", it + 1), wk(it + 2), (C, "s")]
+            else:
+                mma += s(it + 2)
+    progs = {"producer": prod, "mma": mma}
+    for h in (0, 1):
+        g = []
+        for j in range(n):
+            b, _ = ebar(h, j)
+            g += [(W, "s", j), (A, "sfree"), (W, ("dp", j & 1), j >> 1), (A, b)]
+        progs[f"wg{h}"] = g
+    counts = {"s": 1, "sfree": 2, ("dp", 0): 1, ("dp", 1): 1}
+    counts |= {(x, i): 1 for x in ("vfull", "vempty") for i in range(vs)}
+    counts |= {(x, i): 1 for x in ("kfull", "kempty") for i in range(ks)}
+    counts |= {("e", h, b): 1 for h in (0, 1) for b in (0, 1)}
+    return progs, counts
+
+
+# ----------------------------------------------------------------------------- dK/dV kernel
+
+def dkv_protocol(n, qs=3, gs=2):
+    """fa_bwd_dkv_tc_kernel: producer (Q then dO per block), MMA issuer, 2 elementwise groups."""
+    prod, mma = [], []
+    for j in range(n):
+        if j >= qs:
+            prod.append((W, ("qempty", j % qs), j // qs - 1))
+        prod.append((C, ("qfull", j % qs)))
+        if j >= gs:
+            prod.append((W, ("gempty", j % gs), j // gs - 1))
+        prod.append((C, ("gfull", j % gs)))
+    wq = lambda j: (W, ("qfull", j % qs), j // qs)  # noqa: E731
+    wg = lambda j: (W, ("gfull", j % gs), j // gs)  # noqa: E731
+    mma += [wq(0), (C, "s"), wg(0), (C, "dp")]
+    for it in range(n):
+        mma += [(W, ("p", 0), it), (W, ("p", 1), it), (C, ("gempty", it % gs))]
+        if it + 1 < n:
+            mma += [wq(it + 1), (C, "s")]
+        mma += [(W, ("e", 0), it), (W, ("e", 1), it), (C, ("qempty", it % qs))]
+        if it + 1 < n:
+            mma += [wg(it + 1), (C, "dp")]
+    progs = {"producer": prod, "mma": mma}
+    for h in (0, 1):
+        progs[f"wg{h}"] = [x for j in range(n)
+                           for x in ((W, "s", j), (A, ("p", h)), (W, "dp", j), (A, ("e", h)))]
+    counts = {"s": 1, "dp": 1, ("p", 0): 1, ("p", 1): 1, ("e", 0): 1, ("e", 1): 1}
+    counts |= {(x, i): 1 for x in ("qfull", "qempty") for i in range(qs)}
+    counts |= {(x, i): 1 for x in ("gfull", "gempty") for i in range(gs)}
+    return progs, counts
+
+
+# ----------------------------------------------------------------------------- forward kernel
+
+def fwd_protocol(j0, j1, stages=2):
+    """fa_fwd_tc_kernel: producer (K then V per block), MMA issuer, one softmax group per tile."""
+    jmax = max(j0, j1)
+    jt = (j0, j1)
+    prod = [(C, "q")]
+    for j in range(jmax):
+        if j >= stages:
+            prod.append((W, ("kempty", j % stages), j // stages - 1))
+        prod.append((C, ("kfull", j % stages)))
+        if j >= stages:
+            prod.append((W, ("vempty", j % stages), j // stages - 1))
+        prod.append((C, ("vfull", j % stages)))
+    wk = lambda j: (W, ("kfull", j % stages), j // stages)  # noqa: E731
+    mma = [(W, "q", 0), wk(0)]
+    for t in (0, 1):
+        if jt[t] > 0:
+            mma.append((C, ("sfull", t)))
+    mma.append((C, ("kempty", 0)))
+    for j in range(jmax):
+        mma.append((W, ("vfull", j % stages), j // stages))
+        k_next = False
+        for t in (0, 1):
+            if j < jt[t]:
+                mma.append((W, ("pfull", t), j))
+                if j + 1 == jt[t]:
+                    mma.append((C, ("ofinal", t)))
+                else:
+                    if not k_next:
+                        mma.append(wk(j + 1))
+                    k_next = True
+                    mma.append((C, ("sfull", t)))
+        if k_next:
+            mma.append((C, ("kempty", (j + 1) % stages)))
+        mma.append((C, ("vempty", j % stages)))
+    progs = {"producer": prod, "mma": mma}
+    for t in (0, 1):
+        g = []
+        for j in range(jt[t]):
+            g += [(W, ("sfull", t), j), (A, ("pfull", t))]
+        if jt[t] > 0:
+            g.append((W, ("ofinal", t), 0))
+        progs[f"softmax{t}"] = g
+    counts = {"q": 1}
+    counts |= {(x, i): 1 for x in ("kfull", "kempty", "vfull", "vempty") for i in range(stages)}
+    counts |= {(x, t): 1 for x in ("sfull", "pfull", "ofinal") for t in (0, 1)}
+    return progs, counts
+
+
+# ----------------------------------------------------------------------------- tests
+
+SCHEDULES = 300
+
+
+def explore(make, seeds=SCHEDULES):
+    for seed in range(seeds):
+        progs, counts = make()
+        run(progs, counts, random.Random(seed))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7])
+def test_dq_protocol(n):
+    explore(lambda: dq_protocol(n))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7])
+def test_dkv_protocol(n):
+    explore(lambda: dkv_protocol(n))
+
+
+@pytest.mark.parametrize("stages", [2, 4])  # d = 128 and d = 64
+@pytest.mark.parametrize("j0,j1", [(1, 1), (1, 2), (2, 3), (3, 3), (4, 5), (0, 1), (6, 7)])
+def test_fwd_protocol(j0, j1, stages):
+    explore(lambda: fwd_protocol(j0, j1, stages))
+
+
+def test_model_catches_a_barrier_two_phases_ahead():
+    """The dQ protocol with one dS barrier per warpgroup (instead of one per block parity) lets
+    the elementwise warps complete block j+1 before the MMA warp waits for block j: the model
+    must find that schedule."""
+    with pytest.raises(Hazard):
+        explore(lambda: dq_protocol(6, e_per_parity=False))
+
+
+def test_model_catches_a_deadlock():
+    """A producer that waits for the release of the stage it is about to fill deadlocks."""
+    progs = {"producer": [(W, "empty", 0), (C, "full")], "consumer": [(W, "full", 0), (C, "empty")]}
+    with pytest.raises(Hazard, match="deadlock"):
+        run(progs, {"empty": 1, "full": 1}, random.Random(0))
