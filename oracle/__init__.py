@@ -5,9 +5,10 @@ import this package.  The library under test never imports it, and it imports no
 the library.  The arithmetic lives in ``oracle.c`` (plain C, fp64); this module only builds
 that file with gcc, marshals numpy arrays into it and splits work across host threads.
 
-Every function takes arrays shaped ``[B, H, N, d]`` (``[N, d]`` for the ``*_head`` forms),
-upcasts them exactly to float64 and returns float64 arrays.  ``lse`` is the natural-log
-log-sum-exp of the scaled logits, shaped ``[B, H, N]``.
+Every function takes arrays shaped ``[B, H, N, d]`` (``[N, d]`` for the ``*_head`` forms,
+packed ``[total, heads, d]`` for ``attention_varlen``), upcasts them exactly to float64 and
+returns float64 arrays.  ``lse`` is the natural-log log-sum-exp of the scaled logits, shaped
+``[B, H, N]`` (``[H, total_q]`` for ``attention_varlen``).
 
 Parity status of each function (which checks pin it) is listed in the tests
 ``tests/test_oracle_pins.py``; every function here is pinned.
@@ -58,7 +59,10 @@ def _load():
             lib.oracle_attention_fwd.argtypes = [i, i, i, d, i, _dp, _dp, _dp, _dp, _dp, i]
             lib.oracle_attention_bwd.argtypes = [i, i, i, d, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                                  _dp, _dp, _dp, i]
+            lib.oracle_attention_rect_head.argtypes = [i, i, i, d, i, _dp, _dp, _dp, _dp, _dp,
+                                                       _dp, _dp, _dp, _dp, _dp]
             for f in (lib.oracle_attention_fwd_head, lib.oracle_attention_bwd_head,
+                      lib.oracle_attention_rect_head,
                       lib.oracle_attention_fwd_tiled_head, lib.oracle_attention_rows_head,
                       lib.oracle_attention_fwd, lib.oracle_attention_bwd):
                 f.restype = ctypes.c_int
@@ -171,4 +175,73 @@ def attention_rows_head(q, k, v, do, scale: float, causal: bool, qrows, krows,
         qr.ctypes.data_as(_ip), _p(out["o"]), _p(out["lse"]), _p(out["delta"]), _p(out["dq"]), nk,
         kr.ctypes.data_as(_ip), _p(out["dk"]), _p(out["dv"]), nthreads or default_threads()),
         "rows_head")
+    return out
+
+
+def attention_rect_head(q, k, v, scale: float, causal: bool, do=None):
+    """One head with Nq query rows [Nq, d] and Nk key rows [Nk, d]; causal is aligned to the
+    bottom-right corner (key j visible to query i iff j <= i + Nk - Nq).  Returns dict o, lse
+    (and, with do, delta, dq, dk, dv)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Nq, d = q.shape
+    Nk = k.shape[0]
+    out = {"o": np.empty((Nq, d)), "lse": np.empty(Nq)}
+    if do is not None:
+        do = _f64(do)
+        out |= {"delta": np.empty(Nq), "dq": np.empty((Nq, d)), "dk": np.empty((Nk, d)),
+                "dv": np.empty((Nk, d))}
+    g = out.get
+    _check(_load().oracle_attention_rect_head(
+        Nq, Nk, d, float(scale), int(bool(causal)), _p(q), _p(k), _p(v), _p(do), _p(out["o"]),
+        _p(out["lse"]), _p(g("delta")), _p(g("dq")), _p(g("dk")), _p(g("dv"))), "rect_head")
+    return out
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool, do=None,
+                     nthreads: int | None = None):
+    """Packed variable-length batch with grouped key/value heads.
+
+    q (and do) are ``[total_q, H, d]``, k and v ``[total_k, Hkv, d]``; sequence b owns query
+    rows ``cu_seqlens_q[b]:cu_seqlens_q[b+1]`` and key rows ``cu_seqlens_k[b]:cu_seqlens_k[b+1]``.
+    Query head h attends to key/value head ``h // (H // Hkv)``.  Each (sequence, head) pair is
+    one ``attention_rect_head`` problem.  The gradients of a shared key/value head are the sum
+    over the query heads that read it (chain rule), added in head order.
+    Returns dict o ``[total_q, H, d]``, lse ``[H, total_q]`` and, with do, delta
+    ``[H, total_q]``, dq ``[total_q, H, d]``, dk and dv ``[total_k, Hkv, d]``.
+    """
+    import concurrent.futures as cf
+
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    do = None if do is None else _f64(do)
+    cu_q = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    total_q, H, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if H % Hkv or len(cu_q) != len(cu_k):
+        raise ValueError("H must be a multiple of Hkv; cu_seqlens must have equal lengths")
+    G = H // Hkv
+    jobs = [(b, h) for b in range(len(cu_q) - 1) for h in range(H)]
+
+    def one(job):
+        b, h = job
+        qs, ks = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        hk = h // G
+        return attention_rect_head(q[qs, h], k[ks, hk], v[ks, hk], scale, causal,
+                                   None if do is None else do[qs, h])
+
+    with cf.ThreadPoolExecutor(max_workers=nthreads or default_threads()) as ex:
+        res = list(ex.map(one, jobs))
+    out = {"o": np.zeros((total_q, H, d)), "lse": np.zeros((H, total_q))}
+    if do is not None:
+        out |= {"delta": np.zeros((H, total_q)), "dq": np.zeros((total_q, H, d)),
+                "dk": np.zeros((total_k, Hkv, d)), "dv": np.zeros((total_k, Hkv, d))}
+    for (b, h), r in zip(jobs, res):
+        qs, ks = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        out["o"][qs, h] = r["o"]
+        out["lse"][h, qs] = r["lse"]
+        if do is not None:
+            out["delta"][h, qs] = r["delta"]
+            out["dq"][qs, h] = r["dq"]
+            out["dk"][ks, h // G] += r["dk"]
+            out["dv"][ks, h // G] += r["dv"]
     return out

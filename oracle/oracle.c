@@ -392,6 +392,90 @@ int oracle_attention_rows_head(int N, int d, double scale, int causal, const dou
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Algorithm 0 and its backward for one head with Nq query rows and Nk key rows (Nq != Nk
+ * allowed).  [IO-essay] places the kernel under chunked prefill: a chunk of the last Nq
+ * queries of a sequence attends to all Nk keys of the sequence so far, with the causal mask
+ * inside the chunk.  So the causal mask is aligned to the bottom-right corner:
+ *   key j is visible to query i  iff  j <= i + (Nk - Nq),
+ * which is the square mask of [Triton-FA2] "개선 3" when Nq == Nk.
+ * A query row that sees no key (Nq > Nk, or Nk == 0) has an empty softmax: its P row is 0,
+ * O_i = 0 and lse_i = log(0) = -inf, and it contributes no gradient.
+ * dO == NULL computes the forward only (dQ, dK, dV, delta are then ignored).
+ * ------------------------------------------------------------------------------------- */
+int oracle_attention_rect_head(int Nq, int Nk, int d, double scale, int causal,
+                               const double* Q, const double* K, const double* V,
+                               const double* dO, double* O, double* lse, double* delta,
+                               double* dQ, double* dK, double* dV)
+{
+    if (Nq < 0 || Nk < 0 || d < 1 || !O || !lse) return ORACLE_EINVAL;
+    if (dO && (!dQ || !dK || !dV)) return ORACLE_EINVAL;
+    const long nq = Nq, nk = Nk, off = (long)Nk - (long)Nq;
+    double* P = (double*)malloc(sizeof(double) * (nq * nk + 1));
+    double* dP = dO ? (double*)malloc(sizeof(double) * (nq * nk + 1)) : NULL;
+    if (!P || (dO && !dP)) { free(P); free(dP); return ORACLE_ENOMEM; }
+    /* S = scale Q K^T with the mask, then P = softmax(S) row by row */
+    for (long i = 0; i < nq; ++i) {
+        double* Pi = P + i * nk;
+        double m = -INFINITY;
+        for (long j = 0; j < nk; ++j) {
+            if (causal && j > i + off) { Pi[j] = -INFINITY; continue; }
+            double sij = 0.0;
+            for (int c = 0; c < d; ++c) sij += Q[i * d + c] * K[j * d + c];
+            Pi[j] = scale * sij;
+            if (Pi[j] > m) m = Pi[j];
+        }
+        if (m == -INFINITY) { /* no visible key */
+            for (long j = 0; j < nk; ++j) Pi[j] = 0.0;
+            lse[i] = -INFINITY;
+        } else {
+            double l = 0.0;
+            for (long j = 0; j < nk; ++j) { Pi[j] = exp(Pi[j] - m); l += Pi[j]; }
+            for (long j = 0; j < nk; ++j) Pi[j] /= l;
+            lse[i] = m + log(l);
+        }
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (long j = 0; j < nk; ++j) acc += Pi[j] * V[j * d + c];
+            O[i * d + c] = acc;
+        }
+    }
+    if (dO) {
+        /* dP = dO V^T ; Delta_i = sum_j P_ij dP_ij ; dS = P o (dP - Delta) */
+        for (long i = 0; i < nq; ++i) {
+            double dl = 0.0;
+            for (long j = 0; j < nk; ++j) {
+                double a = 0.0;
+                for (int c = 0; c < d; ++c) a += dO[i * d + c] * V[j * d + c];
+                dP[i * nk + j] = a;
+                dl += P[i * nk + j] * a;
+            }
+            if (delta) delta[i] = dl;
+            for (long j = 0; j < nk; ++j) dP[i * nk + j] = P[i * nk + j] * (dP[i * nk + j] - dl);
+        }
+        /* dV = P^T dO ; dK = scale dS^T Q ; dQ = scale dS K */
+        for (long j = 0; j < nk; ++j)
+            for (int c = 0; c < d; ++c) {
+                double av = 0.0, ak = 0.0;
+                for (long i = 0; i < nq; ++i) {
+                    av += P[i * nk + j] * dO[i * d + c];
+                    ak += dP[i * nk + j] * Q[i * d + c];
+                }
+                dV[j * d + c] = av;
+                dK[j * d + c] = scale * ak;
+            }
+        for (long i = 0; i < nq; ++i)
+            for (int c = 0; c < d; ++c) {
+                double aq = 0.0;
+                for (long j = 0; j < nk; ++j) aq += dP[i * nk + j] * K[j * d + c];
+                dQ[i * d + c] = scale * aq;
+            }
+    }
+    free(P);
+    free(dP);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------------
  * Batched drivers: heads are independent; one head per worker thread at a time.
  * Arrays are [BH, N, d] (lse and delta [BH, N]), contiguous.
  * ------------------------------------------------------------------------------------- */

@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_varlen_pins as vpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -28,6 +29,12 @@ MUTATIONS = [
     ("tiled_no_rescale", "(l[i] * a_old * O[i * d + c] + a_new * PV[c]) / lnew",
      "(l[i] * O[i * d + c] + a_new * PV[c]) / lnew"),
     ("rows_delta", "ds = p * (jb->dp[j] - delta_i)", "ds = p * jb->dp[j]"),
+    ("rect_offset_sign", "if (causal && j > i + off)", "if (causal && j > i - off)"),
+    ("rect_top_left_mask", "if (causal && j > i + off)", "if (causal && j > i)"),
+    ("rect_empty_row_lse", "lse[i] = -INFINITY;\n        } else {", "lse[i] = 0.0;\n        } else {"),
+    ("rect_dk_unscaled", "dK[j * d + c] = scale * ak;", "dK[j * d + c] = ak;"),
+    ("rect_missing_delta", "P[i * nk + j] * (dP[i * nk + j] - dl)", "P[i * nk + j] * dP[i * nk + j]"),
+    ("rect_dv_uses_ds", "av += P[i * nk + j] * dO[i * d + c];", "av += dP[i * nk + j] * dO[i * d + c];"),
 ]
 
 # Pin calls run against each mutant; each is (callable, args).
@@ -43,6 +50,12 @@ PIN_CALLS = [
     (pins.test_backward_matches_central_finite_differences, (False, 5, 4)),
     (pins.test_delta_identity_and_gradient_sums, (True,)),
     (pins.test_rows_mode_equals_full_materialisation, (True,)),
+    (vpins.test_rect_q_zero_closed_form, (7, 3, True)),
+    (vpins.test_rect_q_zero_closed_form, (3, 7, True)),
+    (vpins.test_rect_is_the_tail_chunk_of_a_square_causal_problem, (9, 4)),
+    (vpins.test_rect_backward_matches_central_finite_differences, (3, 5, True)),
+    (vpins.test_rect_backward_matches_central_finite_differences, (4, 6, False)),
+    (vpins.test_empty_sequences_give_zero_outputs_and_gradients, ()),
 ]
 
 
@@ -67,7 +80,7 @@ def test_pins_catch_planted_mistake(name, text, repl, monkeypatch):
         mutant = ctypes.CDLL(lib_path)
         for fn in ("oracle_attention_fwd_head", "oracle_attention_bwd_head",
                    "oracle_attention_fwd_tiled_head", "oracle_attention_rows_head",
-                   "oracle_attention_fwd", "oracle_attention_bwd"):
+                   "oracle_attention_fwd", "oracle_attention_bwd", "oracle_attention_rect_head"):
             f = getattr(mutant, fn)
             f.argtypes = getattr(real, fn).argtypes
             f.restype = ctypes.c_int
