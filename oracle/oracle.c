@@ -452,23 +452,22 @@ int oracle_attention_rect_head(int Nq, int Nk, int d, double scale, int causal,
             if (delta) delta[i] = dl;
             for (long j = 0; j < nk; ++j) dP[i * nk + j] = P[i * nk + j] * (dP[i * nk + j] - dl);
         }
-        /* dV = P^T dO ; dK = scale dS^T Q ; dQ = scale dS K */
-        for (long j = 0; j < nk; ++j)
-            for (int c = 0; c < d; ++c) {
-                double av = 0.0, ak = 0.0;
-                for (long i = 0; i < nq; ++i) {
-                    av += P[i * nk + j] * dO[i * d + c];
-                    ak += dP[i * nk + j] * Q[i * d + c];
+        /* dV = P^T dO ; dK = scale dS^T Q ; dQ = scale dS K  (sums over i and j, row by row) */
+        for (long x = 0; x < nk * d; ++x) { dV[x] = 0.0; dK[x] = 0.0; }
+        for (long i = 0; i < nq; ++i) {
+            double* dQi = dQ + i * d;
+            for (int c = 0; c < d; ++c) dQi[c] = 0.0;
+            for (long j = 0; j < nk; ++j) {
+                const double p = P[i * nk + j], ds = dP[i * nk + j];
+                for (int c = 0; c < d; ++c) {
+                    dV[j * d + c] += p * dO[i * d + c];
+                    dK[j * d + c] += ds * Q[i * d + c];
+                    dQi[c] += ds * K[j * d + c];
                 }
-                dV[j * d + c] = av;
-                dK[j * d + c] = scale * ak;
             }
-        for (long i = 0; i < nq; ++i)
-            for (int c = 0; c < d; ++c) {
-                double aq = 0.0;
-                for (long j = 0; j < nk; ++j) aq += dP[i * nk + j] * K[j * d + c];
-                dQ[i * d + c] = scale * aq;
-            }
+        }
+        for (long x = 0; x < nk * d; ++x) dK[x] *= scale;
+        for (long x = 0; x < nq * d; ++x) dQ[x] *= scale;
     }
     free(P);
     free(dP);

@@ -32,9 +32,9 @@ MUTATIONS = [
     ("rect_offset_sign", "if (causal && j > i + off)", "if (causal && j > i - off)"),
     ("rect_top_left_mask", "if (causal && j > i + off)", "if (causal && j > i)"),
     ("rect_empty_row_lse", "lse[i] = -INFINITY;\n        } else {", "lse[i] = 0.0;\n        } else {"),
-    ("rect_dk_unscaled", "dK[j * d + c] = scale * ak;", "dK[j * d + c] = ak;"),
+    ("rect_dk_unscaled", "for (long x = 0; x < nk * d; ++x) dK[x] *= scale;", ""),
     ("rect_missing_delta", "P[i * nk + j] * (dP[i * nk + j] - dl)", "P[i * nk + j] * dP[i * nk + j]"),
-    ("rect_dv_uses_ds", "av += P[i * nk + j] * dO[i * d + c];", "av += dP[i * nk + j] * dO[i * d + c];"),
+    ("rect_dv_uses_ds", "dV[j * d + c] += p * dO[i * d + c];", "dV[j * d + c] += ds * dO[i * d + c];"),
 ]
 
 # Pin calls run against each mutant; each is (callable, args).
