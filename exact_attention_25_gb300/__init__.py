@@ -15,6 +15,8 @@ from ._lib import FA_BF16, FA_F32, FaError, check, load
 __all__ = [
     "FA_BF16", "FA_F32", "FaError", "load", "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_causal_block_counts", "forward", "backward",
+    "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "forward_varlen",
+    "backward_varlen",
 ]
 
 
@@ -141,4 +143,87 @@ def backward(q, k, v, o, do, lse, scale: float | None = None, causal: bool = Fal
                                 device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, workspace, stream, impl)
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------- packed batches
+
+def _varlen_shapes(q, k, cu_q, cu_k):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("packed tensors must be [total, heads, d]")
+    if cu_q.dtype != _torch_int32() or cu_k.dtype != _torch_int32():
+        raise TypeError("cu_seqlens must be int32")
+    if cu_q.dim() != 1 or cu_k.dim() != 1 or cu_q.numel() != cu_k.numel() or cu_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be 1-D with B + 1 entries each")
+    total_q, H, d = (int(x) for x in q.shape)
+    total_k, Hkv = int(k.shape[0]), int(k.shape[1])
+    return cu_q.numel() - 1, total_q, total_k, H, Hkv, d
+
+
+def _torch_int32():
+    import torch
+
+    return torch.int32
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, scale: float, causal: bool, stream=None) -> None:
+    """C ``fa_fwd_varlen``: q, o [total_q, H, d]; k, v [total_k, Hkv, d] (bf16); lse
+    [H, total_q] fp32 (or None); cu_seqlens_* int32 [B + 1] on the device."""
+    _check_tensors(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
+    B, total_q, total_k, H, Hkv, d = _varlen_shapes(q, k, cu_seqlens_q, cu_seqlens_k)
+    check(load().fa_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
+        int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, H, Hkv, d, float(scale),
+        int(bool(causal)), _stream(stream)))
+
+
+def fa_bwd_varlen_workspace_bytes(total_q: int, H: int, d: int) -> int:
+    return int(load().fa_bwd_varlen_workspace_bytes(total_q, H, d))
+
+
+def fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                  max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool, workspace,
+                  stream=None) -> None:
+    """C ``fa_bwd_varlen``: writes dq [total_q, H, d], dk, dv [total_k, Hkv, d] in place."""
+    _check_tensors(q, k, v, o, do, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k)
+    B, total_q, total_k, H, Hkv, d = _varlen_shapes(q, k, cu_seqlens_q, cu_seqlens_k)
+    nbytes = workspace.numel() * workspace.element_size()
+    check(load().fa_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q), int(max_seqlen_k), total_q,
+        total_k, H, Hkv, d, float(scale), int(bool(causal)), _ptr(workspace), nbytes,
+        _stream(stream)))
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                   scale: float | None = None, causal: bool = False, stream=None):
+    """Allocate O ([total_q, H, d]) and LSE ([H, total_q] fp32) and run fa_fwd_varlen."""
+    import torch
+
+    d = int(q.shape[-1])
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((int(q.shape[1]), int(q.shape[0])), dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
+                  causal, stream)
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                    max_seqlen_k: int, scale: float | None = None, causal: bool = False,
+                    stream=None, workspace=None):
+    """Allocate dQ, dK, dV (and the workspace unless given) and run fa_bwd_varlen."""
+    import torch
+
+    total_q, H, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = d ** -0.5
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_varlen_workspace_bytes(total_q, H, d), dtype=torch.uint8,
+                                device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  max_seqlen_k, scale, causal, workspace, stream)
     return dq, dk, dv

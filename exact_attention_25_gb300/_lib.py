@@ -1,6 +1,7 @@
 """ctypes binding of libfa.so.  Argument marshalling only: every step of the computation runs
 in the library's CUDA kernels.  Tensors are torch CUDA tensors (torch supplies device memory
-and streams); shapes are [B, H, N, d], contiguous.  Raises if the library is missing: there
+and streams); shapes are [B, H, N, d] (or, for the variable-length calls, packed
+[total, heads, d]), contiguous.  Raises if the library is missing: there
 is no fallback implementation."""
 from __future__ import annotations
 
@@ -22,7 +23,8 @@ EXPORTS = (
     "fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_stage", "fa_fwd_impl", "fa_bwd_impl",
     "fa_bwd_noalloc", "fa_debug_set_flags",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_status_string", "fa_last_error",
-    "fa_causal_block_counts", "fa_version",
+    "fa_causal_block_counts", "fa_version", "fa_fwd_varlen", "fa_bwd_varlen_workspace_bytes",
+    "fa_bwd_varlen",
 )
 
 _lock = threading.Lock()
@@ -59,6 +61,11 @@ def load(path: str | None = None):
                                      sz, i, vp]
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.fa_bwd_noalloc.restype = ctypes.c_int
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_bwd_varlen_workspace_bytes.argtypes = [i, i, i]
+        lib.fa_bwd_varlen_workspace_bytes.restype = sz
+        lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                      i, i, f, i, vp, sz, vp]
         lib.fa_device_status.argtypes = [vp]
         lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.fa_set_wait_limit_ns.restype = None
@@ -71,7 +78,7 @@ def load(path: str | None = None):
         lib.fa_causal_block_counts.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
         lib.fa_version.restype = ctypes.c_char_p
         for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_bwd_stage", "fa_device_status",
-                   "fa_causal_block_counts"):
+                   "fa_causal_block_counts", "fa_fwd_varlen", "fa_bwd_varlen"):
             getattr(lib, fn).restype = ctypes.c_int
         if path is None:
             _lib = lib

@@ -91,15 +91,19 @@ int get_encoder()
     return FA_OK;
 }
 
-// 3-D view [BH, N, d] of a bf16 tensor; box = 64 columns (one 128-byte swizzle panel) x
-// `rows` rows x 1 head.  Rows beyond N read as zero.
-int make_map(CUtensorMap* m, const void* base, int BH, int N, int d, int rows)
+// 3-D view of a bf16 tensor for 128-row tiles of one head; box = 64 columns (one 128-byte
+// swizzle panel) x `rows` rows x 1 head.  Fixed layout [heads, R, d]: dimensions (d, R, heads);
+// packed layout [R, heads, d] (token by token): dimensions (d, heads, R).  Rows beyond R read
+// as zero.
+int make_map(CUtensorMap* m, const void* base, long long heads, long long R, int d, int rows,
+             bool packed)
 {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+    const cuuint64_t dd = static_cast<cuuint64_t>(d);
+    const cuuint64_t nh = static_cast<cuuint64_t>(heads), nr = static_cast<cuuint64_t>(R);
+    cuuint64_t dims[3] = {dd, packed ? nh : nr, packed ? nr : nh};
+    cuuint64_t strides[2] = {dd * 2, (packed ? nh : nr) * dd * 2};
+    cuuint32_t box[3] = {64, packed ? 1u : static_cast<cuuint32_t>(rows),
+                         packed ? static_cast<cuuint32_t>(rows) : 1u};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -127,6 +131,36 @@ int check_common(int B, int H, int N, int d, float scale, int causal, int dtype)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Layout of the fixed-length entry points: [B, H, N, d] for every tensor, [B, H, N] statistics.
+fa::Layout fixed_layout(int B, int H, int N, int d)
+{
+    fa::Layout L{};
+    L.cu_q = L.cu_k = nullptr;
+    L.B = B; L.H = H; L.Hkv = H;
+    L.Nq = L.Nk = N;
+    L.Rq = L.Rk = N;
+    L.q_rs = L.k_rs = d;
+    L.q_hs = L.k_hs = static_cast<long long>(N) * d;
+    return L;
+}
+
+// The four bf16 maps of the tensor-core kernels: q, k, v, and (backward) dout.
+int make_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, const void* dout,
+              const fa::Layout& L, int d)
+{
+    int rc = get_encoder();
+    if (rc) return rc;
+    const bool packed = L.cu_q != nullptr;
+    const long long nhq = packed ? L.H : static_cast<long long>(L.B) * L.H;
+    const long long nhk = packed ? L.Hkv : static_cast<long long>(L.B) * L.Hkv;
+    if ((rc = make_map(&maps[0], q, nhq, L.Rq, d, 128, packed)) ||
+        (rc = make_map(&maps[1], k, nhk, L.Rk, d, 128, packed)) ||
+        (rc = make_map(&maps[2], v, nhk, L.Rk, d, 128, packed)))
+        return rc;
+    if (dout && (rc = make_map(&maps[3], dout, nhq, L.Rq, d, 128, packed))) return rc;
+    return FA_OK;
+}
+
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int N, int d, float scale, int causal, int dtype, int impl, void* stream)
 {
@@ -145,16 +179,14 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     p.debug_flags = g_debug_flags;
+    p.L = fixed_layout(B, H, N, d);
     cudaError_t e;
     if (dtype == FA_F32 || impl == 1) {
         e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st);
     } else {
-        if ((rc = get_encoder())) return rc;
-        CUtensorMap tq, tk, tv;
-        if ((rc = make_map(&tq, q, p.BH, N, d, 128)) || (rc = make_map(&tk, k, p.BH, N, d, 128)) ||
-            (rc = make_map(&tv, v, p.BH, N, d, 128)))
-            return rc;
-        e = fa::launch_fwd_tc(d, tq, tk, tv, p, st);
+        CUtensorMap maps[4];
+        if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d))) return rc;
+        e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return FA_OK;
@@ -194,6 +226,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.N = N; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     p.debug_flags = g_debug_flags;
+    p.L = fixed_layout(B, H, N, d);
     const int is_f32 = dtype == FA_F32;
     cudaError_t e = cudaSuccess;
     if (stage <= 0) {
@@ -204,12 +237,9 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     if (is_f32 || impl == 1) {
         e = fa::launch_bwd_simt(d, is_f32, p, st);
     } else {
-        if ((rc = get_encoder())) return rc;
         // maps: q, k, v, dout (all 128-row boxes)
         CUtensorMap maps[4];
-        const void* srcs[4] = {q, k, v, dout};
-        for (int i = 0; i < 4; ++i)
-            if ((rc = make_map(&maps[i], srcs[i], p.BH, N, d, 128))) return rc;
+        if ((rc = make_maps(maps, q, k, v, dout, p.L, d))) return rc;
         if (stage < 0 || stage == 1) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
         if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq_tc(d, maps, p, st);
     }
@@ -331,6 +361,131 @@ int fa_causal_block_counts(int q_block, int Br, int Bc, int N, int* n_full, int*
 const char* fa_version(void) { return "fa-gb300 0.1 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Packed variable-length batches with grouped key/value heads (fa_fwd_varlen, fa_bwd_varlen).
+// ---------------------------------------------------------------------------------------
+namespace {
+
+int check_varlen(const int* cu_q, const int* cu_k, int B, int* max_q, int* max_k, int total_q,
+                 int total_k, int H, int Hkv, int d, float scale, int causal)
+{
+    if (B < 1 || H < 1 || Hkv < 1) return fail(FA_ERR_INVALID_ARG, "B, H and Hkv must be >= 1");
+    if (H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H must be a multiple of Hkv");
+    if (total_q < 1 || total_k < 1 || *max_q < 1 || *max_k < 1)
+        return fail(FA_ERR_INVALID_ARG, "total_q, total_k, max_seqlen_q and max_seqlen_k must be >= 1");
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED_D, "d must be 64 or 128");
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+        return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    if (!cu_q || !cu_k) return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must be non-null");
+    if ((reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u))
+        return fail(FA_ERR_MISALIGNED, "cu_seqlens_q and cu_seqlens_k must be 4-byte aligned");
+    if (static_cast<long long>(total_q) * H * d >= (1LL << 31) ||
+        static_cast<long long>(total_k) * Hkv * d >= (1LL << 31))
+        return fail(FA_ERR_TOO_LARGE, "total_q*H*d and total_k*Hkv*d must be < 2^31");
+    // no sequence is longer than its packed tensor
+    if (*max_q > total_q) *max_q = total_q;
+    if (*max_k > total_k) *max_k = total_k;
+    if (static_cast<long long>(B) * H * ((*max_q + 127) / 128) >= (1LL << 31) ||
+        static_cast<long long>(B) * Hkv * ((*max_k + 127) / 128) >= (1LL << 31))
+        return fail(FA_ERR_TOO_LARGE, "B*H*ceil(max_seqlen/128) must be < 2^31");
+    return FA_OK;
+}
+
+fa::Layout packed_layout(const int* cu_q, const int* cu_k, int B, int max_q, int max_k,
+                         int total_q, int total_k, int H, int Hkv, int d)
+{
+    fa::Layout L{};
+    L.cu_q = cu_q; L.cu_k = cu_k;
+    L.B = B; L.H = H; L.Hkv = Hkv;
+    L.Nq = max_q; L.Nk = max_k;
+    L.Rq = total_q; L.Rk = total_k;
+    L.q_rs = static_cast<long long>(H) * d; L.q_hs = d;
+    L.k_rs = static_cast<long long>(Hkv) * d; L.k_hs = d;
+    return L;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                             int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H,
+                             int Hkv, int d, float scale, int causal, void* stream)
+{
+    int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_seqlen_q, &max_seqlen_k, total_q,
+                          total_k, H, Hkv, d, scale, causal);
+    if (rc) return rc;
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    fa::FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.N = total_q; p.BH = H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
+                        total_k, H, Hkv, d);
+    CUtensorMap maps[4];
+    if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d))) return rc;
+    cudaError_t e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return FA_OK;
+}
+
+extern "C" size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int d)
+{
+    if (total_q < 1 || H < 1 || (d != 64 && d != 128)) return 0;
+    const size_t rows = static_cast<size_t>(H) * total_q;
+    return 2 * align256(rows * 4) + 256;
+}
+
+extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                             int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H,
+                             int Hkv, int d, float scale, int causal, void* workspace,
+                             size_t workspace_bytes, void* stream)
+{
+    int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_seqlen_q, &max_seqlen_k, total_q,
+                          total_k, H, Hkv, d, scale, causal);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+        return fail(FA_ERR_INVALID_ARG, "every tensor pointer must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA_ERR_MISALIGNED, "tensors must be 16-byte aligned (lse 4-byte)");
+    const size_t need = fa_bwd_varlen_workspace_bytes(total_q, H, d);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    fa::BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    const size_t rows = static_cast<size_t>(H) * total_q;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.delta = reinterpret_cast<float*>(ws);
+    p.lse2 = reinterpret_cast<float*>(ws + align256(rows * 4));
+    p.N = total_q; p.BH = H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
+                        total_k, H, Hkv, d);
+    CUtensorMap maps[4];
+    if ((rc = make_maps(maps, q, k, v, dout, p.L, d))) return rc;
+    cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, st, di->sms);
+    if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return FA_OK;
+}
 
 // ---------------------------------------------------------------------------------------
 // fa_bwd_noalloc: the backward with its scratch in a fixed device array of this library.

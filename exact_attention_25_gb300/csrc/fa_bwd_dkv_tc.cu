@@ -65,7 +65,7 @@ __device__ __forceinline__ void dkv_issue_acc(uint32_t acc, uint32_t buf, uint64
                  idesc, (first && ks == 0) ? 0u : 1u);
 }
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     fa_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -99,19 +99,31 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int N = p.N;
-    const int nblk = (N + 127) / 128;
+    const Layout& L = p.L;
+    constexpr bool packed = PACKED;  // tensors stored token by token
+    const int kblk_max = (L.Nk + 127) / 128;
     // Head-major order; within a head the first key blocks (most query blocks under the causal
     // mask) go first.
-    const int bh = static_cast<int>(blockIdx.x) / nblk;
-    const int kb = static_cast<int>(blockIdx.x) % nblk;
-    const int k0 = kb * 128, k1 = min(N, k0 + 128);
-    int s_begin = 0;  // query blocks [s_begin, nblk) see a key of [k0, k1)
+    const int bkv = static_cast<int>(blockIdx.x) / kblk_max;
+    const int b = bkv / L.Hkv, hk = bkv % L.Hkv;
+    const int kb = static_cast<int>(blockIdx.x) % kblk_max;
+    const SeqRows sr = seq_rows<PACKED>(L, b);
+    const int nq = sr.nq, nk = sr.nk;
+    const int k0 = kb * 128, k1 = min(nk, k0 + 128);
+    if (k0 >= nk) return;  // beyond this sequence's keys (whole CTA, before any sync)
+    const int khead = k_head_index<PACKED>(L, b, hk);
+    const int G = PACKED ? L.H / L.Hkv : 1;  // query heads sharing this key/value head
+    const int shift = PACKED ? nk - nq : 0;  // bottom-right causal alignment
+    const int nqblk = (nq + 127) / 128;
+    int s_begin = 0;  // query blocks [s_begin, nqblk) see a key of [k0, k1)
     if (p.causal)
-        while (s_begin < nblk &&
-               causal_tile_class(s_begin * 128, min(N, s_begin * 128 + 128), k0, k1) == kTileSkip)
+        while (s_begin < nqblk &&
+               causal_class_shifted(s_begin * 128, min(nq, s_begin * 128 + 128), k0, k1, shift) ==
+                   kTileSkip)
             ++s_begin;
-    const int n_it = nblk - s_begin;
+    // Streamed blocks: for each query head g of the group, query blocks s_begin.. in order.
+    const int n_per = nqblk - s_begin;
+    const int n_it = G * n_per;
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_res, 1);
@@ -154,20 +166,22 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         // ------------------------------------------------------------- TMA producer
         mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn) {
-            tma_load_3d_w(sK + pn * C::PANEL_BYTES, &tm_k, &bar_res, 64 * pn, k0, bh);
-            tma_load_3d_w(sV + pn * C::PANEL_BYTES, &tm_v, &bar_res, 64 * pn, k0, bh);
+            tma_load_rows_w(sK + pn * C::PANEL_BYTES, &tm_k, &bar_res, 64 * pn, sr.k0 + k0, khead, packed);
+            tma_load_rows_w(sV + pn * C::PANEL_BYTES, &tm_v, &bar_res, 64 * pn, sr.k0 + k0, khead, packed);
         }
         int issued_q = 0, issued_g = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int row = (s_begin + it) * 128;
+            const int g = PACKED ? it / n_per : 0;
+            const int row = sr.q0 + (s_begin + it - g * n_per) * 128;
+            const int qhead = q_head_index<PACKED>(L, b, hk * G + g);
             // Q first: S^T(it) is issued before dP^T(it)
             const int sq = it % C::QSTAGES;
             if (!warp_wait_all(&bar_qempty[sq], ((it / C::QSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
                 break;
             mbar_arrive_expect_tx_w(&bar_qfull[sq], C::TILE_BYTES);
             for (int pn = 0; pn < C::PANELS; ++pn)
-                tma_load_3d_w(sQ + sq * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_qfull[sq],
-                              64 * pn, row, bh);
+                tma_load_rows_w(sQ + sq * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_qfull[sq],
+                              64 * pn, row, qhead, packed);
             issued_q = it + 1;
             const int sg = it % C::GSTAGES;
             if (!warp_wait_all(&bar_gempty[sg], ((it / C::GSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
@@ -175,8 +189,8 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             mbar_arrive_expect_tx_w(&bar_gfull[sg], C::TILE_BYTES);
             if (!(it == 0 && (p.debug_flags & kDebugDropFirstLoad)))
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d_w(sG + sg * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_g,
-                                  &bar_gfull[sg], 64 * pn, row, bh);
+                    tma_load_rows_w(sG + sg * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_g,
+                                  &bar_gfull[sg], 64 * pn, row, qhead, packed);
             issued_g = it + 1;
         }
         // drain: no copy may still be in flight when the CTA exits
@@ -265,24 +279,26 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         const uint32_t tS = tbase + lane_base + C::COL_S + 64u * h;
         const uint32_t tDP = tbase + lane_base + C::COL_DP + 64u * h;
         const uint32_t tDV = tbase + lane_base + C::COL_DV, tDK = tbase + lane_base + C::COL_DK;
-        const size_t row_base = static_cast<size_t>(bh) * N;
-        const int krow = k0 + r;
+        const int krow = k0 + r;  // key row within the sequence
         const uint64_t c2x2 = f2_make(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int q0 = (s_begin + it) * 128;  // first query of the block
+            const int g = PACKED ? it / n_per : 0;
+            const int q0 = (s_begin + it - g * n_per) * 128;  // first query of the block
+            const size_t row_base =
+                static_cast<size_t>(q_head_index<PACKED>(L, b, hk * G + g)) * L.Rq + sr.q0;
             // stage -L2 and -Delta of this warpgroup's 64 query columns (negated, so the passes
             // below are fma / add only; queries beyond N get P = 0).  The first barrier keeps
             // the previous block's values until every thread of the warpgroup is done with them.
             named_bar_sync(1 + h, 128);
             if (r < 64) {
                 const int qi = q0 + 64 * h + r;
-                sL2[h][r] = (qi < N) ? -p.lse2[row_base + qi] : -INFINITY;
-                sDl[h][r] = (qi < N) ? -p.delta[row_base + qi] : 0.0f;
+                sL2[h][r] = (qi < nq) ? -p.lse2[row_base + qi] : -INFINITY;
+                sDl[h][r] = (qi < nq) ? -p.delta[row_base + qi] : 0.0f;
             }
             named_bar_sync(1 + h, 128);
-            const bool diag = p.causal &&
-                              causal_tile_class(q0, min(N, q0 + 128), k0, k1) == kTileMasked;
+            const bool diag = p.causal && causal_class_shifted(q0, min(nq, q0 + 128), k0, k1,
+                                                               shift) == kTileMasked;
             // ---- phase 1: P^T = exp2(c S^T - L2), written back as bf16 pairs
             if (!warp_wait_all(&bar_s, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
@@ -310,7 +326,7 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             if (diag) {  // key > query is masked
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
-                    if (krow > q0 + 64 * h + c) pv[c] = 0u;
+                    if (krow > q0 + 64 * h + c + shift) pv[c] = 0u;
             }
             {
                 uint32_t pk[32];
@@ -364,8 +380,9 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tAcc = which == 0 ? tDV : tDK;
                 const float mul = which == 0 ? 1.0f : p.scale;
-                __nv_bfloat16* dst_row =
-                    static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + (row_base + krow) * D;
+                __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) +
+                                         static_cast<size_t>(sr.k0 + krow) * L.k_rs +
+                                         static_cast<size_t>(khead) * L.k_hs;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 64; ++ch) {
                     const int c0 = h * (D / 2) + 32 * ch;
@@ -378,7 +395,7 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
                     for (int c = 0; c < 16; ++c)
                         packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
                                                 __uint_as_float(a[2 * c + 1]) * mul);
-                    if (krow < N) {
+                    if (krow < nk) {
                         uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -387,12 +404,13 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
                     }
                 }
             }
-        } else if (n_it == 0 && krow < N) {
-            // a key block that no query sees has zero gradient (cannot occur for square causal
-            // attention, kept for completeness)
+        } else if (n_it == 0 && krow < nk) {
+            // a key block that no query sees (a sequence without queries) has zero gradient
+            const size_t off = static_cast<size_t>(sr.k0 + krow) * L.k_rs +
+                               static_cast<size_t>(khead) * L.k_hs;
             for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c) {
-                static_cast<__nv_bfloat16*>(p.dk)[(row_base + krow) * D + c] = __float2bfloat16_rn(0.0f);
-                static_cast<__nv_bfloat16*>(p.dv)[(row_base + krow) * D + c] = __float2bfloat16_rn(0.0f);
+                static_cast<__nv_bfloat16*>(p.dk)[off + c] = __float2bfloat16_rn(0.0f);
+                static_cast<__nv_bfloat16*>(p.dv)[off + c] = __float2bfloat16_rn(0.0f);
             }
         }
         tc_fence_before();
@@ -405,7 +423,7 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     }
 }
 
-template <int D>
+template <int D, bool PACKED>
 static cudaError_t launch_dkv(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                               const CUtensorMap& g, const BwdParams& p, cudaStream_t st)
 {
@@ -414,22 +432,25 @@ static cudaError_t launch_dkv(const CUtensorMap& k, const CUtensorMap& v, const 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkv_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkv_tc_kernel<D, PACKED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(p.BH * ((p.N + 127) / 128));
-    fa_bwd_dkv_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, q, g, p);
+    dim3 grid(p.L.B * p.L.Hkv * ((p.L.Nk + 127) / 128));
+    fa_bwd_dkv_tc_kernel<D, PACKED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, q, g, p);
     return cudaGetLastError();
 }
 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
 cudaError_t launch_bwd_dkv_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
 {
-    if (d == 64) return launch_dkv<64>(maps[1], maps[2], maps[0], maps[3], p, st);
-    return launch_dkv<128>(maps[1], maps[2], maps[0], maps[3], p, st);
+    if (p.L.cu_q != nullptr)
+        return d == 64 ? launch_dkv<64, true>(maps[1], maps[2], maps[0], maps[3], p, st)
+                       : launch_dkv<128, true>(maps[1], maps[2], maps[0], maps[3], p, st);
+    return d == 64 ? launch_dkv<64, false>(maps[1], maps[2], maps[0], maps[3], p, st)
+                   : launch_dkv<128, false>(maps[1], maps[2], maps[0], maps[3], p, st);
 }
 
 }  // namespace fa

@@ -57,7 +57,7 @@ __device__ __forceinline__ void dq_issue_nt(uint32_t d_tmem, uint64_t adesc, uin
     }
 }
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_g,
@@ -93,19 +93,26 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int N = p.N;
-    const int nblk = (N + 127) / 128;
+    const Layout& L = p.L;
+    constexpr bool packed = PACKED;  // tensors stored token by token
+    const int qblk_max = (L.Nq + 127) / 128;
     // Head-major order; within a head the last query blocks (most key blocks under the causal
     // mask) go first.
-    const int bh = static_cast<int>(blockIdx.x) / nblk;
-    const int qb = nblk - 1 - static_cast<int>(blockIdx.x) % nblk;
-    const int q0 = qb * 128, q1 = min(N, q0 + 128);
-    int n_it = nblk;  // key blocks [0, n_it) seen by any query of [q0, q1)
+    const int bhead = static_cast<int>(blockIdx.x) / qblk_max;
+    const int b = bhead / L.H, h_q = bhead % L.H;
+    const int qb = qblk_max - 1 - static_cast<int>(blockIdx.x) % qblk_max;
+    const SeqRows sr = seq_rows<PACKED>(L, b);
+    const int nq = sr.nq, nk = sr.nk;
+    const int q0 = qb * 128, q1 = min(nq, q0 + 128);
+    if (q0 >= nq) return;  // beyond this sequence's queries (whole CTA, before any sync)
+    const int qhead = q_head_index<PACKED>(L, b, h_q);
+    const int khead = k_head_index<PACKED>(L, b, PACKED ? h_q / (L.H / L.Hkv) : h_q);
+    const int shift = PACKED ? nk - nq : 0;  // bottom-right causal alignment
+    // key blocks [0, n_it) are seen by some query of [q0, q1)
+    int n_it = (nk + 127) / 128;
     if (p.causal) {
-        n_it = 0;
-        while (n_it < nblk &&
-               causal_tile_class(q0, q1, n_it * 128, min(N, n_it * 128 + 128)) != kTileSkip)
-            ++n_it;
+        const int kend = min(nk, q1 + shift);
+        n_it = kend > 0 ? (kend + 127) / 128 : 0;
     }
 
     if (threadIdx.x == 0) {
@@ -149,12 +156,12 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         // ------------------------------------------------------------- TMA producer
         mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn) {
-            tma_load_3d_w(sQ + pn * C::PANEL_BYTES, &tm_q, &bar_res, 64 * pn, q0, bh);
-            tma_load_3d_w(sG + pn * C::PANEL_BYTES, &tm_g, &bar_res, 64 * pn, q0, bh);
+            tma_load_rows_w(sQ + pn * C::PANEL_BYTES, &tm_q, &bar_res, 64 * pn, sr.q0 + q0, qhead, packed);
+            tma_load_rows_w(sG + pn * C::PANEL_BYTES, &tm_g, &bar_res, 64 * pn, sr.q0 + q0, qhead, packed);
         }
         int issued_k = 0, issued_v = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int row = it * 128;
+            const int row = sr.k0 + it * 128;
             // V first: dP(it) is issued before S(it), and V's stage frees earlier than K's
             const int sv = it % C::VSTAGES;
             if (!warp_wait_all(&bar_vempty[sv], ((it / C::VSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
@@ -162,16 +169,16 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             mbar_arrive_expect_tx_w(&bar_vfull[sv], C::TILE_BYTES);
             if (!(it == 0 && (p.debug_flags & kDebugDropFirstLoad)))
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d_w(sV + sv * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
-                                  &bar_vfull[sv], 64 * pn, row, bh);
+                    tma_load_rows_w(sV + sv * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
+                                  &bar_vfull[sv], 64 * pn, row, khead, packed);
             issued_v = it + 1;
             const int sk = it % C::KSTAGES;
             if (!warp_wait_all(&bar_kempty[sk], ((it / C::KSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
                 break;
             mbar_arrive_expect_tx_w(&bar_kfull[sk], C::TILE_BYTES);
             for (int pn = 0; pn < C::PANELS; ++pn)
-                tma_load_3d_w(sK + sk * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[sk],
-                              64 * pn, row, bh);
+                tma_load_rows_w(sK + sk * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[sk],
+                              64 * pn, row, khead, packed);
             issued_k = it + 1;
         }
         // drain: no copy may still be in flight when the CTA exits
@@ -280,10 +287,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const uint32_t tS = tbase + lane_base + C::COL_S + 64u * h;
         const uint32_t tDP = tbase + lane_base + C::COL_DP + 64u * h;
         const uint32_t tAcc = tbase + lane_base + C::COL_ACC;
-        const size_t row_base = static_cast<size_t>(bh) * N;
-        const int qrow = q0 + r;
+        const size_t row_base = static_cast<size_t>(qhead) * L.Rq + sr.q0;
+        const int qrow = q0 + r;  // row within the sequence
         float nL2 = 0.0f, nDl = 0.0f;  // -L2 and -Delta of this thread's query row
-        if (qrow < N) {
+        if (qrow < nq) {
             nL2 = -p.lse2[row_base + qrow];
             nDl = -p.delta[row_base + qrow];
         }
@@ -293,10 +300,12 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         for (int it = 0; it < n_it; ++it) {
             const int k0 = it * 128 + 64 * h;  // first key of this warpgroup's columns
             const uint32_t tDPb = tDP + 128u * (it & 1);  // dP(it), then dS(it)
-            // element-wise mask: causal diagonal block (key > query) and keys beyond N
-            const bool diag = p.causal &&
-                              causal_tile_class(q0, q1, it * 128, min(N, it * 128 + 128)) == kTileMasked;
-            const bool tail = it * 128 + 128 > N;
+            // element-wise mask: blocks straddling the causal diagonal (key > query + shift) and
+            // keys beyond the sequence
+            const bool diag = p.causal && causal_class_shifted(q0, q1, it * 128,
+                                                               min(nk, it * 128 + 128),
+                                                               shift) == kTileMasked;
+            const bool tail = it * 128 + 128 > nk;
             // ---- phase 1: P = exp2(c S - L2) on S, which landed a block ago
             if (!warp_wait_all(&bar_s, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const int key = k0 + c;
-                    if ((diag && key > qrow) || key >= N) pv[c] = 0u;
+                    if ((diag && key > qrow + shift) || key >= nk) pv[c] = 0u;
                 }
             }
             // ---- phase 2: dS = P o (dP - Delta), bf16 pairs over the first 32 columns of dP
@@ -360,7 +369,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
         if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
             tc_fence_after();
-            __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) + (row_base + qrow) * D;
+            __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) +
+                                     static_cast<size_t>(sr.q0 + qrow) * L.q_rs +
+                                     static_cast<size_t>(qhead) * L.q_hs;
 #pragma unroll 1
             for (int ch = 0; ch < D / 64; ++ch) {
                 const int c0 = h * (D / 2) + 32 * ch;
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                 for (int c = 0; c < 16; ++c)
                     packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale,
                                             __uint_as_float(a[2 * c + 1]) * p.scale);
-                if (qrow < N) {
+                if (qrow < nq) {
                     uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -381,11 +392,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                                             packed[4 * c + 3]);
                 }
             }
-        } else if (n_it == 0 && qrow < N) {
-            // a query block that sees no key has zero gradient (cannot occur for square causal
-            // attention, kept for completeness)
+        } else if (n_it == 0 && qrow < nq) {
+            // a query block that sees no key (more queries than keys, or no keys) has zero
+            // gradient
+            const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.q_rs +
+                               static_cast<size_t>(qhead) * L.q_hs;
             for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c)
-                static_cast<__nv_bfloat16*>(p.dq)[(row_base + qrow) * D + c] = __float2bfloat16_rn(0.0f);
+                static_cast<__nv_bfloat16*>(p.dq)[off + c] = __float2bfloat16_rn(0.0f);
         }
         tc_fence_before();
     }
@@ -397,7 +410,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
 }
 
-template <int D>
+template <int D, bool PACKED>
 static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const CUtensorMap& k,
                              const CUtensorMap& v, const BwdParams& p, cudaStream_t st)
 {
@@ -406,22 +419,25 @@ static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const C
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_tc_kernel<D, PACKED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(p.BH * ((p.N + 127) / 128));
-    fa_bwd_dq_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(q, g, k, v, p);
+    dim3 grid(p.L.B * p.L.H * ((p.L.Nq + 127) / 128));
+    fa_bwd_dq_tc_kernel<D, PACKED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(q, g, k, v, p);
     return cudaGetLastError();
 }
 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
 cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
 {
-    if (d == 64) return launch_dq<64>(maps[0], maps[3], maps[1], maps[2], p, st);
-    return launch_dq<128>(maps[0], maps[3], maps[1], maps[2], p, st);
+    if (p.L.cu_q != nullptr)
+        return d == 64 ? launch_dq<64, true>(maps[0], maps[3], maps[1], maps[2], p, st)
+                       : launch_dq<128, true>(maps[0], maps[3], maps[1], maps[2], p, st);
+    return d == 64 ? launch_dq<64, false>(maps[0], maps[3], maps[1], maps[2], p, st)
+                   : launch_dq<128, false>(maps[0], maps[3], maps[1], maps[2], p, st);
 }
 
 }  // namespace fa

@@ -53,7 +53,70 @@ __host__ __device__ inline int causal_tile_class(int q0, int q1, int k0, int k1)
     return kTileMasked;
 }
 
-// Parameters of the forward kernels.  All tensors are contiguous [B*H, N, d] (LSE [B*H, N]).
+// Where the rows of one (sequence, head) problem live.  Two layouts:
+//   fixed length  q/o/dO/dQ [B, H, Nq, d], k/v/dK/dV [B, Hkv, Nk, d]: head index b*H + h (or
+//                 b*Hkv + hk), row offset 0;
+//   packed        q/o/dO/dQ [total_q, H, d], k/v/dK/dV [total_k, Hkv, d] with the sequences
+//                 back to back ("variable length", cu_q / cu_k = B+1 sequence starts): head
+//                 index h (or hk), row offset cu[b].
+// Per-row statistics (lse, Delta, base-2 LSE) are [head index][Rq].  Query head h reads key /
+// value head h / (H / Hkv) (grouped-query attention; Hkv = H is ordinary multi-head).  The
+// fixed-length layout is always square with Hkv = H: kernels compiled for it (PACKED = false)
+// take Nq == Nk and one query head per key/value head as given.
+struct Layout {
+    const int* cu_q;       // packed layout: B+1 query-row starts (device), else null
+    const int* cu_k;       // packed layout: B+1 key-row starts (device), else null
+    int B, H, Hkv;         // sequences, query heads, key/value heads (H % Hkv == 0)
+    int Nq, Nk;            // fixed: rows per sequence; packed: largest sequence (grid, clamps)
+    int Rq, Rk;            // rows per head index: fixed Nq, Nk; packed total_q, total_k
+    long long q_rs, q_hs;  // element strides of one row and one head index: q, o, dO, dQ
+    long long k_rs, k_hs;  // the same for k, v, dK, dV
+};
+
+// Rows of sequence b: global row offsets q0 / k0 and lengths nq / nk.  Packed offsets and
+// lengths are clamped to the tensors (Rq, Rk) and to Nq / Nk, so that inconsistent sequence
+// starts can never address memory outside the caller's buffers.
+struct SeqRows {
+    int q0, nq, k0, nk;
+};
+
+template <bool PACKED>
+__device__ __forceinline__ SeqRows seq_rows(const Layout& L, int b)
+{
+    SeqRows s;
+    if constexpr (!PACKED) {
+        s.q0 = 0; s.nq = L.Nq; s.k0 = 0; s.nk = L.Nk;
+        return s;
+    }
+    const int qa = min(max(L.cu_q[b], 0), L.Rq), qb = min(max(L.cu_q[b + 1], qa), L.Rq);
+    const int ka = min(max(L.cu_k[b], 0), L.Rk), kb = min(max(L.cu_k[b + 1], ka), L.Rk);
+    s.q0 = qa; s.nq = min(qb - qa, L.Nq);
+    s.k0 = ka; s.nk = min(kb - ka, L.Nk);
+    return s;
+}
+
+template <bool PACKED>
+__device__ __forceinline__ int q_head_index(const Layout& L, int b, int h)
+{
+    return PACKED ? h : b * L.H + h;
+}
+template <bool PACKED>
+__device__ __forceinline__ int k_head_index(const Layout& L, int b, int hk)
+{
+    return PACKED ? hk : b * L.Hkv + hk;
+}
+
+// Bottom-right causal alignment for a problem of nq queries and nk keys: query i sees key j
+// iff j <= i + (nk - nq).  For nq == nk this is the square mask above; a chunk of the last nq
+// queries of a longer sequence (chunked prefill) sees every earlier key.  The shifted query
+// bounds go through causal_tile_class unchanged.
+__device__ __forceinline__ int causal_class_shifted(int q0, int q1, int k0, int k1, int shift)
+{
+    return causal_tile_class(q0 + shift, q1 + shift, k0, k1);
+}
+
+// Parameters of the forward kernels.  The SIMT kernels use N and BH (fixed layout, square);
+// the tensor-core kernels use the layout L.
 struct FwdParams {
     const void* q;
     const void* k;
@@ -68,6 +131,7 @@ struct FwdParams {
     int* status;       // device status word (watchdog)
     unsigned long long wait_limit_ns;
     int debug_flags;   // test hook: kDebugDropFirstLoad
+    Layout L;
 };
 
 // Parameters of the backward kernels.
@@ -91,6 +155,7 @@ struct BwdParams {
     int* status;
     unsigned long long wait_limit_ns;
     int debug_flags;
+    Layout L;
 };
 
 }  // namespace fa

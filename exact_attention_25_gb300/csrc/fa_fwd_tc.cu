@@ -59,7 +59,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
         mma_ts_w(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc, ks > 0 ? 1u : acc_first);
 }
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -87,18 +87,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int N = p.N;
-    const int n_qtiles = (N + C::BM - 1) / C::BM;
-    const int n_kblocks = (N + C::BN - 1) / C::BN;
-    const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
-    // Head-major order, so the CTAs resident at one time share one or two heads' K/V in L2;
-    // within a head the heaviest causal pairs (the last ones) go first.
-    const int bh = static_cast<int>(blockIdx.x) / n_pairs;
+    const Layout& L = p.L;
+    constexpr bool packed = PACKED;  // tensors stored token by token
+    const int n_pairs = ((L.Nq + C::BM - 1) / C::BM + C::NT - 1) / C::NT;
+    // Head-major order, so the CTAs resident at one time share one or two heads' K/V in L2
+    // (with grouped heads, the heads of a group share one K/V); within a head the heaviest
+    // causal pairs (the last ones) go first.
+    const int bhead = static_cast<int>(blockIdx.x) / n_pairs;
+    const int b = bhead / L.H, h = bhead % L.H;
     const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) % n_pairs;
+    const SeqRows sr = seq_rows<PACKED>(L, b);
+    const int nq = sr.nq, nk = sr.nk;
+    const int n_qtiles = (nq + C::BM - 1) / C::BM;
+    const int n_kblocks = (nk + C::BN - 1) / C::BN;
     const int qt0 = pair * C::NT;
+    if (qt0 >= n_qtiles) return;  // beyond this sequence's queries (whole CTA, before any sync)
     const int nt = min(C::NT, n_qtiles - qt0);
+    const int qhead = q_head_index<PACKED>(L, b, h);
+    const int khead = k_head_index<PACKED>(L, b, PACKED ? h / (L.H / L.Hkv) : h);
+    const int shift = PACKED ? nk - nq : 0;  // bottom-right causal alignment
 
-    // Key blocks visited by each query tile (a prefix 0..J_t-1 under the causal mask).
+    // Key blocks visited by each query tile: a prefix 0..J_t-1 (under the causal mask, the
+    // blocks whose first key some query of the tile sees).
     int J[C::NT];
 #pragma unroll
     for (int t = 0; t < C::NT; ++t) {
@@ -107,12 +117,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (!p.causal) {
                 J[t] = n_kblocks;
             } else {
-                const int q0 = (qt0 + t) * C::BM, q1 = min(N, q0 + C::BM);
-                int jt = 0;
-                while (jt < n_kblocks &&
-                       causal_tile_class(q0, q1, jt * C::BN, min(N, (jt + 1) * C::BN)) != kTileSkip)
-                    ++jt;
-                J[t] = jt;
+                const int q1 = min(nq, (qt0 + t + 1) * C::BM);
+                const int kend = min(nk, q1 + shift);  // keys [0, kend) are seen by some row
+                J[t] = kend > 0 ? (kend + C::BN - 1) / C::BN : 0;
             }
         }
     }
@@ -156,8 +163,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             mbar_arrive_expect_tx_w(&bar_q, nt * C::TILE_BYTES);
             for (int t = 0; t < nt; ++t)
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d_w(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn,
-                                (qt0 + t) * C::BM, bh);
+                    tma_load_rows_w(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn,
+                                sr.q0 + (qt0 + t) * C::BM, qhead, packed);
             int issued = 0;
             for (int j = 0; j < Jmax; ++j) {
                 const int s = j % C::STAGES;
@@ -167,14 +174,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 if (!warp_wait_all(&bar_kempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
                 mbar_arrive_expect_tx_w(&bar_kfull[s], C::TILE_BYTES);
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d_w(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
-                                64 * pn, j * C::BN, bh);
+                    tma_load_rows_w(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
+                                64 * pn, sr.k0 + j * C::BN, khead, packed);
                 if (!warp_wait_all(&bar_vempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
                 mbar_arrive_expect_tx_w(&bar_vfull[s], C::TILE_BYTES);
                 if (!(j == 0 && (p.debug_flags & kDebugDropFirstLoad)))
                     for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d_w(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
-                                    &bar_vfull[s], 64 * pn, j * C::BN, bh);
+                        tma_load_rows_w(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
+                                    &bar_vfull[s], 64 * pn, sr.k0 + j * C::BN, khead, packed);
                 issued = j + 1;
             }
             // Let no copy land after the CTA exits: wait (bounded, ignoring the abort flag)
@@ -204,14 +211,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const uint32_t tS0 = tbase, tS1 = tbase + 128u;
             const uint32_t tO0 = tbase + 256u, tO1 = tbase + 256u + D;
 
-            bool ok = warp_wait_all(&bar_q, 0, wd, kSiteFwdMmaQ);
+            // (no key block at all: nothing to issue, the softmax warps write empty rows)
+            bool ok = Jmax > 0 && warp_wait_all(&bar_q, 0, wd, kSiteFwdMmaQ);
             ok = ok && warp_wait_all(&bar_kfull[0], 0, wd, kSiteFwdMmaK);
             int committed_k = 0, committed_v = 0;  // key blocks whose K / V release was committed
             if (ok) {
                 tc_fence_after();
-                issue_qk<D, C::PANEL_BYTES>(tS0, dq0, dk0, kIdS);
-                mma_commit_w(&bar_sfull[0]);
-                if (nt > 1) {
+                if (J0 > 0) {
+                    issue_qk<D, C::PANEL_BYTES>(tS0, dq0, dk0, kIdS);
+                    mma_commit_w(&bar_sfull[0]);
+                }
+                if (J1 > 0) {
                     issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), dk0, kIdS);
                     mma_commit_w(&bar_sfull[1]);
                 }
@@ -286,7 +296,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint32_t tP = tS + 64u;
         const uint32_t tO = tbase + lane_base + 256u + static_cast<uint32_t>(t * D);
         const int qt = qt0 + t;
-        const int qrow = qt * C::BM + r;
+        const int qrow = qt * C::BM + r;  // row within the sequence
+        // Element-wise masking is needed from key block jmask on: the blocks that straddle the
+        // causal diagonal of this tile and the ragged last block.  This row sees the keys
+        // [0, klim] of the sequence.
+        int jmask = nk / C::BN;
+        int klim = nk - 1;
+        if (p.causal) {
+            const int e = qt * C::BM + shift + 1;  // blocks below e / BN are fully visible
+            jmask = min(jmask, e > 0 ? e / C::BN : 0);
+            klim = min(klim, qrow + shift);
+        }
         // Softmax runs on x = S * c with c = scale*log2(e) (exp2 form).  For c <= 0 the
         // scores are pre-multiplied so that masked entries remain -inf after scaling.
         const float c2 = p.scale_log2;
@@ -317,12 +337,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 128; ++c) x[c] *= c2;
             }
-            // Element-wise mask only on the diagonal block and on the ragged last block.
-            const bool diag = p.causal && j == qt;
-            const bool tail = (j == n_kblocks - 1) && (N % C::BN) != 0;
-            if (diag || tail) {
-                int lim = N - 1 - j * C::BN;  // last valid key column in this block
-                if (diag) lim = min(lim, qrow - j * C::BN);
+            // Element-wise mask only on blocks that straddle the causal diagonal and on the
+            // ragged last block.
+            if (j >= jmask) {
+                const int lim = klim - j * C::BN;  // last visible key column in this block
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c > lim) x[c] = -INFINITY;
@@ -409,12 +427,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (lane == 0) mbar_arrive(&bar_pfull[t]);
         }
         // ------------------------------------------------------------- epilogue
+        // Where this row goes, re-derived here rather than held in registers across the loop.
+        const int eb = static_cast<int>(blockIdx.x) / n_pairs;
+        const SeqRows se = seq_rows<PACKED>(L, eb / L.H);
+        const int eqhead = q_head_index<PACKED>(L, eb / L.H, eb % L.H);
+        const size_t orow_off = static_cast<size_t>(se.q0 + qrow) * L.q_rs +
+                                static_cast<size_t>(eqhead) * L.q_hs;
+        const size_t lse_off = static_cast<size_t>(eqhead) * L.Rq + se.q0 + qrow;
         if (ok && Jt > 0) {
             if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
                 tc_fence_after();
-                const float inv_l = 1.0f / lr;
-                __nv_bfloat16* orow =
-                    static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * N + qrow) * D;
+                // a row that sees no key (possible when queries outnumber keys) stays 0
+                const float inv_l = lr > 0.0f ? 1.0f / lr : 0.0f;
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + orow_off;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
@@ -426,7 +451,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     for (int c = 0; c < 16; ++c)
                         packed[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
                                                 __uint_as_float(o[2 * c + 1]) * inv_l);
-                    if (qrow < N) {
+                    if (qrow < se.nq) {
                         uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -434,9 +459,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                                                 packed[4 * c + 3]);
                     }
                 }
-                if (qrow < N && p.lse != nullptr)
-                    p.lse[static_cast<size_t>(bh) * N + qrow] = (m + __log2f(l)) * kLn2;
+                if (qrow < se.nq && p.lse != nullptr) p.lse[lse_off] = (m + __log2f(l)) * kLn2;
             }
+        } else if (t < nt && Jt == 0 && qrow < se.nq) {
+            // the whole tile sees no key: O = 0 and lse = log(0) = -inf
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow_off);
+            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (p.lse != nullptr) p.lse[lse_off] = -INFINITY;
         }
         tc_fence_before();
     }
@@ -448,7 +477,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
 }
 
-template <int D>
+template <int D, bool PACKED>
 static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                       const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
 {
@@ -457,24 +486,28 @@ static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, PACKED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const int n_qtiles = (p.N + C::BM - 1) / C::BM;
+    const int n_qtiles = (p.L.Nq + C::BM - 1) / C::BM;
     const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
-    dim3 grid(p.BH * n_pairs);
-    fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
+    dim3 grid(p.L.B * p.L.H * n_pairs);
+    fa_fwd_tc_kernel<D, PACKED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
 {
-    if (d == 64) return launch_fwd_tc_impl<64>(tq, tk, tv, p, st);
-    return launch_fwd_tc_impl<128>(tq, tk, tv, p, st);
+    const bool packed = p.L.cu_q != nullptr;
+    if (d == 64)
+        return packed ? launch_fwd_tc_impl<64, true>(tq, tk, tv, p, st)
+                      : launch_fwd_tc_impl<64, false>(tq, tk, tv, p, st);
+    return packed ? launch_fwd_tc_impl<128, true>(tq, tk, tv, p, st)
+                  : launch_fwd_tc_impl<128, false>(tq, tk, tv, p, st);
 }
 
 }  // namespace fa

@@ -147,7 +147,11 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
     constexpr int EPV = 16 / sizeof(T);  // elements per 16-byte vector
     constexpr int TPR = D / EPV;         // threads per row (8, 16 or 32)
     constexpr int RPW = 32 / TPR;        // rows per warp and iteration
-    const size_t rows = static_cast<size_t>(p.BH) * p.N;
+    // Rows t = hh * Rq + i of the statistics arrays: row i of head index hh, whose elements sit
+    // at i * q_rs + hh * q_hs (either layout).
+    const Layout& L = p.L;
+    const size_t n_heads = static_cast<size_t>(L.cu_q == nullptr ? L.B * L.H : L.H);
+    const size_t rows = n_heads * static_cast<size_t>(L.Rq);
     const int lane = threadIdx.x & 31;
     const int sub = lane % TPR;
     const size_t warps_total = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
@@ -158,9 +162,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
         const bool valid = row < rows;
         float acc = 0.0f;
         if (valid) {
-            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + row * D)[sub];
-            const uint4 b =
-                reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + row * D)[sub];
+            const size_t hh = row / static_cast<size_t>(L.Rq), i = row - hh * static_cast<size_t>(L.Rq);
+            const size_t off = i * static_cast<size_t>(L.q_rs) + hh * static_cast<size_t>(L.q_hs);
+            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off)[sub];
+            const uint4 b = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off)[sub];
             const T* ea = reinterpret_cast<const T*>(&a);
             const T* eb = reinterpret_cast<const T*>(&b);
 #pragma unroll
@@ -361,7 +366,7 @@ template <typename T, int D>
 static cudaError_t bwd_pre(const BwdParams& p, cudaStream_t st, int num_sms)
 {
     constexpr int TPR = D / (16 / sizeof(T));
-    const long rows = static_cast<long>(p.BH) * p.N;
+    const long rows = static_cast<long>(p.L.cu_q == nullptr ? p.L.B * p.L.H : p.L.H) * p.L.Rq;
     const int rows_per_block = 256 / TPR;
     long blocks = (rows + rows_per_block - 1) / rows_per_block;
     const long cap = static_cast<long>(num_sms) * 8;

@@ -132,6 +132,18 @@ __device__ __forceinline__ void tma_load_3d_w(void* dst, const CUtensorMap* map,
         : "memory");
 }
 
+// Rows [row, row + box) of head index `head`, columns [x, x + 64), from a 3-D map whose
+// dimensions are (d, rows, heads), or (d, heads, rows) when head_inner is set (tensors stored
+// token by token, [rows, heads, d]).  Both give the same shared-memory tile.
+__device__ __forceinline__ void tma_load_rows_w(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                int x, int row, int head, bool head_inner)
+{
+    if (head_inner)
+        tma_load_3d_w(dst, map, bar, x, head, row);
+    else
+        tma_load_3d_w(dst, map, bar, x, row, head);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t* bar, uint32_t bytes)
 {
     asm volatile(

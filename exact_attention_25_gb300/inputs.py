@@ -106,3 +106,25 @@ def random_qkv(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: int =
     if with_do:
         out["do"] = torch.randn(shape, generator=g).to(dtype)
     return out
+
+
+def random_varlen(lens_q, lens_k, H: int, Hkv: int, d: int, dtype=torch.bfloat16, seed: int = 0,
+                  in_scale: float = 1.0, with_do: bool = True) -> dict:
+    """Seeded packed batch: q (and do) [total_q, H, d], k, v [total_k, Hkv, d] standard normal
+    (drawn in the order q, k, v, do), and the int32 offsets cu_q, cu_k ([B + 1], CPU) of the
+    sequence lengths ``lens_q`` / ``lens_k``."""
+    if len(lens_q) != len(lens_k):
+        raise ValueError("one query length and one key length per sequence")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    cu_q = torch.tensor([0] + list(lens_q), dtype=torch.int64).cumsum(0).to(torch.int32)
+    cu_k = torch.tensor([0] + list(lens_k), dtype=torch.int64).cumsum(0).to(torch.int32)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    out = {"q": (torch.randn((tq, H, d), generator=g) * in_scale).to(dtype),
+           "k": (torch.randn((tk, Hkv, d), generator=g) * in_scale).to(dtype),
+           "v": (torch.randn((tk, Hkv, d), generator=g) * in_scale).to(dtype),
+           "cu_q": cu_q, "cu_k": cu_k,
+           "max_q": max(lens_q), "max_k": max(lens_k)}
+    if with_do:
+        out["do"] = torch.randn((tq, H, d), generator=g).to(dtype)
+    return out

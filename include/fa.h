@@ -90,6 +90,48 @@ int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, cons
                 float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
                 int impl, void* stream);
 
+/* Packed variable-length batches with grouped key/value heads (bf16, tensor-core path).
+ *
+ * What it computes.  B independent sequences; sequence b has the query rows
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]) and the key/value rows [cu_seqlens_k[b],
+ * cu_seqlens_k[b+1]), so nq_b queries and nk_b keys, which may differ.  Query head h attends to
+ * key/value head h / (H / Hkv): Hkv = H is multi-head attention, 1 < Hkv < H grouped-query
+ * attention and Hkv = 1 multi-query attention (the GQA / MQA models of "서빙에서 Flash
+ * Attention 이득이 예상보다 작은 경우" in "Flash Attention IO-awareness principle").  The
+ * causal mask is aligned to the bottom-right corner: query i sees key j iff
+ * j <= i + (nk_b - nq_b), so a chunk of the last nq_b queries of a prompt sees every earlier
+ * key, as chunked prefill needs ("PagedAttention·Chunked Prefill과의 위치", same page); with
+ * nq_b == nk_b this is the square mask of fa_fwd.  A query row that sees no key (nq_b > nk_b
+ * under the causal mask, or nk_b == 0) gets O = 0, lse = -inf and zero gradient.
+ *
+ * Layout (token by token, no padding between sequences):
+ *   q, o, dout, dq: [total_q, H, d] bf16;  k, v, dk, dv: [total_k, Hkv, d] bf16;
+ *   lse: [H, total_q] fp32 (may be NULL in the forward);
+ *   cu_seqlens_q, cu_seqlens_k: device int32 arrays of B+1 non-decreasing offsets, [0] = 0,
+ *   [B] = total_q (total_k).  The library cannot read them on the host: offsets outside
+ *   [0, total] are clamped on the device and lengths are clamped to max_seqlen_q /
+ *   max_seqlen_k (an upper bound the caller passes; larger values only cost idle CTAs), so
+ *   inconsistent offsets give wrong values but never touch memory outside the buffers.
+ * d is 64 or 128; H % Hkv == 0; total_q*H*d and total_k*Hkv*d < 2^31.  Ownership, alignment,
+ * streams and error codes as for fa_fwd / fa_bwd. */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int max_seqlen_q,
+                  int max_seqlen_k, int total_q, int total_k, int H, int Hkv, int d, float scale,
+                  int causal, void* stream);
+
+/* Bytes of device workspace fa_bwd_varlen needs (Delta and the base-2 LSE, fp32 [H, total_q],
+ * plus alignment).  Returns 0 for invalid sizes. */
+size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int d);
+
+/* Backward of fa_fwd_varlen (o and lse from it with the same arguments).  Gradients as for
+ * fa_bwd; dk and dv of a shared key/value head are the sums over the query heads of its group.
+ * Deterministic (no atomics). */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int max_seqlen_q, int max_seqlen_k, int total_q,
+                  int total_k, int H, int Hkv, int d, float scale, int causal, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
 /* Backward for callers that cannot allocate device memory.  This entry point has no
  * counterpart on the pages; it exists for code that is not allowed to call cudaMalloc or any
  * allocating routine, for example a plugin running inside a host framework that owns every

@@ -145,3 +145,36 @@ def test_flop_convention():
     assert perfmodel.fwd_flops(1, 1, 512, 64, False) == 4 * 512 * 512 * 64
     assert perfmodel.fwd_flops(2, 32, 8192, 128, True) == pytest.approx(1.0995e12, rel=1e-4)
     assert perfmodel.bwd_flops(4, 16, 4096, 128, True) == pytest.approx(6.872e11, rel=1e-3)
+
+
+def fwd_varlen(lib, cu_q=A, cu_k=A, B=2, max_q=10, max_k=10, total_q=20, total_k=20, H=4, Hkv=2,
+               d=128, scale=0.1, causal=1, q=A, o=A2):
+    return lib.fa_fwd_varlen(q, A, A, o, A2, cu_q, cu_k, B, max_q, max_k, total_q, total_k, H,
+                             Hkv, d, ctypes.c_float(scale), causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=4, Hkv=3), -1), (dict(Hkv=0), -1), (dict(B=0), -1), (dict(total_q=0), -1),
+    (dict(max_k=0), -1), (dict(d=96), -2), (dict(cu_q=None), -1), (dict(cu_k=None), -1),
+    (dict(cu_q=P(0x10002)), -3), (dict(q=MIS), -3), (dict(causal=3), -1),
+    (dict(scale=math.nan), -1), (dict(total_q=1 << 20, H=64, d=128), -7),
+])
+def test_varlen_forward_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert fwd_varlen(lib, **kw) == code
+    assert lib.fa_last_error().decode() != ""
+
+
+def test_varlen_backward_rejects_bad_arguments(lib):
+    need = lib.fa_bwd_varlen_workspace_bytes(20, 4, 128)
+    assert need >= 2 * 20 * 4 * 4
+    assert lib.fa_bwd_varlen_workspace_bytes(0, 4, 128) == 0
+    assert lib.fa_bwd_varlen_workspace_bytes(20, 4, 80) == 0
+
+    def call(ws=A, nbytes=need, H=4, Hkv=2):
+        return lib.fa_bwd_varlen(A, A, A, A, A, A, A2, A2, A2, A, A, 2, 10, 10, 20, 20, H, Hkv,
+                                 128, ctypes.c_float(0.1), 1, ws, nbytes, None)
+
+    assert call(ws=None) == -4
+    assert call(nbytes=need - 1) == -4
+    assert call(ws=MIS) == -3
+    assert call(H=5) == -1
