@@ -16,7 +16,8 @@ __all__ = [
     "FA_BF16", "FA_F32", "FaError", "load", "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes",
     "fa_device_status", "fa_set_wait_limit_ns", "fa_causal_block_counts", "forward", "backward",
     "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "forward_varlen",
-    "backward_varlen",
+    "backward_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
+    "forward_decode",
 ]
 
 
@@ -227,3 +228,51 @@ def backward_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_
     fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                   max_seqlen_k, scale, causal, workspace, stream)
     return dq, dk, dv
+
+
+# --------------------------------------------------------------------------- split-KV decode
+
+def fa_decode_num_splits(B: int, Hkv: int, max_seqlen_k: int) -> int:
+    """C ``fa_decode_num_splits``: a split count that fills this GPU's SMs."""
+    n = int(load().fa_decode_num_splits(B, Hkv, max_seqlen_k))
+    check(min(n, 0))
+    return n
+
+
+def fa_decode_workspace_bytes(total_q: int, H: int, d: int, num_splits: int) -> int:
+    return int(load().fa_decode_workspace_bytes(total_q, H, d, num_splits))
+
+
+def fa_fwd_decode(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, scale: float, causal: bool, num_splits: int, workspace,
+                  stream=None) -> None:
+    """C ``fa_fwd_decode``: packed tensors as fa_fwd_varlen; workspace may be None for
+    num_splits = 1."""
+    _check_tensors(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, workspace)
+    B, total_q, total_k, H, Hkv, d = _varlen_shapes(q, k, cu_seqlens_q, cu_seqlens_k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(load().fa_fwd_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
+        int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, H, Hkv, d, float(scale),
+        int(bool(causal)), int(num_splits), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def forward_decode(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                   scale: float | None = None, causal: bool = False, num_splits: int | None = None,
+                   stream=None):
+    """Allocate O, LSE (and the split workspace) and run fa_fwd_decode."""
+    import torch
+
+    total_q, H, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = d ** -0.5
+    if num_splits is None:
+        num_splits = fa_decode_num_splits(int(cu_seqlens_q.numel()) - 1, int(k.shape[1]),
+                                          max_seqlen_k)
+    nbytes = fa_decode_workspace_bytes(total_q, H, d, num_splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    fa_fwd_decode(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
+                  causal, num_splits, ws, stream)
+    return o, lse

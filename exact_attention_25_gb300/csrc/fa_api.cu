@@ -2,6 +2,7 @@
 // call), TMA tensor-map construction, kernel dispatch and the device status word.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -19,6 +20,9 @@ cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
 cudaError_t launch_bwd_dkv_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
+cudaError_t launch_decode(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const DecodeParams& p, cudaStream_t st,
+                          int num_sms);
 
 // Device status word written by bounded waits that give up (0 = fine).
 __device__ int g_status_word;
@@ -484,6 +488,123 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
     if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
     if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return FA_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// Split-KV decode (fa_decode_num_splits, fa_decode_workspace_bytes, fa_fwd_decode).
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr int kDecodeMaxSplits = 256;
+
+size_t decode_part_o_bytes(int total_q, int H, int d, int splits)
+{
+    return align256(static_cast<size_t>(splits) * total_q * H * d * 4);
+}
+
+}  // namespace
+
+extern "C" int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k)
+{
+    if (B < 1 || Hkv < 1 || max_seqlen_k < 1) return fail(FA_ERR_INVALID_ARG, "B, Hkv and max_seqlen_k must be >= 1");
+    DeviceInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    // Fill whole waves of one CTA per SM: the split count whose CTAs (B * Hkv * splits) waste
+    // the smallest fraction of the last wave, keeping at least 8 key blocks per split.
+    const long long units = static_cast<long long>(B) * Hkv;
+    const int nblk = (max_seqlen_k + 127) / 128;
+    int best = 1;
+    double best_eff = 0.0;
+    const int smax = std::max(1, std::min(kDecodeMaxSplits, nblk / 8));
+    for (int sp = 1; sp <= smax; ++sp) {
+        const long long ctas = units * sp;
+        const long long waves = (ctas + di->sms - 1) / di->sms;
+        const double eff = static_cast<double>(ctas) / static_cast<double>(waves * di->sms);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = sp;
+        }
+    }
+    return best;
+}
+
+extern "C" size_t fa_decode_workspace_bytes(int total_q, int H, int d, int num_splits)
+{
+    if (total_q < 1 || H < 1 || (d != 64 && d != 128) || num_splits < 1 ||
+        num_splits > kDecodeMaxSplits)
+        return 0;
+    if (num_splits == 1) return 0;
+    return decode_part_o_bytes(total_q, H, d, num_splits) +
+           align256(static_cast<size_t>(num_splits) * H * total_q * 4) + 256;
+}
+
+extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                             int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H,
+                             int Hkv, int d, float scale, int causal, int num_splits,
+                             void* workspace, size_t workspace_bytes, void* stream)
+{
+    int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_seqlen_q, &max_seqlen_k, total_q,
+                          total_k, H, Hkv, d, scale, causal);
+    if (rc) return rc;
+    const int G = H / Hkv;
+    if (static_cast<long long>(G) * max_seqlen_q > 128)
+        return fail(FA_ERR_INVALID_ARG, "(H / Hkv) * max_seqlen_q must be <= 128 for the decode "
+                                        "kernel; use fa_fwd_varlen");
+    if (num_splits < 1 || num_splits > kDecodeMaxSplits)
+        return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, " +
+                                            std::to_string(kDecodeMaxSplits) + "]");
+    if (static_cast<long long>(B) * Hkv * num_splits >= (1LL << 31))
+        return fail(FA_ERR_TOO_LARGE, "B * Hkv * num_splits must be < 2^31");
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    const size_t need = fa_decode_workspace_bytes(total_q, H, d, num_splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+        if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    }
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    fa::DecodeParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    if (need > 0) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        p.o_part = reinterpret_cast<float*>(ws);
+        p.lse_part = reinterpret_cast<float*>(ws + decode_part_o_bytes(total_q, H, d, num_splits));
+    }
+    p.splits = num_splits; p.G = G; p.q_box = max_seqlen_q;
+    p.scale_log2 = scale * fa::kLog2e; p.causal = causal;
+    p.status = di->status; p.wait_limit_ns = g_wait_limit_ns; p.debug_flags = g_debug_flags;
+    p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
+                        total_k, H, Hkv, d);
+    if ((rc = get_encoder())) return rc;
+    // Q: (d, H, total_q) with a box of (64 columns, G heads, max_seqlen_q tokens), so one copy
+    // brings the G x nq query rows of a (sequence, key/value head) pair; K, V as fa_fwd_varlen.
+    CUtensorMap maps[4];
+    {
+        const cuuint64_t dd = static_cast<cuuint64_t>(d);
+        cuuint64_t dims[3] = {dd, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(total_q)};
+        cuuint64_t strides[2] = {dd * 2, static_cast<cuuint64_t>(H) * dd * 2};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(max_seqlen_q)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = g_encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
+    }
+    if ((rc = make_map(&maps[1], k, Hkv, total_k, d, 128, true)) ||
+        (rc = make_map(&maps[2], v, Hkv, total_k, d, 128, true)))
+        return rc;
+    cudaError_t e = fa::launch_decode(d, maps[0], maps[1], maps[2], p,
+                                      static_cast<cudaStream_t>(stream), di->sms);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return FA_OK;
 }
 

@@ -30,7 +30,18 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--stage", type=int, default=-1)
     ap.add_argument("--time", action="store_true", help="report CUDA-event timing")
+    ap.add_argument("--Hkv", type=int, default=0,
+                    help="packed layout with this many key/value heads (GQA); 0 = fixed layout")
+    ap.add_argument("--Nq", type=int, default=0,
+                    help="packed layout: queries per sequence (the last Nq of N; 0 = N)")
+    ap.add_argument("--decode", action="store_true",
+                    help="packed layout through fa_fwd_decode (split-KV); reports GB/s")
+    ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = suggested)")
     a = ap.parse_args()
+    if a.Hkv and a.decode:
+        return run_decode(a)
+    if a.Hkv:
+        return run_packed(a)
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     shape = (a.B, a.H, a.N, a.d)
@@ -86,6 +97,88 @@ def main():
     fa.fa_device_status()
     torch.cuda.synchronize()
     print("ok", a.which, shape, "causal" if a.causal else "full")
+
+
+def run_packed(a):
+    """B sequences of N keys each and the last Nq of their positions as queries (a chunked
+    prefill step), H query heads over Hkv key/value heads, packed token by token."""
+    import torch
+
+    import exact_attention_25_gb300 as fa
+
+    nq = a.Nq or a.N
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    mk = lambda rows, heads: torch.randn((rows, heads, a.d), generator=g, device="cuda").to(  # noqa: E731
+        torch.bfloat16)
+    q, k, v, do = mk(a.B * nq, a.H), mk(a.B * a.N, a.Hkv), mk(a.B * a.N, a.Hkv), mk(a.B * nq, a.H)
+    cu_q = torch.arange(0, a.B * nq + 1, nq, dtype=torch.int32, device="cuda")
+    cu_k = torch.arange(0, a.B * a.N + 1, a.N, dtype=torch.int32, device="cuda")
+    scale = a.d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((a.H, a.B * nq), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_bytes(a.B * nq, a.H, a.d), dtype=torch.uint8,
+                     device="cuda")
+    fwd = lambda: fa.fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, nq, a.N, scale, a.causal)  # noqa: E731
+    bwd = lambda: fa.fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_q, cu_k, nq, a.N,  # noqa: E731
+                                   scale, a.causal, ws)
+    fwd()
+    run = fwd if a.which == "fwd" else bwd
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    fa.fa_device_status()
+    ms = e0.elapsed_time(e1) / a.iters
+    # visible (query, key) pairs: every key for each query, or under the bottom-right causal
+    # mask the keys j <= i + N - Nq of query i
+    pairs = nq * a.N if not a.causal else sum(min(a.N, i + a.N - nq + 1) for i in range(nq))
+    fl = 4.0 * a.B * a.H * pairs * a.d * (1.0 if a.which == "fwd" else 2.5)
+    print(f"{a.which} packed B={a.B} H={a.H} Hkv={a.Hkv} Nq={nq} Nk={a.N} d={a.d} "
+          f"causal={a.causal}: {ms:.4f} ms {fl / ms / 1e9:.1f} TFLOP/s")
+
+
+def run_decode(a):
+    """A decode step: B sequences of N cached keys, the last Nq positions (default 1) as
+    queries, H query heads over Hkv key/value heads.  Bandwidth counts the bytes the step must
+    move: K and V once, Q, O and the LSE."""
+    import torch
+
+    import exact_attention_25_gb300 as fa
+
+    nq = a.Nq or 1
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    mk = lambda rows, heads: torch.randn((rows, heads, a.d), generator=g, device="cuda").to(  # noqa: E731
+        torch.bfloat16)
+    q, k, v = mk(a.B * nq, a.H), mk(a.B * a.N, a.Hkv), mk(a.B * a.N, a.Hkv)
+    cu_q = torch.arange(0, a.B * nq + 1, nq, dtype=torch.int32, device="cuda")
+    cu_k = torch.arange(0, a.B * a.N + 1, a.N, dtype=torch.int32, device="cuda")
+    splits = a.splits or fa.fa_decode_num_splits(a.B, a.Hkv, a.N)
+    o = torch.empty_like(q)
+    lse = torch.empty((a.H, a.B * nq), device="cuda", dtype=torch.float32)
+    nbytes = fa.fa_decode_workspace_bytes(a.B * nq, a.H, a.d, splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    run = lambda: fa.fa_fwd_decode(q, k, v, o, lse, cu_q, cu_k, nq, a.N, a.d ** -0.5,  # noqa: E731
+                                   a.causal, splits, ws)
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    fa.fa_device_status()
+    ms = e0.elapsed_time(e1) / a.iters
+    moved = 2 * k.numel() * 2 + 2 * q.numel() * 2 + lse.numel() * 4
+    print(f"decode B={a.B} H={a.H} Hkv={a.Hkv} Nq={nq} Nk={a.N} d={a.d} causal={a.causal} "
+          f"splits={splits}: {ms:.4f} ms {moved / ms / 1e6:.1f} GB/s")
 
 
 if __name__ == "__main__":

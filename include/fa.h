@@ -132,6 +132,35 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
                   int total_k, int H, int Hkv, int d, float scale, int causal, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* Split-KV decode: the forward of fa_fwd_varlen (same arguments, layout, mask, results up to
+ * rounding) laid out for few queries per sequence against a long key/value history, the
+ * decoding case that "서빙에서 Flash Attention 이득이 예상보다 작은 경우" in "Flash Attention
+ * IO-awareness principle" hands to decoding kernels.  The G = H / Hkv query heads of a group
+ * and the sequence's queries share one 128-row tile, so they read their K and V once; each
+ * sequence's key blocks are split into num_splits ranges processed in parallel, whose partial
+ * results (O and log-sum-exp per range) a second kernel merges.
+ *   - Requires (H / Hkv) * max_seqlen_q <= 128 (else FA_ERR_INVALID_ARG: use fa_fwd_varlen).
+ *   - num_splits in [1, 256]; fa_decode_num_splits suggests one for this GPU.  Ranges with no
+ *     key block (num_splits larger than the blocks of a sequence) contribute nothing.
+ *   - workspace: caller-owned device buffer of fa_decode_workspace_bytes(total_q, H, d,
+ *     num_splits) bytes (0 for num_splits = 1, when workspace may be NULL); overwritten.
+ * bf16 only, forward only.  Errors as fa_fwd_varlen, plus FA_ERR_WORKSPACE. */
+int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int max_seqlen_q,
+                  int max_seqlen_k, int total_q, int total_k, int H, int Hkv, int d, float scale,
+                  int causal, int num_splits, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/* Bytes of workspace fa_fwd_decode needs: the partial O (fp32 [num_splits, total_q, H, d]) and
+ * log-sum-exp (fp32 [num_splits, H, total_q]) of every range, plus alignment; 0 for
+ * num_splits = 1 or invalid sizes. */
+size_t fa_decode_workspace_bytes(int total_q, int H, int d, int num_splits);
+
+/* A split count for fa_fwd_decode on the current device: the one in [1, max(1, blocks / 8)]
+ * (blocks = ceil(max_seqlen_k / 128)) whose B * Hkv * num_splits CTAs fill the last wave of one
+ * CTA per SM best.  Returns it (>= 1) or a negative FA_ERR_* code. */
+int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k);
+
 /* Backward for callers that cannot allocate device memory.  This entry point has no
  * counterpart on the pages; it exists for code that is not allowed to call cudaMalloc or any
  * allocating routine, for example a plugin running inside a host framework that owns every

@@ -178,3 +178,25 @@ def test_varlen_backward_rejects_bad_arguments(lib):
     assert call(nbytes=need - 1) == -4
     assert call(ws=MIS) == -3
     assert call(H=5) == -1
+
+
+def test_decode_rejects_bad_arguments(lib):
+    need = lib.fa_decode_workspace_bytes(64, 32, 128, 4)
+    assert need >= 4 * 64 * 32 * (128 + 1) * 4
+    assert lib.fa_decode_workspace_bytes(8, 32, 128, 1) == 0
+    assert lib.fa_decode_workspace_bytes(8, 32, 128, 0) == 0
+    assert lib.fa_decode_workspace_bytes(8, 32, 96, 2) == 0
+
+    def call(H=32, Hkv=8, max_q=1, splits=4, ws=A, nbytes=need, d=128):
+        return lib.fa_fwd_decode(A, A, A, A2, A2, A, A, 8, max_q, 1000, 64, 8000, H, Hkv, d,
+                                 ctypes.c_float(0.1), 1, splits, ws, nbytes, None)
+
+    assert call(max_q=33) == -1            # 4 heads x 33 queries > 128 rows
+    assert call(H=30) == -1                # H % Hkv
+    assert call(splits=0) == -1
+    assert call(splits=257) == -1
+    assert call(ws=None) == -4
+    assert call(nbytes=need - 1) == -4
+    assert call(ws=MIS) == -3
+    assert call(d=80) == -2
+    assert lib.fa_decode_num_splits(0, 8, 100) == -1

@@ -208,6 +208,43 @@ def fwd_protocol(j0, j1, stages=2):
     return progs, counts
 
 
+# ----------------------------------------------------------------------------- decode kernel
+
+def decode_protocol(J, stages=3):
+    """fa_decode_split_kernel: producer (Q, then K and V per block), MMA issuer with two S
+    buffers, one softmax group; block jj's softmax waits for the P V product of block jj-1."""
+    prod = [(C, "q")]
+    for j in range(J):
+        if j >= stages:
+            prod.append((W, ("kempty", j % stages), j // stages - 1))
+        prod.append((C, ("kfull", j % stages)))
+        if j >= stages:
+            prod.append((W, ("vempty", j % stages), j // stages - 1))
+        prod.append((C, ("vfull", j % stages)))
+    mma = []
+    if J > 0:
+        mma += [(W, "q", 0), (W, ("kfull", 0), 0), (C, ("sfull", 0)), (C, ("kempty", 0))]
+    for j in range(J):
+        if j + 1 < J:
+            s1 = (j + 1) % stages
+            mma += [(W, ("kfull", s1), (j + 1) // stages), (C, ("sfull", (j + 1) & 1)),
+                    (C, ("kempty", s1))]
+        mma += [(W, "pfull", j), (W, ("vfull", j % stages), j // stages), (C, "pv"),
+                (C, ("vempty", j % stages))]
+    soft = []
+    for j in range(J):
+        soft.append((W, ("sfull", j & 1), j >> 1))
+        if j > 0:
+            soft.append((W, "pv", j - 1))
+        soft.append((A, "pfull"))
+    if J > 0:
+        soft.append((W, "pv", J - 1))
+    progs = {"producer": prod, "mma": mma, "softmax": soft}
+    counts = {"q": 1, "pfull": 1, "pv": 1, ("sfull", 0): 1, ("sfull", 1): 1}
+    counts |= {(x, i): 1 for x in ("kfull", "kempty", "vfull", "vempty") for i in range(stages)}
+    return progs, counts
+
+
 # ----------------------------------------------------------------------------- tests
 
 SCHEDULES = 300
@@ -233,6 +270,12 @@ def test_dkv_protocol(n):
 @pytest.mark.parametrize("j0,j1", [(1, 1), (1, 2), (2, 3), (3, 3), (4, 5), (0, 1), (6, 7)])
 def test_fwd_protocol(j0, j1, stages):
     explore(lambda: fwd_protocol(j0, j1, stages))
+
+
+@pytest.mark.parametrize("stages", [3, 6])  # d = 128 and d = 64
+@pytest.mark.parametrize("J", [0, 1, 2, 3, 5, 8])
+def test_decode_protocol(J, stages):
+    explore(lambda: decode_protocol(J, stages))
 
 
 def test_model_catches_a_barrier_two_phases_ahead():

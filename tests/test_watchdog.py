@@ -7,7 +7,7 @@ import torch
 
 import exact_attention_25_gb300 as fa
 from exact_attention_25_gb300 import _lib
-from exact_attention_25_gb300.inputs import random_qkv
+from exact_attention_25_gb300.inputs import random_qkv, random_varlen
 
 pytestmark = pytest.mark.gpu
 
@@ -52,3 +52,15 @@ def test_backward_wait_expires_and_context_survives(short_waits):
     dq, dk, dv = fa.backward(q, k, v, o, do, lse, causal=False)
     fa.fa_device_status()
     assert torch.isfinite(dq.float()).all() and torch.isfinite(dv.float()).all()
+
+
+def test_decode_wait_expires_and_context_survives(short_waits):
+    x = random_varlen([1, 1], [300, 500], 8, 2, 128, seed=3, with_do=False)
+    q, k, v, cu_q, cu_k = (x[n].cuda() for n in ("q", "k", "v", "cu_q", "cu_k"))
+    short_waits.fa_debug_set_flags(1)
+    fa.forward_decode(q, k, v, cu_q, cu_k, 1, 500, causal=True, num_splits=2)
+    _expect_timeout()
+    short_waits.fa_debug_set_flags(0)
+    o, lse = fa.forward_decode(q, k, v, cu_q, cu_k, 1, 500, causal=True, num_splits=2)
+    fa.fa_device_status()
+    assert torch.isfinite(o.float()).all()
