@@ -49,6 +49,24 @@ def dist_setup():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world_size: int, ms: float) -> float:
+    """Weak scaling: every rank runs its own copy of the workload, so the job does
+    world_size times the work in the slowest rank's time."""
+    return world_size * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples every 50 ms while running."""
 
@@ -205,21 +223,15 @@ def run_gpu(args):
         torch.cuda.synchronize()
     barrier()
     fa.fa_device_status(stream)
-    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), dev)
     kern_ms = {name: statistics.median(e[i].elapsed_time(e[i + 1]) for e in ev)
                for i, name in enumerate(("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"))}
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
-    if ws > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
     ms_per_step = total_ms / args.steps
     f_fwd = perfmodel.fwd_flops(B, H, N, d, w.causal)
     f_bwd = perfmodel.bwd_flops(B, H, N, d, w.causal)
-    value = ws * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(f_fwd + f_bwd, ws, ms_per_step)
     clocks = clk.summary()
 
     # ---- end to end through the public API: pinned host in, results back out ----
@@ -255,14 +267,8 @@ def run_gpu(args):
         e2e_step()
     s1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    if ws > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1) / e2e_steps, dev)
+    e2e_value = whole_job_tflops(f_fwd + f_bwd, ws, e2e_ms)
 
     peaks, peak_src = load_peaks()
     fwd_med = statistics.median(fwd_ms)
