@@ -167,16 +167,42 @@ def _torch_int32():
     return torch.int32
 
 
+def _strides_or_none(*ts):
+    """(row, head) element strides of packed [rows, heads, d] views, or None when every tensor
+    is contiguous (the plain entry points apply).  The d elements of a head must be
+    contiguous."""
+    if all(t.is_contiguous() for t in ts):
+        return None
+    vals = []
+    for t in ts:
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("packed views need contiguous head dimensions (stride 1 in d)")
+        vals += [int(t.stride(0)), int(t.stride(1))]
+    return (ctypes.c_longlong * len(vals))(*vals)
+
+
+def _check_views(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+
+
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, scale: float, causal: bool, stream=None) -> None:
     """C ``fa_fwd_varlen``: q, o [total_q, H, d]; k, v [total_k, Hkv, d] (bf16); lse
-    [H, total_q] fp32 (or None); cu_seqlens_* int32 [B + 1] on the device."""
-    _check_tensors(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
+    [H, total_q] fp32 (or None); cu_seqlens_* int32 [B + 1] on the device.  Views with other
+    row / head strides go through ``fa_fwd_varlen_strided``."""
+    _check_views(q, k, v, o)
+    _check_tensors(lse, cu_seqlens_q, cu_seqlens_k)
     B, total_q, total_k, H, Hkv, d = _varlen_shapes(q, k, cu_seqlens_q, cu_seqlens_k)
-    check(load().fa_fwd_varlen(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
-        int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, H, Hkv, d, float(scale),
-        int(bool(causal)), _stream(stream)))
+    tail = (_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q), int(max_seqlen_k),
+            total_q, total_k, H, Hkv, d, float(scale), int(bool(causal)), _stream(stream))
+    st = _strides_or_none(q, k, v, o)
+    if st is None:
+        check(load().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), *tail))
+    else:
+        check(load().fa_fwd_varlen_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), st,
+                                           *tail))
 
 
 def fa_bwd_varlen_workspace_bytes(total_q: int, H: int, d: int) -> int:
@@ -186,15 +212,22 @@ def fa_bwd_varlen_workspace_bytes(total_q: int, H: int, d: int) -> int:
 def fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
                   max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool, workspace,
                   stream=None) -> None:
-    """C ``fa_bwd_varlen``: writes dq [total_q, H, d], dk, dv [total_k, Hkv, d] in place."""
-    _check_tensors(q, k, v, o, do, lse, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k)
+    """C ``fa_bwd_varlen``: writes dq [total_q, H, d], dk, dv [total_k, Hkv, d] in place.
+    Views with other row / head strides go through ``fa_bwd_varlen_strided``."""
+    _check_views(q, k, v, o, do, dq, dk, dv)
+    _check_tensors(lse, workspace, cu_seqlens_q, cu_seqlens_k)
     B, total_q, total_k, H, Hkv, d = _varlen_shapes(q, k, cu_seqlens_q, cu_seqlens_k)
     nbytes = workspace.numel() * workspace.element_size()
-    check(load().fa_bwd_varlen(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q), int(max_seqlen_k), total_q,
-        total_k, H, Hkv, d, float(scale), int(bool(causal)), _ptr(workspace), nbytes,
-        _stream(stream)))
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv))
+    tail = (_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q), int(max_seqlen_k),
+            total_q, total_k, H, Hkv, d, float(scale), int(bool(causal)), _ptr(workspace), nbytes,
+            _stream(stream))
+    st = _strides_or_none(q, k, v, o, do, dq, dk, dv)
+    if st is None:
+        check(load().fa_bwd_varlen(*head, *tail))
+    else:
+        check(load().fa_bwd_varlen_strided(*head, st, *tail))
 
 
 def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
@@ -205,7 +238,7 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
     d = int(q.shape[-1])
     if scale is None:
         scale = d ** -0.5
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     lse = torch.empty((int(q.shape[1]), int(q.shape[0])), dtype=torch.float32, device=q.device)
     fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
                   causal, stream)
@@ -224,7 +257,7 @@ def backward_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_
     if workspace is None:
         workspace = torch.empty(fa_bwd_varlen_workspace_bytes(total_q, H, d), dtype=torch.uint8,
                                 device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = (torch.empty(t.shape, dtype=t.dtype, device=t.device) for t in (q, k, v))
     fa_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                   max_seqlen_k, scale, causal, workspace, stream)
     return dq, dk, dv

@@ -99,13 +99,15 @@ int get_encoder()
 // swizzle panel) x `rows` rows x 1 head.  Fixed layout [heads, R, d]: dimensions (d, R, heads);
 // packed layout [R, heads, d] (token by token): dimensions (d, heads, R).  Rows beyond R read
 // as zero.
+// rs, hs: element strides of a row and of a head index.
 int make_map(CUtensorMap* m, const void* base, long long heads, long long R, int d, int rows,
-             bool packed)
+             bool packed, long long rs, long long hs)
 {
     const cuuint64_t dd = static_cast<cuuint64_t>(d);
     const cuuint64_t nh = static_cast<cuuint64_t>(heads), nr = static_cast<cuuint64_t>(R);
     cuuint64_t dims[3] = {dd, packed ? nh : nr, packed ? nr : nh};
-    cuuint64_t strides[2] = {dd * 2, (packed ? nh : nr) * dd * 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(packed ? hs : rs) * 2,
+                             static_cast<cuuint64_t>(packed ? rs : hs) * 2};
     cuuint32_t box[3] = {64, packed ? 1u : static_cast<cuuint32_t>(rows),
                          packed ? static_cast<cuuint32_t>(rows) : 1u};
     cuuint32_t estr[3] = {1, 1, 1};
@@ -135,7 +137,34 @@ int check_common(int B, int H, int N, int d, float scale, int causal, int dtype)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Layout of the fixed-length entry points: [B, H, N, d] for every tensor, [B, H, N] statistics.
+// Element strides (row, head index) of the eight tensors of a call, in the order
+// q, k, v, o, dout, dq, dk, dv.
+struct Strides {
+    long long rs[8], hs[8];
+};
+enum { kQ = 0, kK, kV, kO, kDO, kDQ, kDK, kDV };
+
+// The strides the kernels address directly go into the layout; q, k, v, dout go into maps.
+void put_strides(fa::Layout& L, const Strides& st)
+{
+    L.o_rs = st.rs[kO]; L.o_hs = st.hs[kO];
+    L.do_rs = st.rs[kDO]; L.do_hs = st.hs[kDO];
+    L.dq_rs = st.rs[kDQ]; L.dq_hs = st.hs[kDQ];
+    L.dk_rs = st.rs[kDK]; L.dk_hs = st.hs[kDK];
+    L.dv_rs = st.rs[kDV]; L.dv_hs = st.hs[kDV];
+}
+
+// Fixed-length entry points: [B, H, N, d] for every tensor, [B, H, N] statistics.
+Strides fixed_strides(int N, int d)
+{
+    Strides st;
+    for (int t = 0; t < 8; ++t) {
+        st.rs[t] = d;
+        st.hs[t] = static_cast<long long>(N) * d;
+    }
+    return st;
+}
+
 fa::Layout fixed_layout(int B, int H, int N, int d)
 {
     fa::Layout L{};
@@ -143,25 +172,26 @@ fa::Layout fixed_layout(int B, int H, int N, int d)
     L.B = B; L.H = H; L.Hkv = H;
     L.Nq = L.Nk = N;
     L.Rq = L.Rk = N;
-    L.q_rs = L.k_rs = d;
-    L.q_hs = L.k_hs = static_cast<long long>(N) * d;
+    put_strides(L, fixed_strides(N, d));
     return L;
 }
 
 // The four bf16 maps of the tensor-core kernels: q, k, v, and (backward) dout.
 int make_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, const void* dout,
-              const fa::Layout& L, int d)
+              const fa::Layout& L, int d, const Strides& st)
 {
     int rc = get_encoder();
     if (rc) return rc;
     const bool packed = L.cu_q != nullptr;
     const long long nhq = packed ? L.H : static_cast<long long>(L.B) * L.H;
     const long long nhk = packed ? L.Hkv : static_cast<long long>(L.B) * L.Hkv;
-    if ((rc = make_map(&maps[0], q, nhq, L.Rq, d, 128, packed)) ||
-        (rc = make_map(&maps[1], k, nhk, L.Rk, d, 128, packed)) ||
-        (rc = make_map(&maps[2], v, nhk, L.Rk, d, 128, packed)))
+    if ((rc = make_map(&maps[0], q, nhq, L.Rq, d, 128, packed, st.rs[kQ], st.hs[kQ])) ||
+        (rc = make_map(&maps[1], k, nhk, L.Rk, d, 128, packed, st.rs[kK], st.hs[kK])) ||
+        (rc = make_map(&maps[2], v, nhk, L.Rk, d, 128, packed, st.rs[kV], st.hs[kV])))
         return rc;
-    if (dout && (rc = make_map(&maps[3], dout, nhq, L.Rq, d, 128, packed))) return rc;
+    if (dout && (rc = make_map(&maps[3], dout, nhq, L.Rq, d, 128, packed, st.rs[kDO],
+                               st.hs[kDO])))
+        return rc;
     return FA_OK;
 }
 
@@ -189,7 +219,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
         e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st);
     } else {
         CUtensorMap maps[4];
-        if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d))) return rc;
+        if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d, fixed_strides(N, d)))) return rc;
         e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -243,7 +273,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     } else {
         // maps: q, k, v, dout (all 128-row boxes)
         CUtensorMap maps[4];
-        if ((rc = make_maps(maps, q, k, v, dout, p.L, d))) return rc;
+        if ((rc = make_maps(maps, q, k, v, dout, p.L, d, fixed_strides(N, d)))) return rc;
         if (stage < 0 || stage == 1) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
         if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq_tc(d, maps, p, st);
     }
@@ -397,17 +427,122 @@ int check_varlen(const int* cu_q, const int* cu_k, int B, int* max_q, int* max_k
     return FA_OK;
 }
 
+// Contiguous packed tensors: q-side [total_q, H, d], k-side [total_k, Hkv, d].
+Strides packed_strides(int H, int Hkv, int d)
+{
+    Strides st;
+    for (int t = 0; t < 8; ++t) {
+        const bool kside = t == kK || t == kV || t == kDK || t == kDV;
+        st.rs[t] = static_cast<long long>(kside ? Hkv : H) * d;
+        st.hs[t] = d;
+    }
+    return st;
+}
+
+// Caller strides: `n` (row, head) pairs in the order q, k, v, o[, dout, dq, dk, dv].  Each must
+// be positive and a multiple of 8 elements (16 bytes, for the tensor maps and the 16-byte
+// stores), and a head must not be wider than its row step (tensors stored token by token).
+int read_strides(const long long* user, int n, int H, int Hkv, int d, Strides* st)
+{
+    *st = packed_strides(H, Hkv, d);
+    if (!user) return fail(FA_ERR_INVALID_ARG, "strides must be non-null");
+    for (int t = 0; t < n; ++t) {
+        const long long rs = user[2 * t], hs = user[2 * t + 1];
+        if (rs <= 0 || hs <= 0 || (rs % 8) || (hs % 8))
+            return fail(FA_ERR_MISALIGNED, "strides must be positive multiples of 8 elements");
+        if (hs < d || rs < hs)
+            return fail(FA_ERR_INVALID_ARG, "each head's d elements must fit within its head step, "
+                                            "and the head step within the row step");
+        st->rs[t] = rs;
+        st->hs[t] = hs;
+    }
+    return FA_OK;
+}
+
 fa::Layout packed_layout(const int* cu_q, const int* cu_k, int B, int max_q, int max_k,
-                         int total_q, int total_k, int H, int Hkv, int d)
+                         int total_q, int total_k, int H, int Hkv, int d, const Strides& st)
 {
     fa::Layout L{};
     L.cu_q = cu_q; L.cu_k = cu_k;
     L.B = B; L.H = H; L.Hkv = Hkv;
     L.Nq = max_q; L.Nk = max_k;
     L.Rq = total_q; L.Rk = total_k;
-    L.q_rs = static_cast<long long>(H) * d; L.q_hs = d;
-    L.k_rs = static_cast<long long>(Hkv) * d; L.k_hs = d;
+    put_strides(L, st);
     return L;
+}
+
+int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_q, const int* cu_k, int B, int max_q, int max_k, int total_q,
+                     int total_k, int H, int Hkv, int d, float scale, int causal,
+                     const long long* user_strides, void* stream)
+{
+    int rc = check_varlen(cu_q, cu_k, B, &max_q, &max_k, total_q, total_k, H, Hkv, d, scale,
+                          causal);
+    if (rc) return rc;
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    Strides st = packed_strides(H, Hkv, d);
+    if (user_strides && (rc = read_strides(user_strides, 4, H, Hkv, d, &st))) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    fa::FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.N = total_q; p.BH = H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    p.L = packed_layout(cu_q, cu_k, B, max_q, max_k, total_q, total_k, H, Hkv, d, st);
+    CUtensorMap maps[4];
+    if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d, st))) return rc;
+    cudaError_t e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return FA_OK;
+}
+
+int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, const int* cu_q,
+                     const int* cu_k, int B, int max_q, int max_k, int total_q, int total_k,
+                     int H, int Hkv, int d, float scale, int causal,
+                     const long long* user_strides, void* workspace, size_t workspace_bytes,
+                     void* stream)
+{
+    int rc = check_varlen(cu_q, cu_k, B, &max_q, &max_k, total_q, total_k, H, Hkv, d, scale,
+                          causal);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+        return fail(FA_ERR_INVALID_ARG, "every tensor pointer must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA_ERR_MISALIGNED, "tensors must be 16-byte aligned (lse 4-byte)");
+    Strides st = packed_strides(H, Hkv, d);
+    if (user_strides && (rc = read_strides(user_strides, 8, H, Hkv, d, &st))) return rc;
+    const size_t need = fa_bwd_varlen_workspace_bytes(total_q, H, d);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    fa::BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    const size_t rows = static_cast<size_t>(H) * total_q;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.delta = reinterpret_cast<float*>(ws);
+    p.lse2 = reinterpret_cast<float*>(ws + align256(rows * 4));
+    p.N = total_q; p.BH = H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    p.L = packed_layout(cu_q, cu_k, B, max_q, max_k, total_q, total_k, H, Hkv, d, st);
+    CUtensorMap maps[4];
+    if ((rc = make_maps(maps, q, k, v, dout, p.L, d, st))) return rc;
+    cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, cs, di->sms);
+    if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, cs);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return FA_OK;
 }
 
 }  // namespace
@@ -417,27 +552,22 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
                              int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H,
                              int Hkv, int d, float scale, int causal, void* stream)
 {
-    int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_seqlen_q, &max_seqlen_k, total_q,
-                          total_k, H, Hkv, d, scale, causal);
-    if (rc) return rc;
-    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
-        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
-    DeviceInfo* di = nullptr;
-    if ((rc = device_info(&di))) return rc;
-    fa::FwdParams p{};
-    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-    p.N = total_q; p.BH = H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
-    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
-    p.debug_flags = g_debug_flags;
-    p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
-                        total_k, H, Hkv, d);
-    CUtensorMap maps[4];
-    if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d))) return rc;
-    cudaError_t e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
-    return FA_OK;
+    return fwd_varlen_entry(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q,
+                            max_seqlen_k, total_q, total_k, H, Hkv, d, scale, causal, nullptr,
+                            stream);
+}
+
+extern "C" int fa_fwd_varlen_strided(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, const long long* strides,
+                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                                     int max_seqlen_q, int max_seqlen_k, int total_q,
+                                     int total_k, int H, int Hkv, int d, float scale, int causal,
+                                     void* stream)
+{
+    if (!strides) return fail(FA_ERR_INVALID_ARG, "strides must be non-null");
+    return fwd_varlen_entry(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q,
+                            max_seqlen_k, total_q, total_k, H, Hkv, d, scale, causal, strides,
+                            stream);
 }
 
 extern "C" size_t fa_bwd_varlen_workspace_bytes(int total_q, int H, int d)
@@ -454,41 +584,23 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
                              int Hkv, int d, float scale, int causal, void* workspace,
                              size_t workspace_bytes, void* stream)
 {
-    int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_seqlen_q, &max_seqlen_k, total_q,
-                          total_k, H, Hkv, d, scale, causal);
-    if (rc) return rc;
-    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
-        return fail(FA_ERR_INVALID_ARG, "every tensor pointer must be non-null");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
-        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return fail(FA_ERR_MISALIGNED, "tensors must be 16-byte aligned (lse 4-byte)");
-    const size_t need = fa_bwd_varlen_workspace_bytes(total_q, H, d);
-    if (!workspace || workspace_bytes < need)
-        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
-    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
-    DeviceInfo* di = nullptr;
-    if ((rc = device_info(&di))) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    fa::BwdParams p{};
-    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
-    p.dq = dq; p.dk = dk; p.dv = dv;
-    const size_t rows = static_cast<size_t>(H) * total_q;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.delta = reinterpret_cast<float*>(ws);
-    p.lse2 = reinterpret_cast<float*>(ws + align256(rows * 4));
-    p.N = total_q; p.BH = H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
-    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
-    p.debug_flags = g_debug_flags;
-    p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
-                        total_k, H, Hkv, d);
-    CUtensorMap maps[4];
-    if ((rc = make_maps(maps, q, k, v, dout, p.L, d))) return rc;
-    cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, st, di->sms);
-    if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
-    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, st);
-    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    return FA_OK;
+    return bwd_varlen_entry(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B,
+                            max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale,
+                            causal, nullptr, workspace, workspace_bytes, stream);
+}
+
+extern "C" int fa_bwd_varlen_strided(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dout, const float* lse, void* dq, void* dk,
+                                     void* dv, const long long* strides, const int* cu_seqlens_q,
+                                     const int* cu_seqlens_k, int B, int max_seqlen_q,
+                                     int max_seqlen_k, int total_q, int total_k, int H, int Hkv,
+                                     int d, float scale, int causal, void* workspace,
+                                     size_t workspace_bytes, void* stream)
+{
+    if (!strides) return fail(FA_ERR_INVALID_ARG, "strides must be non-null");
+    return bwd_varlen_entry(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B,
+                            max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale,
+                            causal, strides, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -580,8 +692,9 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
     p.splits = num_splits; p.G = G; p.q_box = max_seqlen_q;
     p.scale_log2 = scale * fa::kLog2e; p.causal = causal;
     p.status = di->status; p.wait_limit_ns = g_wait_limit_ns; p.debug_flags = g_debug_flags;
+    const Strides st = packed_strides(H, Hkv, d);
     p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
-                        total_k, H, Hkv, d);
+                        total_k, H, Hkv, d, st);
     if ((rc = get_encoder())) return rc;
     // Q: (d, H, total_q) with a box of (64 columns, G heads, max_seqlen_q tokens), so one copy
     // brings the G x nq query rows of a (sequence, key/value head) pair; K, V as fa_fwd_varlen.
@@ -599,8 +712,8 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
         if (r != CUDA_SUCCESS)
             return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
     }
-    if ((rc = make_map(&maps[1], k, Hkv, total_k, d, 128, true)) ||
-        (rc = make_map(&maps[2], v, Hkv, total_k, d, 128, true)))
+    if ((rc = make_map(&maps[1], k, Hkv, total_k, d, 128, true, st.rs[kK], st.hs[kK])) ||
+        (rc = make_map(&maps[2], v, Hkv, total_k, d, 128, true, st.rs[kV], st.hs[kV])))
         return rc;
     cudaError_t e = fa::launch_decode(d, maps[0], maps[1], maps[2], p,
                                       static_cast<cudaStream_t>(stream), di->sms);

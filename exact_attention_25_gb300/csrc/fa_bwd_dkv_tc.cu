@@ -380,9 +380,11 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tAcc = which == 0 ? tDV : tDK;
                 const float mul = which == 0 ? 1.0f : p.scale;
+                const long long rs = which == 0 ? L.dv_rs : L.dk_rs;
+                const long long hs = which == 0 ? L.dv_hs : L.dk_hs;
                 __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) +
-                                         static_cast<size_t>(sr.k0 + krow) * L.k_rs +
-                                         static_cast<size_t>(khead) * L.k_hs;
+                                         static_cast<size_t>(sr.k0 + krow) * rs +
+                                         static_cast<size_t>(khead) * hs;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 64; ++ch) {
                     const int c0 = h * (D / 2) + 32 * ch;
@@ -406,11 +408,13 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             }
         } else if (n_it == 0 && krow < nk) {
             // a key block that no query sees (a sequence without queries) has zero gradient
-            const size_t off = static_cast<size_t>(sr.k0 + krow) * L.k_rs +
-                               static_cast<size_t>(khead) * L.k_hs;
+            const size_t offk = static_cast<size_t>(sr.k0 + krow) * L.dk_rs +
+                                static_cast<size_t>(khead) * L.dk_hs;
+            const size_t offv = static_cast<size_t>(sr.k0 + krow) * L.dv_rs +
+                                static_cast<size_t>(khead) * L.dv_hs;
             for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c) {
-                static_cast<__nv_bfloat16*>(p.dk)[off + c] = __float2bfloat16_rn(0.0f);
-                static_cast<__nv_bfloat16*>(p.dv)[off + c] = __float2bfloat16_rn(0.0f);
+                static_cast<__nv_bfloat16*>(p.dk)[offk + c] = __float2bfloat16_rn(0.0f);
+                static_cast<__nv_bfloat16*>(p.dv)[offv + c] = __float2bfloat16_rn(0.0f);
             }
         }
         tc_fence_before();

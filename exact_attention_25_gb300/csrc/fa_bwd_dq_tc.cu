@@ -370,8 +370,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
             tc_fence_after();
             __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) +
-                                     static_cast<size_t>(sr.q0 + qrow) * L.q_rs +
-                                     static_cast<size_t>(qhead) * L.q_hs;
+                                     static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
+                                     static_cast<size_t>(qhead) * L.dq_hs;
 #pragma unroll 1
             for (int ch = 0; ch < D / 64; ++ch) {
                 const int c0 = h * (D / 2) + 32 * ch;
@@ -395,8 +395,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         } else if (n_it == 0 && qrow < nq) {
             // a query block that sees no key (more queries than keys, or no keys) has zero
             // gradient
-            const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.q_rs +
-                               static_cast<size_t>(qhead) * L.q_hs;
+            const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
+                               static_cast<size_t>(qhead) * L.dq_hs;
             for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c)
                 static_cast<__nv_bfloat16*>(p.dq)[off + c] = __float2bfloat16_rn(0.0f);
         }

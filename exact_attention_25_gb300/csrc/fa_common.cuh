@@ -69,8 +69,13 @@ struct Layout {
     int B, H, Hkv;         // sequences, query heads, key/value heads (H % Hkv == 0)
     int Nq, Nk;            // fixed: rows per sequence; packed: largest sequence (grid, clamps)
     int Rq, Rk;            // rows per head index: fixed Nq, Nk; packed total_q, total_k
-    long long q_rs, q_hs;  // element strides of one row and one head index: q, o, dO, dQ
-    long long k_rs, k_hs;  // the same for k, v, dK, dV
+    // Element strides of one row and one head index of the tensors the kernels address
+    // directly (q, k, v and dO are read through tensor maps that carry their own strides).
+    long long o_rs, o_hs;
+    long long do_rs, do_hs;
+    long long dq_rs, dq_hs;
+    long long dk_rs, dk_hs;
+    long long dv_rs, dv_hs;
 };
 
 // Rows of sequence b: global row offsets q0 / k0 and lengths nq / nk.  Packed offsets and

@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                     packed[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
                                             __uint_as_float(o[2 * c + 1]) * inv_l);
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                                      t * L.q_rs + static_cast<size_t>(h) * L.q_hs +
+                                                      t * L.o_rs + static_cast<size_t>(h) * L.o_hs +
                                                       32 * ch);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -468,8 +468,8 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodePara
             }
         }
         const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + t * L.q_rs +
-                             static_cast<size_t>(h) * L.q_hs + lane * EPL;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + t * L.o_rs +
+                             static_cast<size_t>(h) * L.o_hs + lane * EPL;
         if constexpr (EPL == 4) {
             *reinterpret_cast<uint2*>(dst) =
                 make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));

@@ -431,8 +431,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int eb = static_cast<int>(blockIdx.x) / n_pairs;
         const SeqRows se = seq_rows<PACKED>(L, eb / L.H);
         const int eqhead = q_head_index<PACKED>(L, eb / L.H, eb % L.H);
-        const size_t orow_off = static_cast<size_t>(se.q0 + qrow) * L.q_rs +
-                                static_cast<size_t>(eqhead) * L.q_hs;
+        const size_t orow_off = static_cast<size_t>(se.q0 + qrow) * L.o_rs +
+                                static_cast<size_t>(eqhead) * L.o_hs;
         const size_t lse_off = static_cast<size_t>(eqhead) * L.Rq + se.q0 + qrow;
         if (ok && Jt > 0) {
             if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {

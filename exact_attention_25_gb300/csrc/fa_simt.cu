@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
     constexpr int TPR = D / EPV;         // threads per row (8, 16 or 32)
     constexpr int RPW = 32 / TPR;        // rows per warp and iteration
     // Rows t = hh * Rq + i of the statistics arrays: row i of head index hh, whose elements sit
-    // at i * q_rs + hh * q_hs (either layout).
+    // at i * rs + hh * hs with the strides of O and of dO.
     const Layout& L = p.L;
     const size_t n_heads = static_cast<size_t>(L.cu_q == nullptr ? L.B * L.H : L.H);
     const size_t rows = n_heads * static_cast<size_t>(L.Rq);
@@ -163,9 +163,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
         float acc = 0.0f;
         if (valid) {
             const size_t hh = row / static_cast<size_t>(L.Rq), i = row - hh * static_cast<size_t>(L.Rq);
-            const size_t off = i * static_cast<size_t>(L.q_rs) + hh * static_cast<size_t>(L.q_hs);
-            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off)[sub];
-            const uint4 b = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off)[sub];
+            const size_t off_o = i * static_cast<size_t>(L.o_rs) + hh * static_cast<size_t>(L.o_hs);
+            const size_t off_g = i * static_cast<size_t>(L.do_rs) + hh * static_cast<size_t>(L.do_hs);
+            const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off_o)[sub];
+            const uint4 b = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off_g)[sub];
             const T* ea = reinterpret_cast<const T*>(&a);
             const T* eb = reinterpret_cast<const T*>(&b);
 #pragma unroll

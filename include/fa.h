@@ -132,6 +132,28 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
                   int total_k, int H, int Hkv, int d, float scale, int causal, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* fa_fwd_varlen / fa_bwd_varlen on tensors with caller-chosen element strides, so that views
+ * need no copy: for example q, k and v taken from one fused projection [total, 3, H, d], or
+ * outputs written into slices of larger buffers.  strides is a host array of (row, head)
+ * element-stride pairs, one pair per tensor in argument order: q, k, v, o for the forward
+ * (8 values); q, k, v, o, dout, dq, dk, dv for the backward (16 values).  Row i, head h of a
+ * tensor starts at base + i * row + h * head elements; its d elements are contiguous.
+ * Each stride must be a positive multiple of 8 elements (16 bytes; else FA_ERR_MISALIGNED),
+ * head >= d and row >= head (tensors stored token by token; else FA_ERR_INVALID_ARG).
+ * Output views must not overlap.  Everything else as fa_fwd_varlen / fa_bwd_varlen. */
+int fa_fwd_varlen_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const long long* strides, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, int B, int max_seqlen_q, int max_seqlen_k,
+                          int total_q, int total_k, int H, int Hkv, int d, float scale,
+                          int causal, void* stream);
+
+int fa_bwd_varlen_strided(const void* q, const void* k, const void* v, const void* o,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          const long long* strides, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, int B, int max_seqlen_q, int max_seqlen_k,
+                          int total_q, int total_k, int H, int Hkv, int d, float scale,
+                          int causal, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Split-KV decode: the forward of fa_fwd_varlen (same arguments, layout, mask, results up to
  * rounding) laid out for few queries per sequence against a long key/value history, the
  * decoding case that "서빙에서 Flash Attention 이득이 예상보다 작은 경우" in "Flash Attention

@@ -200,3 +200,21 @@ def test_decode_rejects_bad_arguments(lib):
     assert call(ws=MIS) == -3
     assert call(d=80) == -2
     assert lib.fa_decode_num_splits(0, 8, 100) == -1
+
+
+def test_strided_varlen_rejects_bad_strides(lib):
+    def fwd_st(vals):
+        arr = None if vals is None else (ctypes.c_longlong * len(vals))(*vals)
+        return lib.fa_fwd_varlen_strided(A, A, A, A2, A2, arr, A, A, 2, 10, 10, 20, 20, 4, 2, 128,
+                                         ctypes.c_float(0.1), 1, None)
+
+    good = [3 * 4 * 128, 128, 3 * 4 * 128, 128, 3 * 4 * 128, 128, 4 * 128, 128]
+    assert fwd_st(None) == -1
+    bad = list(good); bad[0] = 3 * 4 * 128 + 4          # row stride not a multiple of 8
+    assert fwd_st(bad) == -3
+    bad = list(good); bad[3] = 64                       # head step narrower than d = 128
+    assert fwd_st(bad) == -1
+    bad = list(good); bad[6] = 64; bad[7] = 128          # row step narrower than the head step
+    assert fwd_st(bad) == -1
+    bad = list(good); bad[5] = 0
+    assert fwd_st(bad) == -3
