@@ -30,7 +30,13 @@ struct FwdCfg {
     static constexpr int SMEM_Q = NT * TILE_BYTES;
     static constexpr int SMEM_K = STAGES * TILE_BYTES;
     static constexpr int SMEM_V = STAGES * TILE_BYTES;
-    static constexpr int SMEM_BYTES = SMEM_Q + SMEM_K + SMEM_V + 1024;  // + alignment slack
+    // d = 64: the P V product runs at N = 128 against V and a constant panel whose first column
+    // is 1.0, so O's column 64 accumulates the sum of the bf16 P weights on the tensor core
+    // (the row sum that normalises O), instead of ~190 softmax instructions per row and block.
+    static constexpr bool SUM_ON_MMA = (D == 64);
+    static constexpr int O_COLS = SUM_ON_MMA ? 128 : D;  // TMEM columns of one O accumulator
+    static constexpr int SMEM_ONES = SUM_ON_MMA ? PANEL_BYTES : 0;
+    static constexpr int SMEM_BYTES = SMEM_Q + SMEM_K + SMEM_V + SMEM_ONES + 1024;  // + slack
     static constexpr int THREADS = 320;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P stays below 2^8
@@ -72,6 +78,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     uint8_t* sQ = smem;
     uint8_t* sK = sQ + C::SMEM_Q;
     uint8_t* sV = sK + C::SMEM_K;
+    uint8_t* sOnes = sV + C::SMEM_V;  // d = 64 only: the constant column panel
 
     __shared__ __align__(8) uint64_t bar_q;
     __shared__ __align__(8) uint64_t bar_kfull[C::STAGES];
@@ -146,6 +153,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tmem_alloc(&tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    if constexpr (C::SUM_ON_MMA) {
+        // 128 key rows x 64 bf16 columns, 128-byte swizzled like a TMA-written MN-major tile:
+        // column 0 of key row r sits in 16-byte chunk (0 ^ r % 8) of the row.  Written by the
+        // 256 softmax threads, then made visible to the tensor core (async proxy).
+        if (warp < 8) {
+            uint4* dst = reinterpret_cast<uint4*>(sOnes);
+            for (int i = threadIdx.x; i < C::PANEL_BYTES / 16; i += 256) {
+                const int row = i >> 3, chunk = i & 7;
+                dst[i] = make_uint4(chunk == (row & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+        }
+    }
     if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -200,16 +220,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // ------------------------------------------------------------- MMA issuer
         {  // the whole warp runs the loop (warp-uniform values); elect.sync picks the issuer
             constexpr uint32_t kIdS = idesc_bf16_f32(128, C::BN, 0, 0);  // S = Q K^T
-            constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);     // O += P V
+            constexpr uint32_t kIdPV = idesc_bf16_f32(128, C::O_COLS, 0, 1);  // O += P V
             // Everything the issue loop needs lives in scalar registers: base descriptors are
             // built once and advanced by byte offsets (stage, tile, k-step), so the single
             // issuing thread keeps pace with the tensor core.
             const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+            // V is MN-major; its second 64-column panel is the next panel of the stage (d = 128)
+            // or the constant column panel (d = 64), at a stage-dependent distance.
             const uint64_t dv0 = sdesc_sw128(smem_u32(sV), C::PANEL_BYTES, 1024);
+            const uint64_t dvo = sdesc_sw128(smem_u32(sV), smem_u32(sOnes) - smem_u32(sV), 1024);
+            auto vdesc = [&](int s) {
+                if constexpr (C::SUM_ON_MMA) {
+                    // stage s: start address up, distance to the constant panel down, by the
+                    // same number of 16-byte units (both fields sit in the low word and stay
+                    // in range, so neither borrows nor carries)
+                    const uint32_t u = static_cast<uint32_t>(s * C::TILE_BYTES) >> 4;
+                    return (dvo & 0xFFFFFFFF00000000ull) |
+                           static_cast<uint32_t>(static_cast<uint32_t>(dvo) + u - (u << 16));
+                } else {
+                    return sdesc_adv(dv0, s * C::TILE_BYTES);
+                }
+            };
             const int J0 = J[0], J1 = J[1];
             const uint32_t tS0 = tbase, tS1 = tbase + 128u;
-            const uint32_t tO0 = tbase + 256u, tO1 = tbase + 256u + D;
+            const uint32_t tO0 = tbase + 256u, tO1 = tbase + 256u + C::O_COLS;
 
             // (no key block at all: nothing to issue, the softmax warps write empty rows)
             bool ok = Jmax > 0 && warp_wait_all(&bar_q, 0, wd, kSiteFwdMmaQ);
@@ -233,7 +268,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 const uint32_t ph = (j / C::STAGES) & 1;
                 const int s1 = (j + 1) % C::STAGES;
                 const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
-                const uint64_t vd = sdesc_adv(dv0, s * C::TILE_BYTES);
+                const uint64_t vd = vdesc(s);
                 const uint64_t kd1 = sdesc_adv(dk0, s1 * C::TILE_BYTES);
                 const uint32_t acc_first = j > 0 ? 1u : 0u;
                 if (!warp_wait_all(&bar_vfull[s], ph, wd, kSiteFwdMmaV)) { ok = false; break; }
@@ -294,7 +329,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tbase + lane_base + 128u * t;
         const uint32_t tP = tS + 64u;
-        const uint32_t tO = tbase + lane_base + 256u + static_cast<uint32_t>(t * D);
+        const uint32_t tO = tbase + lane_base + 256u + static_cast<uint32_t>(t * C::O_COLS);
         const int qt = qt0 + t;
         const int qrow = qt * C::BM + r;  // row within the sequence
         // Element-wise masking is needed from key block jmask on: the blocks that straddle the
@@ -390,11 +425,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     lsa = f2_add(lsa, f2_make(p0, p1));
                     lsb = f2_add(lsb, f2_make(p2, p3));
                     // lr sums the bf16-rounded weights that the P V product uses, so that
-                    // O = sum(P V) / lr is an exact convex combination of those weights.
-                    lra = f2_add(lra, f2_make(__uint_as_float(w01 << 16),
-                                              __uint_as_float(w01 & 0xFFFF0000u)));
-                    lrb = f2_add(lrb, f2_make(__uint_as_float(w23 << 16),
-                                              __uint_as_float(w23 & 0xFFFF0000u)));
+                    // O = sum(P V) / lr is an exact convex combination of those weights
+                    // (at d = 64 the tensor core forms this sum in O's column 64).
+                    if constexpr (!C::SUM_ON_MMA) {
+                        lra = f2_add(lra, f2_make(__uint_as_float(w01 << 16),
+                                                  __uint_as_float(w01 & 0xFFFF0000u)));
+                        lrb = f2_add(lrb, f2_make(__uint_as_float(w23 << 16),
+                                                  __uint_as_float(w23 & 0xFFFF0000u)));
+                    }
                     pk[c / 2] = w01;
                     pk[c / 2 + 1] = w23;
                 }
@@ -410,8 +448,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             // O still holds the sum up to block j-1 (the commit that signalled S for block j
             // also covers the P V product of block j-1).
             if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // (d = 64: columns 64..95 hold the rounded row sum, rescaled with O)
 #pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
+                for (int ch = 0; ch < (C::SUM_ON_MMA ? D / 32 + 1 : D / 32); ++ch) {
                     uint32_t o[32];
                     tmem_ld32(tO + 32u * ch, o);
                     tmem_wait_ld();
@@ -438,6 +477,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
                 tc_fence_after();
                 // a row that sees no key (possible when queries outnumber keys) stays 0
+                if constexpr (C::SUM_ON_MMA) {  // the rounded row sum from O's column 64
+                    uint32_t sc[32];
+                    tmem_ld32(tO + 64u, sc);
+                    tmem_wait_ld();
+                    reg_fence32(sc);
+                    lr = __uint_as_float(sc[0]);
+                }
                 const float inv_l = lr > 0.0f ? 1.0f / lr : 0.0f;
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + orow_off;
 #pragma unroll 1

@@ -190,6 +190,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
                  : "memory");
 }
 
+// Makes this thread's ordinary shared-memory stores visible to the async proxy (the tensor
+// core and TMA), for data written with st.shared and then read as an MMA operand.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
