@@ -41,8 +41,9 @@ def test_largest_accepted_problem_sampled_rows():
             assert rel_l2(dk[0, h, krows], ref["dk"]) <= TOL_GRAD_REL_L2
             assert rel_l2(dv[0, h, krows], ref["dv"]) <= TOL_GRAD_REL_L2
     # identities at every head (any size): rows of dS sum to 0, rows of P to 1
-    dk_sum = dk.double().sum(2)
-    dk_norm = dk.double().abs().sum(2)
+    dk_sum = dk.sum(2, dtype=torch.float64)
+    dk_norm = dk.abs().sum(2, dtype=torch.float64)
     assert bool((dk_sum.abs() <= 2e-2 * dk_norm + 1e-3).all())
-    assert torch.allclose(dv.double().sum(2), do.double().sum(2), rtol=2e-2, atol=0.25)
+    assert torch.allclose(dv.sum(2, dtype=torch.float64), do.sum(2, dtype=torch.float64),
+                          rtol=2e-2, atol=0.25)
     assert np.isfinite(f64(lse[0, :, -1])).all()
