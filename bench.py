@@ -49,6 +49,34 @@ def dist_setup():
     return ws, rank, local
 
 
+def run_near_gpu(device_index: int) -> str:
+    """Restrict this process to the CPUs of the GPU's own NUMA node, so that pinned host
+    buffers (placed where the allocating thread runs) sit next to the GPU.  Returns the node
+    or a reason it was left alone."""
+    import torch
+
+    try:
+        props = torch.cuda.get_device_properties(device_index)
+        pci = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{pci}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return "no NUMA node reported"
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return f"node {node}: none of its CPUs are available"
+        os.sched_setaffinity(0, cpus)
+        return f"node {node}"
+    except Exception as e:  # informational only: the measurement proceeds either way
+        return f"left alone ({type(e).__name__})"
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """The largest value of x over all ranks (the job's time is its slowest rank's)."""
     import torch
@@ -239,6 +267,7 @@ def run_gpu(args):
     # results device -> host.  The steps are pipelined over two device buffer sets and three
     # streams (copy-in, compute, copy-out): step i+1's inputs and step i-1's results move while
     # step i computes, as a serving or training loop would overlap them.
+    host_node = run_near_gpu(local)
     hq, hk, hv, hdo = (t.pin_memory() for t in (x["q"], x["k"], x["v"], x["do"]))
     ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -347,6 +376,7 @@ def run_gpu(args):
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "pinned_host_memory": host_node,
                 "overlap": "step i+1's host->device and step i-1's device->host copies run on "
                            "their own streams while step i computes (two device buffer sets)"},
         "gpu_launches": args.steps * 4,
