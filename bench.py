@@ -170,7 +170,7 @@ def kernel_source_sha256(kernel: str) -> str:
     csrc = os.path.join(root, "exact_attention_25_gb300", "csrc")
     h = hashlib.sha256()
     for path in (os.path.join(csrc, KERNEL_SOURCES[kernel]), os.path.join(csrc, "fa_common.cuh"),
-                 os.path.join(csrc, "tc_ptx.cuh"), os.path.join(root, "include", "fa.h")):
+                 os.path.join(csrc, "tc_ptx.cuh")):
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()
