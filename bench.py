@@ -164,15 +164,21 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_sha256(kernel: str) -> str:
+    """Hash of the code of `kernel` (its .cu file and the two device headers), with comments
+    and whitespace removed so that editing a comment does not count as changing the kernel."""
     import hashlib
+    import re
 
     root = os.path.dirname(os.path.abspath(__file__))
     csrc = os.path.join(root, "exact_attention_25_gb300", "csrc")
     h = hashlib.sha256()
     for path in (os.path.join(csrc, KERNEL_SOURCES[kernel]), os.path.join(csrc, "fa_common.cuh"),
                  os.path.join(csrc, "tc_ptx.cuh")):
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -12,7 +12,9 @@
 //   warp  8     TMA producer (whole warp, one elected lane issues)
 //   warp  9     TMEM allocator + MMA issuer (whole warp, one elected lane issues)
 // TMEM columns: S_t at [128t, 128t+128) (fp32), P_t (bf16 pairs) aliased on the upper half
-// of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised).
+// of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised); at d = 64, O_t at
+// [256 + 128t, 384 + 128t), whose column 64 accumulates the row sum of the bf16 P (the P V
+// product runs at N = 128 against V and a constant ones-column panel).
 #include "fa_common.cuh"
 #include "tc_ptx.cuh"
 
