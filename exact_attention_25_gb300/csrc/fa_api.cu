@@ -9,6 +9,7 @@
 #include <string>
 
 #include "fa_common.cuh"
+#include "fa_decode.cuh"
 
 namespace fa {
 cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -661,15 +662,20 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
     int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_seqlen_q, &max_seqlen_k, total_q,
                           total_k, H, Hkv, d, scale, causal);
     if (rc) return rc;
-    const int G = H / Hkv;
-    if (static_cast<long long>(G) * max_seqlen_q > 128)
-        return fail(FA_ERR_INVALID_ARG, "(H / Hkv) * max_seqlen_q must be <= 128 for the decode "
-                                        "kernel; use fa_fwd_varlen");
+    // The rows of a CTA are G query heads of a group times max_seqlen_q queries, at most 128:
+    // G is the largest divisor of the group size H / Hkv that fits.
+    if (max_seqlen_q > 128)
+        return fail(FA_ERR_INVALID_ARG, "max_seqlen_q must be <= 128 for the decode kernel; use "
+                                        "fa_fwd_varlen");
+    const int group = H / Hkv;
+    int G = 1;
+    for (int g = 1; g <= group; ++g)
+        if (group % g == 0 && g * max_seqlen_q <= 128) G = g;
     if (num_splits < 1 || num_splits > kDecodeMaxSplits)
         return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, " +
                                             std::to_string(kDecodeMaxSplits) + "]");
-    if (static_cast<long long>(B) * Hkv * num_splits >= (1LL << 31))
-        return fail(FA_ERR_TOO_LARGE, "B * Hkv * num_splits must be < 2^31");
+    if (static_cast<long long>(B) * Hkv * (group / G) * num_splits >= (1LL << 31))
+        return fail(FA_ERR_TOO_LARGE, "B * H / G * num_splits must be < 2^31");
     if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
@@ -689,7 +695,7 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
         p.o_part = reinterpret_cast<float*>(ws);
         p.lse_part = reinterpret_cast<float*>(ws + decode_part_o_bytes(total_q, H, d, num_splits));
     }
-    p.splits = num_splits; p.G = G; p.q_box = max_seqlen_q;
+    p.splits = num_splits; p.G = G; p.head_chunks = group / G; p.q_box = max_seqlen_q;
     p.scale_log2 = scale * fa::kLog2e; p.causal = causal;
     p.status = di->status; p.wait_limit_ns = g_wait_limit_ns; p.debug_flags = g_debug_flags;
     const Strides st = packed_strides(H, Hkv, d);
@@ -697,7 +703,7 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
                         total_k, H, Hkv, d, st);
     if ((rc = get_encoder())) return rc;
     // Q: (d, H, total_q) with a box of (64 columns, G heads, max_seqlen_q tokens), so one copy
-    // brings the G x nq query rows of a (sequence, key/value head) pair; K, V as fa_fwd_varlen.
+    // brings the G x nq query rows of a CTA; K, V as fa_fwd_varlen.
     CUtensorMap maps[4];
     {
         const cuuint64_t dd = static_cast<cuuint64_t>(d);

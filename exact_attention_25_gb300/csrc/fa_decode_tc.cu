@@ -15,7 +15,7 @@
 // warp 5 TMEM allocator and MMA issuer.  TMEM: two S buffers [0,128), [128,256) so S of block
 // j+1 is computed while the softmax works on block j (P of a block, bf16 pairs, overwrites the
 // upper half of its S buffer), O at [256, 256+d).
-#include "fa_common.cuh"
+#include "fa_decode.cuh"
 #include "tc_ptx.cuh"
 
 namespace fa {
@@ -84,9 +84,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Layout& L = p.L;
-    const int bkv = static_cast<int>(blockIdx.x) / p.splits;
     const int split = static_cast<int>(blockIdx.x) % p.splits;
+    const int rest = static_cast<int>(blockIdx.x) / p.splits;
+    const int chunk = rest % p.head_chunks, bkv = rest / p.head_chunks;
     const int b = bkv / L.Hkv, hk = bkv % L.Hkv;
+    const int h0 = hk * (L.H / L.Hkv) + chunk * p.G;  // first query head of this CTA
     const SeqRows sr = seq_rows<true>(L, b);
     const int nq = min(sr.nq, p.q_box), nk = sr.nk;
     if (nq == 0) return;  // no queries in this sequence (whole CTA, before any sync)
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         const uint32_t q_bytes = static_cast<uint32_t>(C::PANELS * 128 * G * p.q_box);
         mbar_arrive_expect_tx_w(&bar_q, q_bytes);
         for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_3d_w(sQ + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn, hk * G, sr.q0);
+            tma_load_3d_w(sQ + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn, h0, sr.q0);
         int issued = 0;
         for (int jj = 0; jj < J; ++jj) {
             const int s = jj % C::STAGES;
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         const int r = threadIdx.x;  // tile row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t tO = tbase + lane_base + 256u;
-        const int i = r / G;  // query of this row within the sequence (head hk * G + r % G)
+        const int i = r / G;  // query of this row within the sequence (head h0 + r % G)
         // x = S * c with c = scale * log2(e); for c <= 0 the scores are scaled first so that
         // masked entries stay -inf (as in the forward kernel).
         const float c2 = p.scale_log2;
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             if (lane == 0) mbar_arrive(&bar_pfull);
         }
         // ------------------------------------------------------------- epilogue
-        // Row r holds query i of head hk * G + g.  With one split this is the final result;
+        // Row r holds query i of head h0 + g.  With one split this is the final result;
         // with several, the range's O normalised by its own weights and its natural-log LSE.
         // A row that sees no key of the range (or a range without blocks) gives O = 0 and
         // lse = -inf, which the combine step weighs with e^{-inf} = 0.
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         const bool valid = r < G * nq;
         const int g = r - i * G;
         const size_t t = static_cast<size_t>(sr.q0) + i;  // token row of the packed tensors
-        const int h = hk * G + g;
+        const int h = h0 + g;
         const float inv_l = lr > 0.0f ? 1.0f / lr : 0.0f;
         const float lse_row = (have && l > 0.0f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll 1
@@ -497,7 +499,7 @@ static cudaError_t launch_decode_impl(const CUtensorMap& tq, const CUtensorMap& 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid(p.L.B * p.L.Hkv * p.splits);
+    dim3 grid(p.L.B * p.L.Hkv * p.head_chunks * p.splits);
     fa_decode_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;

@@ -157,11 +157,13 @@ int fa_bwd_varlen_strided(const void* q, const void* k, const void* v, const voi
 /* Split-KV decode: the forward of fa_fwd_varlen (same arguments, layout, mask, results up to
  * rounding) laid out for few queries per sequence against a long key/value history, the
  * decoding case that "서빙에서 Flash Attention 이득이 예상보다 작은 경우" in "Flash Attention
- * IO-awareness principle" hands to decoding kernels.  The G = H / Hkv query heads of a group
- * and the sequence's queries share one 128-row tile, so they read their K and V once; each
- * sequence's key blocks are split into num_splits ranges processed in parallel, whose partial
- * results (O and log-sum-exp per range) a second kernel merges.
- *   - Requires (H / Hkv) * max_seqlen_q <= 128 (else FA_ERR_INVALID_ARG: use fa_fwd_varlen).
+ * IO-awareness principle" hands to decoding kernels.  The query heads of a group (H / Hkv)
+ * and the sequence's queries share one 128-row tile, so they read their K and V once (when
+ * the group times max_seqlen_q exceeds 128 rows, the group's heads are split into the fewest
+ * equal chunks that fit, one tile each); each sequence's key blocks are split into num_splits
+ * ranges processed in parallel, whose partial results (O and log-sum-exp per range) a second
+ * kernel merges.
+ *   - Requires max_seqlen_q <= 128 (else FA_ERR_INVALID_ARG: use fa_fwd_varlen).
  *   - num_splits in [1, 256]; fa_decode_num_splits suggests one for this GPU.  Ranges with no
  *     key block (num_splits larger than the blocks of a sequence) contribute nothing.
  *   - workspace: caller-owned device buffer of fa_decode_workspace_bytes(total_q, H, d,

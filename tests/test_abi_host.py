@@ -181,17 +181,17 @@ def test_varlen_backward_rejects_bad_arguments(lib):
 
 
 def test_decode_rejects_bad_arguments(lib):
-    need = lib.fa_decode_workspace_bytes(64, 32, 128, 4)
-    assert need >= 4 * 64 * 32 * (128 + 1) * 4
+    need = lib.fa_decode_workspace_bytes(256, 32, 128, 4)
+    assert need >= 4 * 256 * 32 * (128 + 1) * 4
     assert lib.fa_decode_workspace_bytes(8, 32, 128, 1) == 0
     assert lib.fa_decode_workspace_bytes(8, 32, 128, 0) == 0
     assert lib.fa_decode_workspace_bytes(8, 32, 96, 2) == 0
 
     def call(H=32, Hkv=8, max_q=1, splits=4, ws=A, nbytes=need, d=128):
-        return lib.fa_fwd_decode(A, A, A, A2, A2, A, A, 8, max_q, 1000, 64, 8000, H, Hkv, d,
+        return lib.fa_fwd_decode(A, A, A, A2, A2, A, A, 8, max_q, 1000, 256, 8000, H, Hkv, d,
                                  ctypes.c_float(0.1), 1, splits, ws, nbytes, None)
 
-    assert call(max_q=33) == -1            # 4 heads x 33 queries > 128 rows
+    assert call(max_q=129) == -1           # more queries than one 128-row tile
     assert call(H=30) == -1                # H % Hkv
     assert call(splits=0) == -1
     assert call(splits=257) == -1

@@ -31,6 +31,8 @@ CASES = {
     "speculative_4": ([4, 4, 2], [300, 1025, 2], 16, 2),
     "full_tile": ([16, 9], [16, 900], 8, 1),
     "empty_sequences": ([1, 0, 1, 1], [0, 50, 260, 1], 8, 2),
+    "heads_over_two_tiles": ([8, 3], [700, 129], 32, 1),      # 32 x 8 rows: chunks of 16 heads
+    "group_not_a_power_of_two": ([11, 5], [300, 1000], 12, 1),  # 12 x 11 rows: chunks of 6
 }
 
 
@@ -101,10 +103,10 @@ def test_decode_step_at_serving_size_sampled_groups():
     print("decode at size, splits", splits, stats)
 
 
-def test_decode_rejects_groups_that_do_not_fit_one_tile():
-    x = random_varlen([9], [100], 16, 1, 64, seed=1, with_do=False)  # 16 x 9 > 128 rows
+def test_decode_rejects_more_queries_than_one_tile():
+    x = random_varlen([129], [300], 2, 1, 64, seed=1, with_do=False)  # 129 queries > 128 rows
     dev = {n: x[n].cuda() for n in ("q", "k", "v", "cu_q", "cu_k")}
     with pytest.raises(fa.FaError) as ei:
-        fa.forward_decode(dev["q"], dev["k"], dev["v"], dev["cu_q"], dev["cu_k"], 9, 100,
+        fa.forward_decode(dev["q"], dev["k"], dev["v"], dev["cu_q"], dev["cu_k"], 129, 300,
                           num_splits=1)
     assert ei.value.code == -1
