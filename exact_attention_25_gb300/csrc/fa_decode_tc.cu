@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+    // The combine kernel may be scheduled now (programmatic dependent launch); it waits for
+    // this whole grid to finish before it reads the partial results.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 4) {
         // ------------------------------------------------------------- TMA producer
@@ -434,6 +437,9 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodeParams p)
 {
     constexpr int EPL = D / 32;  // columns per lane
+    // launched as a programmatic dependent of the split kernel: wait until that grid has
+    // completed and its partial results are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Layout& L = p.L;
     const size_t rows = static_cast<size_t>(L.Rq) * L.H;
     const int lane = threadIdx.x & 31;
@@ -507,8 +513,18 @@ static cudaError_t launch_decode_impl(const CUtensorMap& tq, const CUtensorMap& 
     long blocks = (rows + 7) / 8;  // 8 warps (rows) per CTA
     const long cap = static_cast<long>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    fa_decode_combine_kernel<D><<<static_cast<int>(blocks), 256, 0, st>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the combine grid's launch overlaps the split grid's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D>, p);
 }
 
 cudaError_t launch_decode(int d, const CUtensorMap& tq, const CUtensorMap& tk,
