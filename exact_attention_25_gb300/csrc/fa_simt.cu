@@ -49,17 +49,66 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// Stage rows [row0, row0+rows) of one head into shared memory as fp32 with row stride ld;
-// rows at or beyond N are zero.
-template <typename T, int D>
-__device__ __forceinline__ void stage_rows(float* dst, int ld, const T* head, int row0, int rows,
-                                           int N)
+// Four consecutive elements as fp32 (one 16-byte load for fp32, one 8-byte load for bf16).
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p)
 {
-    for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p)
+{
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// Stage rows [row0, row0+ROWS) of one head into shared memory as fp32 with row stride ld;
+// rows at or beyond N are zero.  Every thread of the 128-thread CTA first loads all of its
+// 4-element vectors into registers and only then stores them, so the loads of a whole tile
+// are in flight together.
+template <typename T, int D, int ROWS>
+__device__ __forceinline__ void stage_rows(float* dst, int ld, const T* head, int row0, int N)
+{
+    constexpr int NV = ROWS * D / 4;          // 4-element vectors in the tile
+    constexpr int PER = (NV + 127) / 128;     // per thread
+    float4 vals[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = (static_cast<int>(threadIdx.x) + i * 128) * 4;
         const int r = e / D, c = e % D;
         const int g = row0 + r;
-        dst[r * ld + c] = (g < N) ? ld_elem(head + static_cast<size_t>(g) * D + c) : 0.0f;
+        vals[i] = (e < ROWS * D && g < N) ? load4(head + static_cast<size_t>(g) * D + c)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = (static_cast<int>(threadIdx.x) + i * 128) * 4;
+        if (e < ROWS * D) {
+            float* d = dst + (e / D) * ld + (e % D);
+            d[0] = vals[i].x;
+            d[1] = vals[i].y;
+            d[2] = vals[i].z;
+            d[3] = vals[i].w;
+        }
+    }
+}
+
+// Dot product of two D-vectors in shared memory with four independent partial sums.
+template <int D>
+__device__ __forceinline__ float dot_smem(const float* a, const float* b)
+{
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int c = 0; c < D; c += 4) {
+        s0 = fmaf(a[c], b[c], s0);
+        s1 = fmaf(a[c + 1], b[c + 1], s1);
+        s2 = fmaf(a[c + 2], b[c + 2], s2);
+        s3 = fmaf(a[c + 3], b[c + 3], s3);
+    }
+    return (s0 + s1) + (s2 + s3);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -80,7 +129,7 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
     const T* q = static_cast<const T*>(p.q) + hoff;
     const T* k = static_cast<const T*>(p.k) + hoff;
     const T* v = static_cast<const T*>(p.v) + hoff;
-    stage_rows<T, D>(Qs, D, q, row_base, kSimtRows, N);
+    stage_rows<T, D, kSimtRows>(Qs, D, q, row_base, N);
 
     const float c2 = p.scale_log2;
     float m[kSimtRowsPerWarp], l[kSimtRowsPerWarp], o[kSimtRowsPerWarp][DL];
@@ -95,32 +144,50 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
     const int n_tiles = p.causal ? (last_row / kSimtTile + 1) : (N + kSimtTile - 1) / kSimtTile;
     for (int kt = 0; kt < n_tiles; ++kt) {
         __syncthreads();
-        stage_rows<T, D>(Ks, D + 1, k, kt * kSimtTile, kSimtTile, N);
-        stage_rows<T, D>(Vs, D, v, kt * kSimtTile, kSimtTile, N);
+        stage_rows<T, D, kSimtTile>(Ks, D + 1, k, kt * kSimtTile, N);
+        stage_rows<T, D, kSimtTile>(Vs, D, v, kt * kSimtTile, N);
         __syncthreads();
         const int key = kt * kSimtTile + lane;
+        // scores of this warp's rows against the tile's keys (lane = key) ...
+        float pr[kSimtRowsPerWarp], alpha[kSimtRowsPerWarp];
 #pragma unroll
         for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
             const int lr = warp * kSimtRowsPerWarp + rr;
             const int row = row_base + lr;
-            float s = 0.0f;
-#pragma unroll 8
-            for (int c = 0; c < D; ++c) s = fmaf(Qs[lr * D + c], Ks[lane * (D + 1) + c], s);
+            const float s = dot_smem<D>(Qs + lr * D, Ks + lane * (D + 1));
             const bool valid = key < N && (!p.causal || key <= row);
-            const float x = valid ? s * c2 : -INFINITY;
-            const float mnew = fmaxf(m[rr], warp_max(x));
-            if (mnew == -INFINITY) continue;  // nothing visible yet (uniform across the warp)
-            const float alpha = ex2(m[rr] - mnew);
-            const float pr = ex2(x - mnew);
-            l[rr] = l[rr] * alpha + warp_sum(pr);
+            pr[rr] = valid ? s * c2 : -INFINITY;
+        }
+        // ... the online-softmax update of each row (rows with nothing visible yet keep their
+        // state: alpha = 1, weights 0) ...
+#pragma unroll
+        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+            const float mnew = fmaxf(m[rr], warp_max(pr[rr]));
+            if (mnew == -INFINITY) {
+                alpha[rr] = 1.0f;
+                pr[rr] = 0.0f;
+                continue;
+            }
+            alpha[rr] = ex2(m[rr] - mnew);
+            pr[rr] = ex2(pr[rr] - mnew);
+            l[rr] = l[rr] * alpha[rr] + warp_sum(pr[rr]);
             m[rr] = mnew;
+        }
+        // ... and O += P V for all rows at once (one V read per key serves every row)
 #pragma unroll
-            for (int t = 0; t < DL; ++t) o[rr][t] *= alpha;
+        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr)
+#pragma unroll
+            for (int t = 0; t < DL; ++t) o[rr][t] *= alpha[rr];
 #pragma unroll 4
-            for (int c = 0; c < kSimtTile; ++c) {
-                const float pc = __shfl_sync(0xffffffffu, pr, c);
+        for (int c = 0; c < kSimtTile; ++c) {
+            float vc[DL];
 #pragma unroll
-                for (int t = 0; t < DL; ++t) o[rr][t] = fmaf(pc, Vs[c * D + lane + 32 * t], o[rr][t]);
+            for (int t = 0; t < DL; ++t) vc[t] = Vs[c * D + lane + 32 * t];
+#pragma unroll
+            for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+                const float pc = __shfl_sync(0xffffffffu, pr[rr], c);
+#pragma unroll
+                for (int t = 0; t < DL; ++t) o[rr][t] = fmaf(pc, vc[t], o[rr][t]);
             }
         }
     }
@@ -201,8 +268,8 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_simt_kernel(const BwdParams p)
     const T* k = static_cast<const T*>(p.k) + hoff;
     const T* v = static_cast<const T*>(p.v) + hoff;
     const T* g = static_cast<const T*>(p.dout) + hoff;
-    stage_rows<T, D>(Qs, D, q, row_base, kSimtRows, N);
-    stage_rows<T, D>(Gs, D, g, row_base, kSimtRows, N);
+    stage_rows<T, D, kSimtRows>(Qs, D, q, row_base, N);
+    stage_rows<T, D, kSimtRows>(Gs, D, g, row_base, N);
     float L2[kSimtRowsPerWarp], Dl[kSimtRowsPerWarp], acc[kSimtRowsPerWarp][DL];
 #pragma unroll
     for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
@@ -218,8 +285,8 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_simt_kernel(const BwdParams p)
     const int n_tiles = p.causal ? (last_row / kSimtTile + 1) : (N + kSimtTile - 1) / kSimtTile;
     for (int kt = 0; kt < n_tiles; ++kt) {
         __syncthreads();
-        stage_rows<T, D>(Ks, D + 1, k, kt * kSimtTile, kSimtTile, N);
-        stage_rows<T, D>(Vs, D + 1, v, kt * kSimtTile, kSimtTile, N);
+        stage_rows<T, D, kSimtTile>(Ks, D + 1, k, kt * kSimtTile, N);
+        stage_rows<T, D, kSimtTile>(Vs, D + 1, v, kt * kSimtTile, N);
         __syncthreads();
         const int key = kt * kSimtTile + lane;
 #pragma unroll
@@ -276,8 +343,8 @@ __global__ void __launch_bounds__(128) fa_bwd_dkv_simt_kernel(const BwdParams p)
     const T* k = static_cast<const T*>(p.k) + hoff;
     const T* v = static_cast<const T*>(p.v) + hoff;
     const T* g = static_cast<const T*>(p.dout) + hoff;
-    stage_rows<T, D>(Kw, D, k, key_base, kSimtRows, N);
-    stage_rows<T, D>(Vw, D, v, key_base, kSimtRows, N);
+    stage_rows<T, D, kSimtRows>(Kw, D, k, key_base, N);
+    stage_rows<T, D, kSimtRows>(Vw, D, v, key_base, N);
     float dk[kSimtRowsPerWarp][DL], dv[kSimtRowsPerWarp][DL];
 #pragma unroll
     for (int rr = 0; rr < kSimtRowsPerWarp; ++rr)
@@ -288,8 +355,8 @@ __global__ void __launch_bounds__(128) fa_bwd_dkv_simt_kernel(const BwdParams p)
     const int n_tiles = (N + kSimtTile - 1) / kSimtTile;
     for (int it = first_tile; it < n_tiles; ++it) {
         __syncthreads();
-        stage_rows<T, D>(Qs, D + 1, q, it * kSimtTile, kSimtTile, N);
-        stage_rows<T, D>(Gs, D + 1, g, it * kSimtTile, kSimtTile, N);
+        stage_rows<T, D, kSimtTile>(Qs, D + 1, q, it * kSimtTile, N);
+        stage_rows<T, D, kSimtTile>(Gs, D + 1, g, it * kSimtTile, N);
         if (threadIdx.x < kSimtTile) {
             const int i = it * kSimtTile + threadIdx.x;
             Ls[threadIdx.x] = (i < N) ? p.lse2[static_cast<size_t>(bh) * N + i] : INFINITY;

@@ -30,6 +30,8 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--stage", type=int, default=-1)
     ap.add_argument("--time", action="store_true", help="report CUDA-event timing")
+    ap.add_argument("--dtype", choices=["bf16", "fp32"], default="bf16",
+                    help="fixed layout: fp32 runs the SIMT kernels")
     ap.add_argument("--Hkv", type=int, default=0,
                     help="packed layout with this many key/value heads (GQA); 0 = fixed layout")
     ap.add_argument("--Nq", type=int, default=0,
@@ -45,8 +47,8 @@ def main():
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     shape = (a.B, a.H, a.N, a.d)
-    q, k, v, do = (torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
-                   for _ in range(4))
+    dt = torch.float32 if a.dtype == "fp32" else torch.bfloat16
+    q, k, v, do = (torch.randn(shape, generator=g, device="cuda").to(dt) for _ in range(4))
     scale = a.d ** -0.5
     o = torch.empty_like(q)
     lse = torch.empty((a.B, a.H, a.N), device="cuda", dtype=torch.float32)
@@ -77,8 +79,8 @@ def main():
             print(f"bwd stage {a.stage} B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: "
                   f"{ms:.4f} ms")
             return
-        print(f"{a.which} B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: {ms:.4f} ms "
-              f"{fl / ms / 1e9:.1f} TFLOP/s")
+        print(f"{a.which} {a.dtype} B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: "
+              f"{ms:.4f} ms {fl / ms / 1e9:.1f} TFLOP/s")
         return
     if a.which == "fwd":
         for _ in range(a.iters):
