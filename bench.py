@@ -423,12 +423,19 @@ def cpu_baseline(target_s: float = 15.0) -> dict:
         if el > target_s / 4 or n_s >= 8192:
             break
         n_s *= 2
-    flops = (perfmodel.fwd_flops(1, heads, n_s, w.d, True) + perfmodel.bwd_flops(1, heads, n_s, w.d, True))
-    del np
+    # the timed sample: as many runs of that size as fill about target_s seconds
+    reps = max(1, int(np.ceil(target_s / el)))
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.attention_bwd(q, k, v, do, w.scale, w.causal, nthreads=cores)
+    el = time.perf_counter() - t
+    flops = reps * (perfmodel.fwd_flops(1, heads, n_s, w.d, True) +
+                    perfmodel.bwd_flops(1, heads, n_s, w.d, True))
     return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": round(el, 3),
-            "sample": f"fp64 oracle forward+backward of the first {n_s} tokens of {heads} heads "
-                      f"(causal prefix, d=128) of the workload; FLOPs by the causal convention"}
+            "sample": f"{reps} x fp64 oracle forward+backward of the first {n_s} tokens of {heads} "
+                      f"heads (causal prefix, d=128) of the workload; FLOPs by the causal "
+                      f"convention"}
 
 
 def run_reference(args):
