@@ -1,0 +1,80 @@
+"""Seeded random sweep over packed-batch problems: per case a random number of sequences with
+random query and key lengths (including empty, single-token and ragged ones, more keys than
+queries and the reverse), a random head grouping, d, mask and decode split count.  Every
+case runs the packed forward and backward and, where its shape allows, the split-KV decode,
+each checked against the fp64 oracle with the bf16 tolerances of the fixed-length tests."""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_25_gb300 as fa
+import oracle
+from exact_attention_25_gb300.inputs import random_varlen
+from tests.gpu_util import check_grads
+from tests.test_varlen_parity import check_fwd_with_empty_rows
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 48
+
+
+def draw_case(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 6))
+    Hkv = int(rng.choice([1, 2, 4]))
+    H = Hkv * int(rng.choice([1, 2, 3, 4]))
+    d = int(rng.choice([64, 128]))
+    causal = bool(rng.integers(0, 2))
+
+    def length(hi):
+        kind = rng.random()
+        if kind < 0.1:
+            return 0
+        if kind < 0.2:
+            return 1
+        return int(rng.integers(2, hi))
+
+    lens_k = [length(700) for _ in range(B)]
+    # queries: a chunk of the keys (chunked prefill), the same length, or longer
+    lens_q = []
+    for nk in lens_k:
+        mode = rng.random()
+        if mode < 0.4:
+            lens_q.append(int(rng.integers(0, nk + 1)))
+        elif mode < 0.8:
+            lens_q.append(nk)
+        else:
+            lens_q.append(nk + int(rng.integers(1, 200)))
+    if max(lens_q) == 0:
+        lens_q[0] = 1
+    if max(lens_k) == 0:
+        lens_k[0] = 1
+    splits = int(rng.integers(1, 9))
+    return lens_q, lens_k, H, Hkv, d, causal, splits
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_packed_problem(seed):
+    lens_q, lens_k, H, Hkv, d, causal, splits = draw_case(1000 + seed)
+    what = f"seed={seed} lens_q={lens_q} lens_k={lens_k} H={H} Hkv={Hkv} d={d} causal={causal}"
+    x = random_varlen(lens_q, lens_k, H, Hkv, d, seed=seed)
+    dev = {n: x[n].cuda() for n in ("q", "k", "v", "do", "cu_q", "cu_k")}
+    scale = d ** -0.5
+    o, lse = fa.forward_varlen(dev["q"], dev["k"], dev["v"], dev["cu_q"], dev["cu_k"], x["max_q"],
+                               x["max_k"], scale=scale, causal=causal)
+    dq, dk, dv = fa.backward_varlen(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, dev["cu_q"],
+                                    dev["cu_k"], x["max_q"], x["max_k"], scale=scale,
+                                    causal=causal)
+    fa.fa_device_status()
+    ref = oracle.attention_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], scale, causal,
+                                  do=x["do"])
+    check_fwd_with_empty_rows({"o": o, "lse": lse}, ref, what)
+    got = {"dq": dq, "dk": dk, "dv": dv}
+    if sum(lens_q) and sum(lens_k):
+        check_grads(got, ref, torch.bfloat16, what)
+    if x["max_q"] <= 128:  # the decode kernel takes up to 128 queries per sequence
+        od, lsed = fa.forward_decode(dev["q"], dev["k"], dev["v"], dev["cu_q"], dev["cu_k"],
+                                     x["max_q"], x["max_k"], scale=scale, causal=causal,
+                                     num_splits=splits)
+        fa.fa_device_status()
+        check_fwd_with_empty_rows({"o": od, "lse": lsed}, ref, what + f" decode splits={splits}")
