@@ -10,12 +10,20 @@
  * backward pass follows "Backward 구현" of "Triton 06: Flash Attention v2": Delta =
  * rowsum(dO o O), then dK, dV and dQ recomputed from the stored log-sum-exp.
  *
+ * Entry-point families.
+ *   - Fixed length (fa_fwd, fa_bwd and their variants): every tensor is contiguous row-major
+ *     [B, H, N, d]; lse is [B, H, N] float32; dtype FA_BF16 (bfloat16 tensors, fp32
+ *     accumulation, tensor cores) or FA_F32 (all fp32, SIMT kernels); B*H*N*d < 2^31.
+ *   - Packed (fa_fwd_varlen, fa_bwd_varlen, their _strided forms, fa_fwd_decode): sequences of
+ *     different lengths back to back, [total, heads, d], grouped key/value heads, bf16; their
+ *     conventions are stated with them below.
+ *
  * Conventions shared by every entry point.
- *   - Layout: every tensor is contiguous row-major [B, H, N, d]; lse is [B, H, N] float32.
- *   - dtype: FA_BF16 (bfloat16 q/k/v/o/dout/dq/dk/dv, fp32 accumulation) or FA_F32 (all fp32).
- *   - d (head dimension) is 64 or 128.  N >= 1, B >= 1, H >= 1, B*H*N*d < 2^31.
+ *   - d (head dimension) is 64 or 128; sizes are >= 1.
  *   - Causal mask: key index j <= query index i (top-left aligned, square), the condition
- *     offs_m >= offs_n of "개선 3" in "Triton 06: Flash Attention v2".
+ *     offs_m >= offs_n of "개선 3" in "Triton 06: Flash Attention v2"; the packed calls align
+ *     it to the bottom-right corner, which is the same mask when queries and keys are equal
+ *     in number.
  *   - lse receives, per query row, the natural log of sum_j exp(scale * q_i . k_j) over the
  *     visible keys (the base-2 value the kernels keep is converted, as that post describes).
  *   - Pointers are device pointers, 16-byte aligned.  The caller allocates and owns every
