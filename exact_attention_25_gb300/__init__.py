@@ -56,9 +56,23 @@ def _check_tensors(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _grouped(q, k) -> bool:
+    """True when k has fewer heads or another length than q (the fa_*_gqa entry points)."""
+    return tuple(k.shape[1:3]) != tuple(q.shape[1:3])
+
+
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None, impl: int = 0) -> None:
-    """C ``fa_fwd`` (``fa_fwd_impl`` when impl != 0): writes o and lse in place."""
+    """C ``fa_fwd`` (``fa_fwd_impl`` when impl != 0): writes o and lse in place.  With k and v
+    of shape [B, Hkv, Nk, d] other than q's [B, H, Nq, d] it calls ``fa_fwd_gqa``."""
     _check_tensors(q, k, v, o, lse)
+    if _grouped(q, k):
+        if impl:
+            raise ValueError("grouped heads and Nq != Nk run on the tensor-core path only")
+        B, H, Nq, d = _shape(q)
+        _, Hkv, Nk, _ = _shape(k)
+        check(load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk,
+                                d, float(scale), int(bool(causal)), _stream(stream)))
+        return
     B, H, N, d = _shape(q)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
             int(bool(causal)), _dtype_code(q))
@@ -75,10 +89,20 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspace,
            stream=None, impl: int = 0) -> None:
-    """C ``fa_bwd`` (``fa_bwd_impl`` when impl != 0): writes dq, dk, dv in place."""
+    """C ``fa_bwd`` (``fa_bwd_impl`` when impl != 0): writes dq, dk, dv in place; grouped or
+    non-square shapes call ``fa_bwd_gqa``."""
     _check_tensors(q, k, v, o, do, lse, dq, dk, dv, workspace)
-    B, H, N, d = _shape(q)
     nbytes = workspace.numel() * workspace.element_size()
+    if _grouped(q, k):
+        if impl:
+            raise ValueError("grouped heads and Nq != Nk run on the tensor-core path only")
+        B, H, Nq, d = _shape(q)
+        _, Hkv, Nk, _ = _shape(k)
+        check(load().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                _ptr(dk), _ptr(dv), B, H, Hkv, Nq, Nk, d, float(scale),
+                                int(bool(causal)), _ptr(workspace), nbytes, _stream(stream)))
+        return
+    B, H, N, d = _shape(q)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
             _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _ptr(workspace),
             nbytes)

@@ -25,7 +25,7 @@ EXPORTS = (
     "fa_device_status", "fa_set_wait_limit_ns", "fa_status_string", "fa_last_error",
     "fa_causal_block_counts", "fa_version", "fa_fwd_varlen", "fa_bwd_varlen_workspace_bytes",
     "fa_bwd_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
-    "fa_fwd_varlen_strided", "fa_bwd_varlen_strided",
+    "fa_fwd_varlen_strided", "fa_bwd_varlen_strided", "fa_fwd_gqa", "fa_bwd_gqa",
 )
 
 _lock = threading.Lock()
@@ -67,6 +67,9 @@ def load(path: str | None = None):
         lib.fa_bwd_varlen_workspace_bytes.restype = sz
         lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
                                       i, i, f, i, vp, sz, vp]
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp,
+                                   sz, vp]
         lib.fa_fwd_varlen_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
                                               i, i, f, i, vp]
         lib.fa_bwd_varlen_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i,
@@ -89,7 +92,8 @@ def load(path: str | None = None):
         lib.fa_version.restype = ctypes.c_char_p
         for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_bwd_stage", "fa_device_status",
                    "fa_causal_block_counts", "fa_fwd_varlen", "fa_bwd_varlen", "fa_fwd_decode",
-                   "fa_decode_num_splits", "fa_fwd_varlen_strided", "fa_bwd_varlen_strided"):
+                   "fa_decode_num_splits", "fa_fwd_varlen_strided", "fa_bwd_varlen_strided",
+                   "fa_fwd_gqa", "fa_bwd_gqa"):
             getattr(lib, fn).restype = ctypes.c_int
         if path is None:
             _lib = lib

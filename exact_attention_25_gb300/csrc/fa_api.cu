@@ -398,6 +398,112 @@ const char* fa_version(void) { return "fa-gb300 0.1 (sm_103a)"; }
 }  // extern "C"
 
 // ---------------------------------------------------------------------------------------
+// Fixed-length batches with grouped key/value heads and Nq != Nk (fa_fwd_gqa, fa_bwd_gqa).
+// ---------------------------------------------------------------------------------------
+namespace {
+
+int check_gqa(int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal)
+{
+    if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
+        return fail(FA_ERR_INVALID_ARG, "B, H, Hkv, Nq and Nk must be >= 1");
+    if (H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H must be a multiple of Hkv");
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED_D, "d must be 64 or 128");
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+        return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    if (static_cast<long long>(B) * H * Nq * d >= (1LL << 31) ||
+        static_cast<long long>(B) * Hkv * Nk * d >= (1LL << 31))
+        return fail(FA_ERR_TOO_LARGE, "B*H*Nq*d and B*Hkv*Nk*d must be < 2^31");
+    return FA_OK;
+}
+
+// [B, H, Nq, d] queries, [B, Hkv, Nk, d] keys and values, [B, H, Nq] statistics.
+fa::Layout gqa_layout(int B, int H, int Hkv, int Nq, int Nk, int d, Strides* st)
+{
+    for (int t = 0; t < 8; ++t) {
+        const bool kside = t == kK || t == kV || t == kDK || t == kDV;
+        st->rs[t] = d;
+        st->hs[t] = static_cast<long long>(kside ? Nk : Nq) * d;
+    }
+    fa::Layout L{};
+    L.cu_q = L.cu_k = nullptr;
+    L.B = B; L.H = H; L.Hkv = Hkv;
+    L.Nq = Nq; L.Nk = Nk;
+    L.Rq = Nq; L.Rk = Nk;
+    put_strides(L, *st);
+    return L;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                          void* stream)
+{
+    int rc = check_gqa(B, H, Hkv, Nq, Nk, d, scale, causal);
+    if (rc) return rc;
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    fa::FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.N = Nq; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    Strides st;
+    p.L = gqa_layout(B, H, Hkv, Nq, Nk, d, &st);
+    CUtensorMap maps[4];
+    if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d, st))) return rc;
+    cudaError_t e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return FA_OK;
+}
+
+extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                          void* workspace, size_t workspace_bytes, void* stream)
+{
+    int rc = check_gqa(B, H, Hkv, Nq, Nk, d, scale, causal);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+        return fail(FA_ERR_INVALID_ARG, "every tensor pointer must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA_ERR_MISALIGNED, "tensors must be 16-byte aligned (lse 4-byte)");
+    const size_t need = fa_bwd_workspace_bytes(B, H, Nq, d);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    fa::BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    const size_t rows = static_cast<size_t>(B) * H * Nq;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.delta = reinterpret_cast<float*>(ws);
+    p.lse2 = reinterpret_cast<float*>(ws + align256(rows * 4));
+    p.N = Nq; p.BH = B * H; p.scale = scale; p.scale_log2 = scale * fa::kLog2e;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    Strides st;
+    p.L = gqa_layout(B, H, Hkv, Nq, Nk, d, &st);
+    CUtensorMap maps[4];
+    if ((rc = make_maps(maps, q, k, v, dout, p.L, d, st))) return rc;
+    cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, cs, di->sms);
+    if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, cs);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return FA_OK;
+}
+
+// ---------------------------------------------------------------------------------------
 // Packed variable-length batches with grouped key/value heads (fa_fwd_varlen, fa_bwd_varlen).
 // ---------------------------------------------------------------------------------------
 namespace {

@@ -24,6 +24,8 @@
 // so the dV product starts as soon as phase 1 is done, and phase 1 of block i+1 overlaps
 // dK(i) and dP^T(i+1) on the pipe.  Q_i is read by S^T(i) and last by dK(i) (3-stage ring);
 // dO_i by dP^T(i) and last by dV(i) (2 stages).
+#include <type_traits>
+
 #include "fa_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -65,7 +67,7 @@ __device__ __forceinline__ void dkv_issue_acc(uint32_t acc, uint32_t buf, uint64
                  idesc, (first && ks == 0) ? 0u : 1u);
 }
 
-template <int D, bool PACKED>
+template <int D, int MODE>
 __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     fa_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -100,20 +102,21 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Layout& L = p.L;
-    constexpr bool packed = PACKED;  // tensors stored token by token
+    constexpr bool packed = mode_packed(MODE);  // tensors stored token by token
+    constexpr bool general = mode_general(MODE);  // grouped heads, Nq != Nk
     const int kblk_max = (L.Nk + 127) / 128;
     // Head-major order; within a head the first key blocks (most query blocks under the causal
     // mask) go first.
     const int bkv = static_cast<int>(blockIdx.x) / kblk_max;
     const int b = bkv / L.Hkv, hk = bkv % L.Hkv;
     const int kb = static_cast<int>(blockIdx.x) % kblk_max;
-    const SeqRows sr = seq_rows<PACKED>(L, b);
+    const SeqRows sr = seq_rows<packed>(L, b);
     const int nq = sr.nq, nk = sr.nk;
     const int k0 = kb * 128, k1 = min(nk, k0 + 128);
     if (k0 >= nk) return;  // beyond this sequence's keys (whole CTA, before any sync)
-    const int khead = k_head_index<PACKED>(L, b, hk);
-    const int G = PACKED ? L.H / L.Hkv : 1;  // query heads sharing this key/value head
-    const int shift = PACKED ? nk - nq : 0;  // bottom-right causal alignment
+    const int khead = k_head_index<packed>(L, b, hk);
+    const int G = general ? L.H / L.Hkv : 1;  // query heads sharing this key/value head
+    const int shift = general ? nk - nq : 0;  // bottom-right causal alignment
     const int nqblk = (nq + 127) / 128;
     int s_begin = 0;  // query blocks [s_begin, nqblk) see a key of [k0, k1)
     if (p.causal)
@@ -171,9 +174,9 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         }
         int issued_q = 0, issued_g = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int g = PACKED ? it / n_per : 0;
+            const int g = general ? it / n_per : 0;
             const int row = sr.q0 + (s_begin + it - g * n_per) * 128;
-            const int qhead = q_head_index<PACKED>(L, b, hk * G + g);
+            const int qhead = q_head_index<packed>(L, b, hk * G + g);
             // Q first: S^T(it) is issued before dP^T(it)
             const int sq = it % C::QSTAGES;
             if (!warp_wait_all(&bar_qempty[sq], ((it / C::QSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
@@ -283,10 +286,10 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         const uint64_t c2x2 = f2_make(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int g = PACKED ? it / n_per : 0;
+            const int g = general ? it / n_per : 0;
             const int q0 = (s_begin + it - g * n_per) * 128;  // first query of the block
             const size_t row_base =
-                static_cast<size_t>(q_head_index<PACKED>(L, b, hk * G + g)) * L.Rq + sr.q0;
+                static_cast<size_t>(q_head_index<packed>(L, b, hk * G + g)) * L.Rq + sr.q0;
             // stage -L2 and -Delta of this warpgroup's 64 query columns (negated, so the passes
             // below are fma / add only; queries beyond N get P = 0).  The first barrier keeps
             // the previous block's values until every thread of the warpgroup is done with them.
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     }
 }
 
-template <int D, bool PACKED>
+template <int D, int MODE>
 static cudaError_t launch_dkv(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                               const CUtensorMap& g, const BwdParams& p, cudaStream_t st)
 {
@@ -436,25 +439,29 @@ static cudaError_t launch_dkv(const CUtensorMap& k, const CUtensorMap& v, const 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkv_tc_kernel<D, PACKED>,
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkv_tc_kernel<D, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     dim3 grid(p.L.B * p.L.Hkv * ((p.L.Nk + 127) / 128));
-    fa_bwd_dkv_tc_kernel<D, PACKED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, q, g, p);
+    fa_bwd_dkv_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, q, g, p);
     return cudaGetLastError();
 }
 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
 cudaError_t launch_bwd_dkv_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
 {
-    if (p.L.cu_q != nullptr)
-        return d == 64 ? launch_dkv<64, true>(maps[1], maps[2], maps[0], maps[3], p, st)
-                       : launch_dkv<128, true>(maps[1], maps[2], maps[0], maps[3], p, st);
-    return d == 64 ? launch_dkv<64, false>(maps[1], maps[2], maps[0], maps[3], p, st)
-                   : launch_dkv<128, false>(maps[1], maps[2], maps[0], maps[3], p, st);
+    const int mode = layout_mode(p.L.cu_q, p.L.H, p.L.Hkv, p.L.Nq, p.L.Nk);
+    auto run = [&](auto dc) {
+        constexpr int Dc = decltype(dc)::value;
+        if (mode == kModePacked) return launch_dkv<Dc, kModePacked>(maps[1], maps[2], maps[0], maps[3], p, st);
+        if (mode == kModeFixedGroup)
+            return launch_dkv<Dc, kModeFixedGroup>(maps[1], maps[2], maps[0], maps[3], p, st);
+        return launch_dkv<Dc, kModeFixed>(maps[1], maps[2], maps[0], maps[3], p, st);
+    };
+    return d == 64 ? run(std::integral_constant<int, 64>{}) : run(std::integral_constant<int, 128>{});
 }
 
 }  // namespace fa

@@ -27,6 +27,8 @@
 // TMEM columns: S [0, 128), dP buffers [128, 256) and [256, 384), acc [384, 384 + d).
 // Within a dP buffer, warpgroup h's dS (32 columns of bf16 pairs) lands at [64h, 64h + 32),
 // the first half of the columns it loaded itself.
+#include <type_traits>
+
 #include "fa_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -57,7 +59,7 @@ __device__ __forceinline__ void dq_issue_nt(uint32_t d_tmem, uint64_t adesc, uin
     }
 }
 
-template <int D, bool PACKED>
+template <int D, int MODE>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_g,
@@ -94,20 +96,21 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Layout& L = p.L;
-    constexpr bool packed = PACKED;  // tensors stored token by token
+    constexpr bool packed = mode_packed(MODE);  // tensors stored token by token
+    constexpr bool general = mode_general(MODE);  // grouped heads, Nq != Nk
     const int qblk_max = (L.Nq + 127) / 128;
     // Head-major order; within a head the last query blocks (most key blocks under the causal
     // mask) go first.
     const int bhead = static_cast<int>(blockIdx.x) / qblk_max;
     const int b = bhead / L.H, h_q = bhead % L.H;
     const int qb = qblk_max - 1 - static_cast<int>(blockIdx.x) % qblk_max;
-    const SeqRows sr = seq_rows<PACKED>(L, b);
+    const SeqRows sr = seq_rows<packed>(L, b);
     const int nq = sr.nq, nk = sr.nk;
     const int q0 = qb * 128, q1 = min(nq, q0 + 128);
     if (q0 >= nq) return;  // beyond this sequence's queries (whole CTA, before any sync)
-    const int qhead = q_head_index<PACKED>(L, b, h_q);
-    const int khead = k_head_index<PACKED>(L, b, PACKED ? h_q / (L.H / L.Hkv) : h_q);
-    const int shift = PACKED ? nk - nq : 0;  // bottom-right causal alignment
+    const int qhead = q_head_index<packed>(L, b, h_q);
+    const int khead = k_head_index<packed>(L, b, general ? h_q / (L.H / L.Hkv) : h_q);
+    const int shift = general ? nk - nq : 0;  // bottom-right causal alignment
     // key blocks [0, n_it) are seen by some query of [q0, q1)
     int n_it = (nk + 127) / 128;
     if (p.causal) {
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
 }
 
-template <int D, bool PACKED>
+template <int D, int MODE>
 static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const CUtensorMap& k,
                              const CUtensorMap& v, const BwdParams& p, cudaStream_t st)
 {
@@ -419,25 +422,29 @@ static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const C
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_tc_kernel<D, PACKED>,
+        cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_tc_kernel<D, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     dim3 grid(p.L.B * p.L.H * ((p.L.Nq + 127) / 128));
-    fa_bwd_dq_tc_kernel<D, PACKED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(q, g, k, v, p);
+    fa_bwd_dq_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(q, g, k, v, p);
     return cudaGetLastError();
 }
 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
 cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
 {
-    if (p.L.cu_q != nullptr)
-        return d == 64 ? launch_dq<64, true>(maps[0], maps[3], maps[1], maps[2], p, st)
-                       : launch_dq<128, true>(maps[0], maps[3], maps[1], maps[2], p, st);
-    return d == 64 ? launch_dq<64, false>(maps[0], maps[3], maps[1], maps[2], p, st)
-                   : launch_dq<128, false>(maps[0], maps[3], maps[1], maps[2], p, st);
+    const int mode = layout_mode(p.L.cu_q, p.L.H, p.L.Hkv, p.L.Nq, p.L.Nk);
+    auto run = [&](auto dc) {
+        constexpr int Dc = decltype(dc)::value;
+        if (mode == kModePacked) return launch_dq<Dc, kModePacked>(maps[0], maps[3], maps[1], maps[2], p, st);
+        if (mode == kModeFixedGroup)
+            return launch_dq<Dc, kModeFixedGroup>(maps[0], maps[3], maps[1], maps[2], p, st);
+        return launch_dq<Dc, kModeFixed>(maps[0], maps[3], maps[1], maps[2], p, st);
+    };
+    return d == 64 ? run(std::integral_constant<int, 64>{}) : run(std::integral_constant<int, 128>{});
 }
 
 }  // namespace fa

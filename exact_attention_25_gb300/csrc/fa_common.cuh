@@ -60,9 +60,21 @@ __host__ __device__ inline int causal_tile_class(int q0, int q1, int k0, int k1)
 //                 back to back ("variable length", cu_q / cu_k = B+1 sequence starts): head
 //                 index h (or hk), row offset cu[b].
 // Per-row statistics (lse, Delta, base-2 LSE) are [head index][Rq].  Query head h reads key /
-// value head h / (H / Hkv) (grouped-query attention; Hkv = H is ordinary multi-head).  The
-// fixed-length layout is always square with Hkv = H: kernels compiled for it (PACKED = false)
-// take Nq == Nk and one query head per key/value head as given.
+// value head h / (H / Hkv) (grouped-query attention; Hkv = H is ordinary multi-head).
+//
+// Every tensor-core kernel is compiled for three modes: the fixed-length layout with Nq == Nk
+// and Hkv == H (kModeFixed, which skips the group loop and the causal shift), the fixed-length
+// layout with grouped heads and Nq != Nk allowed (kModeFixedGroup), and the packed layout
+// (kModePacked).
+enum LayoutMode : int { kModeFixed = 0, kModeFixedGroup = 1, kModePacked = 2 };
+
+__host__ __device__ constexpr bool mode_packed(int mode) { return mode == kModePacked; }
+__host__ __device__ constexpr bool mode_general(int mode) { return mode != kModeFixed; }
+inline int layout_mode(const void* cu_q, int H, int Hkv, int Nq, int Nk)
+{
+    if (cu_q != nullptr) return kModePacked;
+    return (H != Hkv || Nq != Nk) ? kModeFixedGroup : kModeFixed;
+}
 struct Layout {
     const int* cu_q;       // packed layout: B+1 query-row starts (device), else null
     const int* cu_k;       // packed layout: B+1 key-row starts (device), else null

@@ -15,6 +15,8 @@
 // of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised); at d = 64, O_t at
 // [256 + 128t, 384 + 128t), whose column 64 accumulates the row sum of the bf16 P (the P V
 // product runs at N = 128 against V and a constant ones-column panel).
+#include <type_traits>
+
 #include "fa_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -67,7 +69,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
         mma_ts_w(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc, ks > 0 ? 1u : acc_first);
 }
 
-template <int D, bool PACKED>
+template <int D, int MODE>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -97,7 +99,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Layout& L = p.L;
-    constexpr bool packed = PACKED;  // tensors stored token by token
+    constexpr bool packed = mode_packed(MODE);  // tensors stored token by token
+    constexpr bool general = mode_general(MODE);  // grouped heads, Nq != Nk
     const int n_pairs = ((L.Nq + C::BM - 1) / C::BM + C::NT - 1) / C::NT;
     // Head-major order, so the CTAs resident at one time share one or two heads' K/V in L2
     // (with grouped heads, the heads of a group share one K/V); within a head the heaviest
@@ -105,16 +108,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int bhead = static_cast<int>(blockIdx.x) / n_pairs;
     const int b = bhead / L.H, h = bhead % L.H;
     const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) % n_pairs;
-    const SeqRows sr = seq_rows<PACKED>(L, b);
+    const SeqRows sr = seq_rows<packed>(L, b);
     const int nq = sr.nq, nk = sr.nk;
     const int n_qtiles = (nq + C::BM - 1) / C::BM;
     const int n_kblocks = (nk + C::BN - 1) / C::BN;
     const int qt0 = pair * C::NT;
     if (qt0 >= n_qtiles) return;  // beyond this sequence's queries (whole CTA, before any sync)
     const int nt = min(C::NT, n_qtiles - qt0);
-    const int qhead = q_head_index<PACKED>(L, b, h);
-    const int khead = k_head_index<PACKED>(L, b, PACKED ? h / (L.H / L.Hkv) : h);
-    const int shift = PACKED ? nk - nq : 0;  // bottom-right causal alignment
+    const int qhead = q_head_index<packed>(L, b, h);
+    const int khead = k_head_index<packed>(L, b, general ? h / (L.H / L.Hkv) : h);
+    const int shift = general ? nk - nq : 0;  // bottom-right causal alignment
 
     // Key blocks visited by each query tile: a prefix 0..J_t-1 (under the causal mask, the
     // blocks whose first key some query of the tile sees).
@@ -470,8 +473,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // ------------------------------------------------------------- epilogue
         // Where this row goes, re-derived here rather than held in registers across the loop.
         const int eb = static_cast<int>(blockIdx.x) / n_pairs;
-        const SeqRows se = seq_rows<PACKED>(L, eb / L.H);
-        const int eqhead = q_head_index<PACKED>(L, eb / L.H, eb % L.H);
+        const SeqRows se = seq_rows<packed>(L, eb / L.H);
+        const int eqhead = q_head_index<packed>(L, eb / L.H, eb % L.H);
         const size_t orow_off = static_cast<size_t>(se.q0 + qrow) * L.o_rs +
                                 static_cast<size_t>(eqhead) * L.o_hs;
         const size_t lse_off = static_cast<size_t>(eqhead) * L.Rq + se.q0 + qrow;
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
 }
 
-template <int D, bool PACKED>
+template <int D, int MODE>
 static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                       const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
 {
@@ -534,7 +537,7 @@ static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, PACKED>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -543,19 +546,21 @@ static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& 
     const int n_qtiles = (p.L.Nq + C::BM - 1) / C::BM;
     const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
     dim3 grid(p.L.B * p.L.H * n_pairs);
-    fa_fwd_tc_kernel<D, PACKED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
+    fa_fwd_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
 {
-    const bool packed = p.L.cu_q != nullptr;
-    if (d == 64)
-        return packed ? launch_fwd_tc_impl<64, true>(tq, tk, tv, p, st)
-                      : launch_fwd_tc_impl<64, false>(tq, tk, tv, p, st);
-    return packed ? launch_fwd_tc_impl<128, true>(tq, tk, tv, p, st)
-                  : launch_fwd_tc_impl<128, false>(tq, tk, tv, p, st);
+    const int mode = layout_mode(p.L.cu_q, p.L.H, p.L.Hkv, p.L.Nq, p.L.Nk);
+    auto run = [&](auto dc) {
+        constexpr int Dc = decltype(dc)::value;
+        if (mode == kModePacked) return launch_fwd_tc_impl<Dc, kModePacked>(tq, tk, tv, p, st);
+        if (mode == kModeFixedGroup) return launch_fwd_tc_impl<Dc, kModeFixedGroup>(tq, tk, tv, p, st);
+        return launch_fwd_tc_impl<Dc, kModeFixed>(tq, tk, tv, p, st);
+    };
+    return d == 64 ? run(std::integral_constant<int, 64>{}) : run(std::integral_constant<int, 128>{});
 }
 
 }  // namespace fa

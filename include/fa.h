@@ -98,6 +98,22 @@ int fa_bwd_impl(const void* q, const void* k, const void* v, const void* o, cons
                 float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
                 int impl, void* stream);
 
+/* Fixed-length batches with grouped key/value heads and possibly different query and key
+ * lengths (bf16, tensor-core path): q, o, dout, dq are [B, H, Nq, d], k, v, dk, dv are
+ * [B, Hkv, Nk, d], lse is [B, H, Nq] fp32, all contiguous.  Query head h reads key/value head
+ * h / (H / Hkv) and the causal mask is aligned to the bottom-right corner (query i sees key
+ * j iff j <= i + Nk - Nq), as for fa_fwd_varlen; rows that see no key get O = 0, lse = -inf.
+ * H % Hkv == 0; B*H*Nq*d and B*Hkv*Nk*d < 2^31.  The backward's workspace is
+ * fa_bwd_workspace_bytes(B, H, Nq, d); dk and dv of a shared head sum over its group.
+ * Ownership, alignment, streams and errors as fa_fwd / fa_bwd. */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream);
+
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+               const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+               int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+               void* stream);
+
 /* Packed variable-length batches with grouped key/value heads (bf16, tensor-core path).
  *
  * What it computes.  B independent sequences; sequence b has the query rows

@@ -218,3 +218,22 @@ def test_strided_varlen_rejects_bad_strides(lib):
     assert fwd_st(bad) == -1
     bad = list(good); bad[5] = 0
     assert fwd_st(bad) == -3
+
+
+def test_grouped_fixed_length_rejects_bad_arguments(lib):
+    def call(B=1, H=4, Hkv=2, Nq=10, Nk=20, d=128, q=A):
+        return lib.fa_fwd_gqa(q, A, A, A2, A2, B, H, Hkv, Nq, Nk, d, ctypes.c_float(0.1), 1, None)
+
+    assert call(H=4, Hkv=3) == -1
+    assert call(Nk=0) == -1
+    assert call(d=96) == -2
+    assert call(q=MIS) == -3
+    assert call(B=1024, H=1024, Nq=1024, d=128) == -7
+
+    def bcall(ws=A, nbytes=None):
+        nb = lib.fa_bwd_workspace_bytes(1, 4, 10, 128) if nbytes is None else nbytes
+        return lib.fa_bwd_gqa(A, A, A, A, A, A, A2, A2, A2, 1, 4, 2, 10, 20, 128,
+                              ctypes.c_float(0.1), 1, ws, nb, None)
+
+    assert bcall(ws=None) == -4
+    assert bcall(nbytes=16) == -4
