@@ -3,6 +3,8 @@ random query and key lengths (including empty, single-token and ragged ones, mor
 queries and the reverse), a random head grouping, d, mask and decode split count.  Every
 case runs the packed forward and backward and, where its shape allows, the split-KV decode,
 each checked against the fp64 oracle with the bf16 tolerances of the fixed-length tests."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +17,9 @@ from tests.test_varlen_parity import check_fwd_with_empty_rows
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 48
+# FA_SWEEP_CASES / FA_SWEEP_FIXED_CASES widen the sweep for a longer stress run
+N_CASES = int(os.environ.get("FA_SWEEP_CASES", "48"))
+N_FIXED_CASES = int(os.environ.get("FA_SWEEP_FIXED_CASES", "16"))
 
 
 def draw_case(seed):
@@ -80,7 +84,7 @@ def test_random_packed_problem(seed):
         check_fwd_with_empty_rows({"o": od, "lse": lsed}, ref, what + f" decode splits={splits}")
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(N_FIXED_CASES))
 def test_random_fixed_length_problem(seed):
     """Fixed-length [B, H, N, d] calls with random sizes, masks and scales (including
     non-standard ones), against the oracle.  Inputs stay at most N(0,1) in magnitude: the
