@@ -17,7 +17,7 @@ __all__ = [
     "fa_device_status", "fa_set_wait_limit_ns", "fa_causal_block_counts", "forward", "backward",
     "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "forward_varlen",
     "backward_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
-    "forward_decode",
+    "forward_decode", "fa_checked_build",
 ]
 
 
@@ -132,6 +132,11 @@ def fa_device_status(stream=None) -> None:
 
 def fa_set_wait_limit_ns(ns: int) -> None:
     load().fa_set_wait_limit_ns(int(ns))
+
+
+def fa_checked_build() -> bool:
+    """C ``fa_checked_build``: whether the library in use is the bounds-checked variant."""
+    return bool(load().fa_checked_build())
 
 
 def fa_causal_block_counts(q_block: int, Br: int, Bc: int, N: int) -> tuple[int, int]:

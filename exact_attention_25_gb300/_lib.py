@@ -5,18 +5,20 @@ and streams); shapes are [B, H, N, d] (or, for the variable-length calls, packed
 is no fallback implementation."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa.so")
+LIB_CHECKED_PATH = os.path.join(PKG, "libfa_checked.so")
 
 FA_BF16, FA_F32 = 0, 1
 STATUS = {
     0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED_D", -3: "FA_ERR_MISALIGNED",
     -4: "FA_ERR_WORKSPACE", -5: "FA_ERR_LAUNCH", -6: "FA_ERR_DEVICE_TIMEOUT",
-    -7: "FA_ERR_TOO_LARGE", -8: "FA_ERR_UNSUPPORTED_DEVICE",
+    -7: "FA_ERR_TOO_LARGE", -8: "FA_ERR_UNSUPPORTED_DEVICE", -9: "FA_ERR_OUT_OF_BOUNDS",
 }
 # Every symbol include/fa.h declares (tests check the library exports all of them).
 EXPORTS = (
@@ -26,6 +28,7 @@ EXPORTS = (
     "fa_causal_block_counts", "fa_version", "fa_fwd_varlen", "fa_bwd_varlen_workspace_bytes",
     "fa_bwd_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
     "fa_fwd_varlen_strided", "fa_bwd_varlen_strided", "fa_fwd_gqa", "fa_bwd_gqa",
+    "fa_checked_build",
 )
 
 _lock = threading.Lock()
@@ -90,14 +93,30 @@ def load(path: str | None = None):
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_causal_block_counts.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
         lib.fa_version.restype = ctypes.c_char_p
+        lib.fa_checked_build.argtypes = []
         for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_bwd_stage", "fa_device_status",
                    "fa_causal_block_counts", "fa_fwd_varlen", "fa_bwd_varlen", "fa_fwd_decode",
                    "fa_decode_num_splits", "fa_fwd_varlen_strided", "fa_bwd_varlen_strided",
-                   "fa_fwd_gqa", "fa_bwd_gqa"):
+                   "fa_fwd_gqa", "fa_bwd_gqa", "fa_checked_build"):
             getattr(lib, fn).restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
+
+
+@contextlib.contextmanager
+def library(path: str):
+    """Route every binding call to the library at ``path`` (for example the checked build)
+    inside the ``with`` block; the library in use before is restored on exit."""
+    global _lib
+    lib = load(path)
+    with _lock:
+        prev, _lib = _lib, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
 
 
 def check(rc: int) -> None:

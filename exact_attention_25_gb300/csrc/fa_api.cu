@@ -146,13 +146,30 @@ struct Strides {
 enum { kQ = 0, kK, kV, kO, kDO, kDQ, kDK, kDV };
 
 // The strides the kernels address directly go into the layout; q, k, v, dout go into maps.
-void put_strides(fa::Layout& L, const Strides& st)
+// Also sets the element extents that checked builds test accesses against: the smallest
+// buffer holding every row of every head index at those strides (R rows of each head index;
+// the fixed-length layout's head index runs over B*H, the packed one's over H).  The layout's
+// sizes (cu_q, B, H, Hkv, Rq, Rk) must be set first.
+void put_strides(fa::Layout& L, const Strides& st, int d)
 {
     L.o_rs = st.rs[kO]; L.o_hs = st.hs[kO];
     L.do_rs = st.rs[kDO]; L.do_hs = st.hs[kDO];
     L.dq_rs = st.rs[kDQ]; L.dq_hs = st.hs[kDQ];
     L.dk_rs = st.rs[kDK]; L.dk_hs = st.hs[kDK];
     L.dv_rs = st.rs[kDV]; L.dv_hs = st.hs[kDV];
+    const long long bq = L.cu_q ? 1 : L.B;
+    const long long hq = bq * L.H, hk = bq * L.Hkv;
+    // the watchdog test hook's companion: every extent one row short
+    const long long cut = (g_debug_flags & fa::kDebugShrinkExtents) ? 1 : 0;
+    auto ext = [&](int t, long long heads, long long rows) {
+        return rows < 1 ? 0 : (rows - 1) * st.rs[t] + (heads - 1) * st.hs[t] + d - cut * st.rs[t];
+    };
+    L.o_ext = ext(kO, hq, L.Rq);
+    L.do_ext = ext(kDO, hq, L.Rq);
+    L.dq_ext = ext(kDQ, hq, L.Rq);
+    L.dk_ext = ext(kDK, hk, L.Rk);
+    L.dv_ext = ext(kDV, hk, L.Rk);
+    L.stat_ext = hq * L.Rq - cut;
 }
 
 // Fixed-length entry points: [B, H, N, d] for every tensor, [B, H, N] statistics.
@@ -173,7 +190,7 @@ fa::Layout fixed_layout(int B, int H, int N, int d)
     L.B = B; L.H = H; L.Hkv = H;
     L.Nq = L.Nk = N;
     L.Rq = L.Rk = N;
-    put_strides(L, fixed_strides(N, d));
+    put_strides(L, fixed_strides(N, d), d);
     return L;
 }
 
@@ -347,6 +364,8 @@ int fa_device_status(void* stream)
     const int zero = 0;
     if ((e = cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
         return cuda_fail(e, "clearing the status word");
+    if (word == fa::kStatusOutOfBounds)
+        return fail(FA_ERR_OUT_OF_BOUNDS, "a bounds check failed; the access was skipped");
     return fail(FA_ERR_DEVICE_TIMEOUT, "bounded device wait expired at site " + std::to_string(word));
 }
 
@@ -356,6 +375,15 @@ void fa_set_wait_limit_ns(unsigned long long ns)
 }
 
 void fa_debug_set_flags(int flags) { g_debug_flags = flags; }
+
+int fa_checked_build(void)
+{
+#ifdef FA_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 const char* fa_status_string(int code)
 {
@@ -369,6 +397,7 @@ const char* fa_status_string(int code)
         case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
         case FA_ERR_TOO_LARGE: return "FA_ERR_TOO_LARGE";
         case FA_ERR_UNSUPPORTED_DEVICE: return "FA_ERR_UNSUPPORTED_DEVICE";
+        case FA_ERR_OUT_OF_BOUNDS: return "FA_ERR_OUT_OF_BOUNDS";
         default: return "FA_ERR_UNKNOWN";
     }
 }
@@ -430,7 +459,7 @@ fa::Layout gqa_layout(int B, int H, int Hkv, int Nq, int Nk, int d, Strides* st)
     L.B = B; L.H = H; L.Hkv = Hkv;
     L.Nq = Nq; L.Nk = Nk;
     L.Rq = Nq; L.Rk = Nk;
-    put_strides(L, *st);
+    put_strides(L, *st, d);
     return L;
 }
 
@@ -574,7 +603,7 @@ fa::Layout packed_layout(const int* cu_q, const int* cu_k, int B, int max_q, int
     L.B = B; L.H = H; L.Hkv = Hkv;
     L.Nq = max_q; L.Nk = max_k;
     L.Rq = total_q; L.Rk = total_k;
-    put_strides(L, st);
+    put_strides(L, st, d);
     return L;
 }
 
@@ -804,6 +833,9 @@ extern "C" int fa_fwd_decode(const void* q, const void* k, const void* v, void* 
     p.splits = num_splits; p.G = G; p.head_chunks = group / G; p.q_box = max_seqlen_q;
     p.scale_log2 = scale * fa::kLog2e; p.causal = causal;
     p.status = di->status; p.wait_limit_ns = g_wait_limit_ns; p.debug_flags = g_debug_flags;
+    p.part_ext = need > 0 ? static_cast<long long>(num_splits) * total_q * H * d -
+                                ((g_debug_flags & fa::kDebugShrinkExtents) ? d : 0)
+                          : 0;
     const Strides st = packed_strides(H, Hkv, d);
     p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, total_q,
                         total_k, H, Hkv, d, st);

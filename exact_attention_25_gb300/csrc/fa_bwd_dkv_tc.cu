@@ -296,8 +296,9 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             named_bar_sync(1 + h, 128);
             if (r < 64) {
                 const int qi = q0 + 64 * h + r;
-                sL2[h][r] = (qi < nq) ? -p.lse2[row_base + qi] : -INFINITY;
-                sDl[h][r] = (qi < nq) ? -p.delta[row_base + qi] : 0.0f;
+                const bool in = qi < nq && in_extent(row_base + qi, 1, L.stat_ext, p.status);
+                sL2[h][r] = in ? -p.lse2[row_base + qi] : -INFINITY;
+                sDl[h][r] = in ? -p.delta[row_base + qi] : 0.0f;
             }
             named_bar_sync(1 + h, 128);
             const bool diag = p.causal && causal_class_shifted(q0, min(nq, q0 + 128), k0, k1,
@@ -385,9 +386,11 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
                 const float mul = which == 0 ? 1.0f : p.scale;
                 const long long rs = which == 0 ? L.dv_rs : L.dk_rs;
                 const long long hs = which == 0 ? L.dv_hs : L.dk_hs;
-                __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) +
-                                         static_cast<size_t>(sr.k0 + krow) * rs +
-                                         static_cast<size_t>(khead) * hs;
+                const size_t off = static_cast<size_t>(sr.k0 + krow) * rs +
+                                   static_cast<size_t>(khead) * hs;
+                __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + off;
+                const bool in = krow >= nk ||
+                                in_extent(off, D, which == 0 ? L.dv_ext : L.dk_ext, p.status);
 #pragma unroll 1
                 for (int ch = 0; ch < D / 64; ++ch) {
                     const int c0 = h * (D / 2) + 32 * ch;
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
                     for (int c = 0; c < 16; ++c)
                         packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
                                                 __uint_as_float(a[2 * c + 1]) * mul);
-                    if (krow < nk) {
+                    if (krow < nk && in) {
                         uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -415,9 +418,11 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
                                 static_cast<size_t>(khead) * L.dk_hs;
             const size_t offv = static_cast<size_t>(sr.k0 + krow) * L.dv_rs +
                                 static_cast<size_t>(khead) * L.dv_hs;
+            const bool ink = in_extent(offk, D, L.dk_ext, p.status);
+            const bool inv = in_extent(offv, D, L.dv_ext, p.status);
             for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c) {
-                static_cast<__nv_bfloat16*>(p.dk)[offk + c] = __float2bfloat16_rn(0.0f);
-                static_cast<__nv_bfloat16*>(p.dv)[offv + c] = __float2bfloat16_rn(0.0f);
+                if (ink) static_cast<__nv_bfloat16*>(p.dk)[offk + c] = __float2bfloat16_rn(0.0f);
+                if (inv) static_cast<__nv_bfloat16*>(p.dv)[offv + c] = __float2bfloat16_rn(0.0f);
             }
         }
         tc_fence_before();

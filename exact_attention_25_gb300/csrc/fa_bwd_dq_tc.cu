@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const size_t row_base = static_cast<size_t>(qhead) * L.Rq + sr.q0;
         const int qrow = q0 + r;  // row within the sequence
         float nL2 = 0.0f, nDl = 0.0f;  // -L2 and -Delta of this thread's query row
-        if (qrow < nq) {
+        if (qrow < nq && in_extent(row_base + qrow, 1, L.stat_ext, p.status)) {
             nL2 = -p.lse2[row_base + qrow];
             nDl = -p.delta[row_base + qrow];
         }
@@ -372,9 +372,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
         if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
             tc_fence_after();
-            __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) +
-                                     static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
-                                     static_cast<size_t>(qhead) * L.dq_hs;
+            const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
+                               static_cast<size_t>(qhead) * L.dq_hs;
+            __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) + off;
+            const bool in = qrow >= nq || in_extent(off, D, L.dq_ext, p.status);
 #pragma unroll 1
             for (int ch = 0; ch < D / 64; ++ch) {
                 const int c0 = h * (D / 2) + 32 * ch;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                 for (int c = 0; c < 16; ++c)
                     packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale,
                                             __uint_as_float(a[2 * c + 1]) * p.scale);
-                if (qrow < nq) {
+                if (qrow < nq && in) {
                     uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -400,8 +401,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             // gradient
             const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
                                static_cast<size_t>(qhead) * L.dq_hs;
-            for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c)
-                static_cast<__nv_bfloat16*>(p.dq)[off + c] = __float2bfloat16_rn(0.0f);
+            if (in_extent(off, D, L.dq_ext, p.status))
+                for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c)
+                    static_cast<__nv_bfloat16*>(p.dq)[off + c] = __float2bfloat16_rn(0.0f);
         }
         tc_fence_before();
     }

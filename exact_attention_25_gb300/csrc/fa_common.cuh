@@ -37,6 +37,29 @@ enum WaitSite : int {
 // the copy, so the barrier guarding that tile never completes and every bounded wait on it
 // must expire (watchdog test).  Never set in normal operation.
 constexpr int kDebugDropFirstLoad = 1;
+// Test hook of checked builds: the host passes every buffer extent one row short, so the
+// bounds checks must catch (and skip) the last row's accesses.
+constexpr int kDebugShrinkExtents = 2;
+
+// Status word value of a failed bounds check (checked builds); wait sites are below 64.
+constexpr int kStatusOutOfBounds = 0x0B0B;
+
+// Checked builds (-DFA_CHECKED) verify every direct global access of n elements at element
+// offset off against the extent of its buffer; a violation is recorded in the status word
+// and the access is skipped.  Regular builds compile the check away.
+#ifdef FA_CHECKED
+__device__ __forceinline__ bool in_extent(long long off, long long n, long long extent, int* status)
+{
+    if (off >= 0 && off + n <= extent) return true;
+    atomicCAS(status, 0, kStatusOutOfBounds);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_extent(long long, long long, long long, int*)
+{
+    return true;
+}
+#endif
 
 // Causal mask (key index <= query index, top-left aligned): classification of the key
 // block [k0, k1) against the query block [q0, q1), following the two-stage split of the
@@ -88,6 +111,9 @@ struct Layout {
     long long dq_rs, dq_hs;
     long long dk_rs, dk_hs;
     long long dv_rs, dv_hs;
+    // Element extents of those buffers and of the per-row statistics (lse, Delta, base-2
+    // LSE), checked in checked builds only.
+    long long o_ext, do_ext, dq_ext, dk_ext, dv_ext, stat_ext;
 };
 
 // Rows of sequence b: global row offsets q0 / k0 and lengths nq / nk.  Packed offsets and

@@ -30,6 +30,7 @@ struct DecodeParams {
     int* status;
     unsigned long long wait_limit_ns;
     int debug_flags;
+    long long part_ext;  // elements of o_part (checked builds)
     Layout L;
 };
 

@@ -376,6 +376,15 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         const int h = h0 + g;
         const float inv_l = lr > 0.0f ? 1.0f / lr : 0.0f;
         const float lse_row = (have && l > 0.0f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        const size_t o_off = t * L.o_rs + static_cast<size_t>(h) * L.o_hs;
+        const size_t part_off = ((static_cast<size_t>(split) * L.Rq + t) * L.H + h) * D;
+        const size_t lse_off = static_cast<size_t>(h) * L.Rq + t;
+        const size_t lsep_off = (static_cast<size_t>(split) * L.H + h) * L.Rq + t;
+        const bool o_in = !valid || (p.splits == 1 ? in_extent(o_off, D, L.o_ext, p.status)
+                                                   : in_extent(part_off, D, p.part_ext, p.status));
+        const bool lse_in = !valid || (p.splits == 1
+                                           ? p.lse == nullptr || in_extent(lse_off, 1, L.stat_ext, p.status)
+                                           : in_extent(lsep_off, 1, p.part_ext / D, p.status));
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
@@ -387,23 +396,20 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) o[c] = 0u;
             }
-            if (!valid) continue;
+            if (!valid || !o_in) continue;
             if (p.splits == 1) {
                 uint32_t packed[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c)
                     packed[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
                                             __uint_as_float(o[2 * c + 1]) * inv_l);
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                                      t * L.o_rs + static_cast<size_t>(h) * L.o_hs +
-                                                      32 * ch);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o_off + 32 * ch);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
                                         packed[4 * c + 3]);
             } else {
-                float4* dst = reinterpret_cast<float4*>(
-                    p.o_part + ((static_cast<size_t>(split) * L.Rq + t) * L.H + h) * D + 32 * ch);
+                float4* dst = reinterpret_cast<float4*>(p.o_part + part_off + 32 * ch);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l,
@@ -412,11 +418,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                                          __uint_as_float(o[4 * c + 3]) * inv_l);
             }
         }
-        if (valid) {
+        if (valid && lse_in) {
             if (p.splits == 1) {
-                if (p.lse != nullptr) p.lse[static_cast<size_t>(h) * L.Rq + t] = lse_row;
+                if (p.lse != nullptr) p.lse[lse_off] = lse_row;
             } else {
-                p.lse_part[(static_cast<size_t>(split) * L.H + h) * L.Rq + t] = lse_row;
+                p.lse_part[lsep_off] = lse_row;
             }
         }
         tc_fence_before();
@@ -476,8 +482,9 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodePara
             }
         }
         const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + t * L.o_rs +
-                             static_cast<size_t>(h) * L.o_hs + lane * EPL;
+        const size_t o_off = t * L.o_rs + static_cast<size_t>(h) * L.o_hs;
+        if (!in_extent(o_off, D, L.o_ext, p.status)) continue;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + o_off + lane * EPL;
         if constexpr (EPL == 4) {
             *reinterpret_cast<uint2*>(dst) =
                 make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));

@@ -478,6 +478,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const size_t orow_off = static_cast<size_t>(se.q0 + qrow) * L.o_rs +
                                 static_cast<size_t>(eqhead) * L.o_hs;
         const size_t lse_off = static_cast<size_t>(eqhead) * L.Rq + se.q0 + qrow;
+        const bool live = t < nt && qrow < se.nq;
+        const bool o_in = !live || in_extent(orow_off, D, L.o_ext, p.status);
+        const bool lse_in = !live || p.lse == nullptr || in_extent(lse_off, 1, L.stat_ext, p.status);
         if (ok && Jt > 0) {
             if (warp_wait_all(&bar_ofinal[t], 0, wd, kSiteFwdSoftmaxO)) {
                 tc_fence_after();
@@ -502,7 +505,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     for (int c = 0; c < 16; ++c)
                         packed[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
                                                 __uint_as_float(o[2 * c + 1]) * inv_l);
-                    if (qrow < se.nq) {
+                    if (qrow < se.nq && o_in) {
                         uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -510,13 +513,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                                                 packed[4 * c + 3]);
                     }
                 }
-                if (qrow < se.nq && p.lse != nullptr) p.lse[lse_off] = (m + __log2f(l)) * kLn2;
+                if (qrow < se.nq && p.lse != nullptr && lse_in) p.lse[lse_off] = (m + __log2f(l)) * kLn2;
             }
         } else if (t < nt && Jt == 0 && qrow < se.nq) {
             // the whole tile sees no key: O = 0 and lse = log(0) = -inf
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow_off);
-            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-            if (p.lse != nullptr) p.lse[lse_off] = -INFINITY;
+            if (o_in)
+                for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (p.lse != nullptr && lse_in) p.lse[lse_off] = -INFINITY;
         }
         tc_fence_before();
     }

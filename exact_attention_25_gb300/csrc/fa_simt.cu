@@ -226,12 +226,14 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams 
     // The loop bound is uniform across the warp, so the shuffles below see all 32 lanes.
     for (size_t base = gw * RPW; base < rows; base += warps_total * RPW) {
         const size_t row = base + lane / TPR;
-        const bool valid = row < rows;
+        const size_t hh = row / static_cast<size_t>(L.Rq), i = row - hh * static_cast<size_t>(L.Rq);
+        const size_t off_o = i * static_cast<size_t>(L.o_rs) + hh * static_cast<size_t>(L.o_hs);
+        const size_t off_g = i * static_cast<size_t>(L.do_rs) + hh * static_cast<size_t>(L.do_hs);
+        const bool valid = row < rows && in_extent(off_o, D, L.o_ext, p.status) &&
+                           in_extent(off_g, D, L.do_ext, p.status) &&
+                           in_extent(row, 1, L.stat_ext, p.status);
         float acc = 0.0f;
         if (valid) {
-            const size_t hh = row / static_cast<size_t>(L.Rq), i = row - hh * static_cast<size_t>(L.Rq);
-            const size_t off_o = i * static_cast<size_t>(L.o_rs) + hh * static_cast<size_t>(L.o_hs);
-            const size_t off_g = i * static_cast<size_t>(L.do_rs) + hh * static_cast<size_t>(L.do_hs);
             const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off_o)[sub];
             const uint4 b = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off_g)[sub];
             const T* ea = reinterpret_cast<const T*>(&a);

@@ -53,7 +53,8 @@ enum fa_status {
     FA_ERR_LAUNCH = -5,          /* a CUDA call failed; fa_last_error() has its text       */
     FA_ERR_DEVICE_TIMEOUT = -6,  /* a bounded on-device wait expired (watchdog)            */
     FA_ERR_TOO_LARGE = -7,       /* a tensor has 2^31 or more elements                     */
-    FA_ERR_UNSUPPORTED_DEVICE = -8 /* bf16 tensor-core path needs compute capability 10.3 */
+    FA_ERR_UNSUPPORTED_DEVICE = -8, /* bf16 tensor-core path needs compute capability 10.3 */
+    FA_ERR_OUT_OF_BOUNDS = -9    /* checked builds: an access fell outside its buffer      */
 };
 
 /* Forward.  q, k, v: inputs [B,H,N,d]; o: output [B,H,N,d] (same dtype); lse: output
@@ -231,7 +232,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 
 /* Synchronises `stream`, then reads and clears the device status word that bounded waits
  * inside the kernels write when they give up.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (the
- * wait site is appended to fa_last_error()) or FA_ERR_LAUNCH if the synchronisation failed. */
+ * wait site is appended to fa_last_error()), FA_ERR_OUT_OF_BOUNDS (checked builds only) or
+ * FA_ERR_LAUNCH if the synchronisation failed. */
 int fa_device_status(void* stream);
 
 /* Upper bound, in nanoseconds, on every on-device wait (default 2e9).  Values below 1e6 are
@@ -244,6 +246,15 @@ void fa_set_wait_limit_ns(unsigned long long ns);
  * FA_ERR_DEVICE_TIMEOUT.  0 (the default) restores normal operation.  Not for production use;
  * applies to launches made after the call. */
 void fa_debug_set_flags(int flags);
+
+/* 1 if this library is the checked build (libfa_checked.so, compiled with FA_CHECKED), else 0.
+ * A checked build tests every element the kernels read or write directly in global memory
+ * (outputs, gradients, statistics, decode partials; tiles moved by TMA are bounded by their
+ * tensor maps) against the extent of its buffer implied by the call's sizes and strides:
+ * an access outside it is skipped and fa_device_status() then returns FA_ERR_OUT_OF_BOUNDS.
+ * Its results are otherwise identical to the regular build's.  With fa_debug_set_flags(2)
+ * the checked build takes every extent one row short, so the check must fire (test hook). */
+int fa_checked_build(void);
 
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(int code);

@@ -38,6 +38,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_checked_variant_exports_the_same_symbols_and_says_so(lib):
+    path = build.build(checked=True)
+    checked = _lib.load(path)
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    assert checked.fa_checked_build() == 1 and lib.fa_checked_build() == 0
+    # argument validation is shared: the checked variant rejects the same calls
+    assert fwd(checked, d=96) == -2 and fwd(checked, q=MIS) == -3
+
+
 P = ctypes.c_void_p
 A = P(0x10000)  # aligned dummy pointers: validation must reject before dereferencing
 A2 = P(0x20000)
