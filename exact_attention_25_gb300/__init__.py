@@ -17,7 +17,8 @@ __all__ = [
     "fa_device_status", "fa_set_wait_limit_ns", "fa_causal_block_counts", "forward", "backward",
     "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "forward_varlen",
     "backward_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
-    "forward_decode", "fa_checked_build",
+    "forward_decode", "fa_checked_build", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes",
+    "forward_fp8",
 ]
 
 
@@ -137,6 +138,42 @@ def fa_set_wait_limit_ns(ns: int) -> None:
 def fa_checked_build() -> bool:
     """C ``fa_checked_build``: whether the library in use is the bounds-checked variant."""
     return bool(load().fa_checked_build())
+
+
+def fa_fwd_fp8_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_fwd_fp8_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_fp8(q, k, v, o, lse, scale: float, q_descale: float, k_descale: float,
+               v_descale: float, causal: bool, workspace, stream=None) -> None:
+    """C ``fa_fwd_fp8``: q, k, v [B, H, N, 128] e4m3 codes (any 1-byte dtype, for example
+    torch.float8_e4m3fn or uint8), o [B, H, N, 128] bf16, lse [B, H, N] fp32 or None."""
+    _check_tensors(q, k, v, o, lse, workspace)
+    for t in (q, k, v):
+        if t.element_size() != 1 or tuple(t.shape) != tuple(q.shape):
+            raise ValueError("q, k and v must be [B, H, N, d] tensors of 1-byte e4m3 codes")
+    B, H, N, d = _shape(q)
+    nbytes = workspace.numel() * workspace.element_size()
+    check(load().fa_fwd_fp8(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+        float(q_descale), float(k_descale), float(v_descale), int(bool(causal)), _ptr(workspace),
+        nbytes, _stream(stream)))
+
+
+def forward_fp8(q, k, v, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                scale: float | None = None, causal: bool = False, stream=None):
+    """Allocate O (bf16), LSE and the workspace and run fa_fwd_fp8."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(fa_fwd_fp8_workspace_bytes(B, H, N, d), 16), dtype=torch.uint8,
+                     device=q.device)
+    fa_fwd_fp8(q, k, v, o, lse, scale, q_descale, k_descale, v_descale, causal, ws, stream)
+    return o, lse
 
 
 def fa_causal_block_counts(q_block: int, Br: int, Bc: int, N: int) -> tuple[int, int]:

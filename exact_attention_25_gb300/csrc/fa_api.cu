@@ -24,6 +24,9 @@ cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p,
 cudaError_t launch_decode(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const DecodeParams& p, cudaStream_t st,
                           int num_sms);
+cudaError_t launch_fwd_fp8_tc(const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tvt, const FwdParams& p, cudaStream_t st);
+cudaError_t launch_vt_transpose(const void* v, void* vt, int BH, int N, int Npad, cudaStream_t st);
 
 // Device status word written by bounded waits that give up (0 = fine).
 __device__ int g_status_word;
@@ -918,4 +921,86 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     if ((rc = scratch_address(&scratch))) return rc;
     return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype,
                      scratch, kNoallocBytes, 0, -1, stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// e4m3 forward
+// ---------------------------------------------------------------------------------------
+namespace {
+
+long long fp8_pad_keys(int N) { return (static_cast<long long>(N) + 15) / 16 * 16; }
+
+// 3-D map of 8-bit codes, dimensions (x, y, z) with byte strides for y and z; box 128 x 128 x 1
+// (one 128-byte swizzle panel of 128 rows).
+int make_map_u8(CUtensorMap* m, const void* base, cuuint64_t x, cuuint64_t y, cuuint64_t z,
+                cuuint64_t y_stride, cuuint64_t z_stride)
+{
+    cuuint64_t dims[3] = {x, y, z};
+    cuuint64_t strides[2] = {y_stride, z_stride};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
+    return FA_OK;
+}
+
+bool finite(float x) { return x == x && x != INFINITY && x != -INFINITY; }
+
+}  // namespace
+
+extern "C" size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d)
+{
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    return align256(static_cast<size_t>(B) * H * d * static_cast<size_t>(fp8_pad_keys(N)));
+}
+
+extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int N, int d, float scale, float q_descale,
+                          float k_descale, float v_descale, int causal, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    int rc = check_common(B, H, N, d, scale, causal, FA_BF16);
+    if (rc) return rc;
+    if (d != 128) return fail(FA_ERR_UNSUPPORTED_D, "the e4m3 forward takes d = 128 only");
+    if (!finite(q_descale) || !finite(k_descale) || !finite(v_descale) ||
+        !finite(scale * q_descale * k_descale))
+        return fail(FA_ERR_INVALID_ARG, "descale factors (and their product with scale) must be finite");
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    const size_t need = fa_fwd_fp8_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    if ((rc = get_encoder())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long Npad = fp8_pad_keys(N);
+    const cuuint64_t BH = static_cast<cuuint64_t>(B) * H, n = static_cast<cuuint64_t>(N);
+    CUtensorMap maps[3];
+    // Q, K: (d, N, B*H) bytes; V^T: (Npad keys, d, B*H)
+    if ((rc = make_map_u8(&maps[0], q, 128, n, BH, 128, n * 128)) ||
+        (rc = make_map_u8(&maps[1], k, 128, n, BH, 128, n * 128)) ||
+        (rc = make_map_u8(&maps[2], workspace, static_cast<cuuint64_t>(Npad), 128, BH,
+                          static_cast<cuuint64_t>(Npad), static_cast<cuuint64_t>(Npad) * 128)))
+        return rc;
+    fa::FwdParams p{};
+    p.q = q; p.k = k; p.v = workspace; p.o = o; p.lse = lse;
+    p.N = N; p.BH = B * H; p.scale = scale;
+    p.scale_log2 = scale * q_descale * k_descale * fa::kLog2e;
+    p.v_descale = v_descale;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    p.L = fixed_layout(B, H, N, d);
+    cudaError_t e = fa::launch_vt_transpose(v, workspace, B * H, N, static_cast<int>(Npad), st);
+    if (e != cudaSuccess) return cuda_fail(e, "V transpose launch");
+    e = fa::launch_fwd_fp8_tc(maps[0], maps[1], maps[2], p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "e4m3 forward launch");
+    return FA_OK;
 }

@@ -174,6 +174,7 @@ struct FwdParams {
     int* status;       // device status word (watchdog)
     unsigned long long wait_limit_ns;
     int debug_flags;   // test hook: kDebugDropFirstLoad
+    float v_descale;   // e4m3 forward: the factor that turns stored V codes into values
     Layout L;
 };
 

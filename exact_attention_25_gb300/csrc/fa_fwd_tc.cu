@@ -15,6 +15,13 @@
 // of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised); at d = 64, O_t at
 // [256 + 128t, 384 + 128t), whose column 64 accumulates the row sum of the bf16 P (the P V
 // product runs at N = 128 against V and a constant ones-column panel).
+//
+// The e4m3 variant (F8, d = 128, fixed-length square heads) runs the same schedule on 8-bit
+// operands with kind::f8f6f4 MMAs (K = 32 per MMA): Q and K tiles of 128 rows x 128 bytes,
+// P rounded to e4m3 (four per TMEM column, at columns [64, 96) of S_t), and V read from a
+// transposed copy V^T [d, keys] so that both operands of O += P V are K-major.  The
+// descale factors of Q and K are folded into the softmax scale on the host; V's is applied
+// with 1/l in the epilogue.  O is normalised by the fp32 row sum l.
 #include <type_traits>
 
 #include "fa_common.cuh"
@@ -22,22 +29,26 @@
 
 namespace fa {
 
-template <int D>
+template <int D, bool F8 = false>
 struct FwdCfg {
     static constexpr int BM = 128;                 // query rows per tile
     static constexpr int NT = 2;                   // query tiles per CTA
     static constexpr int BN = 128;                 // keys per block
-    static constexpr int PANELS = D / 64;          // 128-byte swizzle panels per row
+    static constexpr int ELEM = F8 ? 1 : 2;        // bytes per operand element
+    static constexpr int PANEL_ELEMS = 128 / ELEM; // elements in one 128-byte panel row
+    static constexpr int PANELS = D / PANEL_ELEMS; // 128-byte swizzle panels per row
     static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-    static constexpr int STAGES = (D == 128) ? 2 : 4;
+    static constexpr int KSTEPS_QK = D * ELEM / 32;   // MMAs per S product (32 bytes of K each)
+    static constexpr int KSTEPS_PV = BN * ELEM / 32;  // MMAs per P V product
+    static constexpr int STAGES = (D == 128 && !F8) ? 2 : 4;
     static constexpr int SMEM_Q = NT * TILE_BYTES;
     static constexpr int SMEM_K = STAGES * TILE_BYTES;
     static constexpr int SMEM_V = STAGES * TILE_BYTES;
     // d = 64: the P V product runs at N = 128 against V and a constant panel whose first column
     // is 1.0, so O's column 64 accumulates the sum of the bf16 P weights on the tensor core
     // (the row sum that normalises O), instead of ~190 softmax instructions per row and block.
-    static constexpr bool SUM_ON_MMA = (D == 64);
+    static constexpr bool SUM_ON_MMA = (D == 64 && !F8);
     static constexpr int O_COLS = SUM_ON_MMA ? 128 : D;  // TMEM columns of one O accumulator
     static constexpr int SMEM_ONES = SUM_ON_MMA ? PANEL_BYTES : 0;
     static constexpr int SMEM_BYTES = SMEM_Q + SMEM_K + SMEM_V + SMEM_ONES + 1024;  // + slack
@@ -46,36 +57,48 @@ struct FwdCfg {
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: P stays below 2^8
 };
 
-// S = Q K^T for one 128-row query tile: D/16 k-steps of 16, the first overwriting D.
-// Executed by the whole MMA warp; one elected lane issues each MMA.
-template <int D, int PANEL>
+// S = Q K^T for one 128-row query tile: KSTEPS k-steps of 32 bytes of d (16 bf16 or 32 e4m3
+// elements), the first overwriting D.  Executed by the whole MMA warp; one elected lane
+// issues each MMA.
+template <int KSTEPS, int PANEL, bool F8>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc,
                                          uint32_t idesc)
 {
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
+    for (int ks = 0; ks < KSTEPS; ++ks) {
         const uint32_t off = (ks / 4) * PANEL + (ks % 4) * 32;
-        mma_ss_w(d_tmem, sdesc_adv(qdesc, off), sdesc_adv(kdesc, off), idesc, ks > 0 ? 1u : 0u);
+        if constexpr (F8)
+            mma_ss_w_f8(d_tmem, sdesc_adv(qdesc, off), sdesc_adv(kdesc, off), idesc, ks > 0 ? 1u : 0u);
+        else
+            mma_ss_w(d_tmem, sdesc_adv(qdesc, off), sdesc_adv(kdesc, off), idesc, ks > 0 ? 1u : 0u);
     }
 }
 
-// O += P V: P (bf16) from TMEM, V (MN-major) from shared memory; BN/16 k-steps over keys.
-template <int BN>
+// O += P V: P from TMEM (8 columns = 32 bytes of keys per k-step), V from shared memory:
+// bf16 V is MN-major (a k-step of 16 keys is 16 rows = 2048 bytes further), e4m3 V^T is
+// K-major (a k-step of 32 keys is 32 bytes further along its rows).
+template <int KSTEPS, bool F8>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
                                          uint32_t idesc, uint32_t acc_first)
 {
 #pragma unroll
-    for (int ks = 0; ks < BN / 16; ++ks)
-        mma_ts_w(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc, ks > 0 ? 1u : acc_first);
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        if constexpr (F8)
+            mma_ts_w_f8(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 32), idesc,
+                        ks > 0 ? 1u : acc_first);
+        else
+            mma_ts_w(d_tmem, p_tmem + 8u * ks, sdesc_adv(vdesc, ks * 2048), idesc,
+                     ks > 0 ? 1u : acc_first);
+    }
 }
 
-template <int D, int MODE>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+template <int D, int MODE, bool F8>
+__global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
 {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -188,8 +211,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             mbar_arrive_expect_tx_w(&bar_q, nt * C::TILE_BYTES);
             for (int t = 0; t < nt; ++t)
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_rows_w(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q, 64 * pn,
-                                sr.q0 + (qt0 + t) * C::BM, qhead, packed);
+                    tma_load_rows_w(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_q,
+                                    C::PANEL_ELEMS * pn, sr.q0 + (qt0 + t) * C::BM, qhead, packed);
             int issued = 0;
             for (int j = 0; j < Jmax; ++j) {
                 const int s = j % C::STAGES;
@@ -200,13 +223,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 mbar_arrive_expect_tx_w(&bar_kfull[s], C::TILE_BYTES);
                 for (int pn = 0; pn < C::PANELS; ++pn)
                     tma_load_rows_w(sK + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bar_kfull[s],
-                                64 * pn, sr.k0 + j * C::BN, khead, packed);
+                                    C::PANEL_ELEMS * pn, sr.k0 + j * C::BN, khead, packed);
                 if (!warp_wait_all(&bar_vempty[s], ph ^ 1, wd, kSiteFwdLoadEmpty)) break;
                 mbar_arrive_expect_tx_w(&bar_vfull[s], C::TILE_BYTES);
-                if (!(j == 0 && (p.debug_flags & kDebugDropFirstLoad)))
+                if (j == 0 && (p.debug_flags & kDebugDropFirstLoad)) {
+                    // (watchdog test: the announced V tile never arrives)
+                } else if constexpr (F8) {
+                    // V^T tile: the d rows of this head, keys [j BN, j BN + BN) (x in bytes)
+                    tma_load_3d_w(sV + s * C::TILE_BYTES, &tm_v, &bar_vfull[s], j * C::BN, 0, khead);
+                } else {
                     for (int pn = 0; pn < C::PANELS; ++pn)
                         tma_load_rows_w(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
-                                    &bar_vfull[s], 64 * pn, sr.k0 + j * C::BN, khead, packed);
+                                        &bar_vfull[s], C::PANEL_ELEMS * pn, sr.k0 + j * C::BN,
+                                        khead, packed);
+                }
                 issued = j + 1;
             }
             // Let no copy land after the CTA exits: wait (bounded, ignoring the abort flag)
@@ -224,16 +254,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
         {  // the whole warp runs the loop (warp-uniform values); elect.sync picks the issuer
-            constexpr uint32_t kIdS = idesc_bf16_f32(128, C::BN, 0, 0);  // S = Q K^T
-            constexpr uint32_t kIdPV = idesc_bf16_f32(128, C::O_COLS, 0, 1);  // O += P V
+            constexpr uint32_t kIdS = F8 ? idesc_e4m3_f32(128, C::BN)  // S = Q K^T
+                                         : idesc_bf16_f32(128, C::BN, 0, 0);
+            constexpr uint32_t kIdPV = F8 ? idesc_e4m3_f32(128, D)  // O += P V
+                                          : idesc_bf16_f32(128, C::O_COLS, 0, 1);
             // Everything the issue loop needs lives in scalar registers: base descriptors are
             // built once and advanced by byte offsets (stage, tile, k-step), so the single
             // issuing thread keeps pace with the tensor core.
             const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
             // V is MN-major; its second 64-column panel is the next panel of the stage (d = 128)
-            // or the constant column panel (d = 64), at a stage-dependent distance.
-            const uint64_t dv0 = sdesc_sw128(smem_u32(sV), C::PANEL_BYTES, 1024);
+            // or the constant column panel (d = 64), at a stage-dependent distance.  (e4m3: V^T
+            // is K-major, 128 d rows of 128 key bytes.)
+            const uint64_t dv0 = F8 ? sdesc_sw128(smem_u32(sV), 16, 1024)
+                                    : sdesc_sw128(smem_u32(sV), C::PANEL_BYTES, 1024);
             const uint64_t dvo = sdesc_sw128(smem_u32(sV), smem_u32(sOnes) - smem_u32(sV), 1024);
             auto vdesc = [&](int s) {
                 if constexpr (C::SUM_ON_MMA) {
@@ -258,11 +292,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (ok) {
                 tc_fence_after();
                 if (J0 > 0) {
-                    issue_qk<D, C::PANEL_BYTES>(tS0, dq0, dk0, kIdS);
+                    issue_qk<C::KSTEPS_QK, C::PANEL_BYTES, F8>(tS0, dq0, dk0, kIdS);
                     mma_commit_w(&bar_sfull[0]);
                 }
                 if (J1 > 0) {
-                    issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), dk0, kIdS);
+                    issue_qk<C::KSTEPS_QK, C::PANEL_BYTES, F8>(tS1, sdesc_adv(dq0, C::TILE_BYTES), dk0, kIdS);
                     mma_commit_w(&bar_sfull[1]);
                 }
                 mma_commit_w(&bar_kempty[0]);  // K(0) is read by these S products only
@@ -282,14 +316,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 if (j < J0) {
                     if (!warp_wait_all(&bar_pfull[0], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv<C::BN>(tO0, tS0 + 64u, vd, kIdPV, acc_first);
+                    issue_pv<C::KSTEPS_PV, F8>(tO0, tS0 + 64u, vd, kIdPV, acc_first);
                     if (j + 1 == J0) {
                         mma_commit_w(&bar_ofinal[0]);
                     } else {
                         if (!warp_wait_all(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
                         tc_fence_after();
                         k_next = true;
-                        issue_qk<D, C::PANEL_BYTES>(tS0, dq0, kd1, kIdS);
+                        issue_qk<C::KSTEPS_QK, C::PANEL_BYTES, F8>(tS0, dq0, kd1, kIdS);
                         mma_commit_w(&bar_sfull[0]);
                     }
                 }
@@ -297,7 +331,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 if (j < J1) {
                     if (!warp_wait_all(&bar_pfull[1], j & 1, wd, kSiteFwdMmaP)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv<C::BN>(tO1, tS1 + 64u, vd, kIdPV, acc_first);
+                    issue_pv<C::KSTEPS_PV, F8>(tO1, tS1 + 64u, vd, kIdPV, acc_first);
                     if (j + 1 == J1) {
                         mma_commit_w(&bar_ofinal[1]);
                     } else {
@@ -305,7 +339,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                             if (!warp_wait_all(&bar_kfull[s1], ph1, wd, kSiteFwdMmaK)) { ok = false; break; }
                             tc_fence_after();
                         }
-                        issue_qk<D, C::PANEL_BYTES>(tS1, sdesc_adv(dq0, C::TILE_BYTES), kd1, kIdS);
+                        issue_qk<C::KSTEPS_QK, C::PANEL_BYTES, F8>(tS1, sdesc_adv(dq0, C::TILE_BYTES), kd1, kIdS);
                         mma_commit_w(&bar_sfull[1]);
                     }
                 }
@@ -425,6 +459,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     p1 = ex2(p1);
                     p2 = ex2(p2);
                     p3 = ex2(p3);
+                    if constexpr (F8) {  // e4m3 P, four keys per column; O is normalised by l
+                        lsa = f2_add(lsa, f2_make(p0, p1));
+                        lsb = f2_add(lsb, f2_make(p2, p3));
+                        pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+                        continue;
+                    }
                     const uint32_t w01 = pack_bf16x2(p0, p1);
                     const uint32_t w23 = pack_bf16x2(p2, p3);
                     lsa = f2_add(lsa, f2_make(p0, p1));
@@ -441,7 +481,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     pk[c / 2] = w01;
                     pk[c / 2 + 1] = w23;
                 }
-                tmem_st16(tP + 16u * cb, pk);
+                if constexpr (F8)
+                    tmem_st8(tP + 8u * cb, pk);
+                else
+                    tmem_st16(tP + 16u * cb, pk);
             }
             {
                 float a0, a1, b0, b1;
@@ -492,7 +535,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     reg_fence32(sc);
                     lr = __uint_as_float(sc[0]);
                 }
-                const float inv_l = lr > 0.0f ? 1.0f / lr : 0.0f;
+                float inv_l;
+                if constexpr (F8)
+                    inv_l = l > 0.0f ? p.v_descale / l : 0.0f;
+                else
+                    inv_l = lr > 0.0f ? 1.0f / lr : 0.0f;
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + orow_off;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
@@ -532,16 +579,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool F8 = false>
 static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                       const CUtensorMap& tv, const FwdParams& p, cudaStream_t st)
 {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, F8>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, MODE>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, MODE, F8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -550,7 +597,7 @@ static cudaError_t launch_fwd_tc_impl(const CUtensorMap& tq, const CUtensorMap& 
     const int n_qtiles = (p.L.Nq + C::BM - 1) / C::BM;
     const int n_pairs = (n_qtiles + C::NT - 1) / C::NT;
     dim3 grid(p.L.B * p.L.H * n_pairs);
-    fa_fwd_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
+    fa_fwd_tc_kernel<D, MODE, F8><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -565,6 +612,13 @@ cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
         return launch_fwd_tc_impl<Dc, kModeFixed>(tq, tk, tv, p, st);
     };
     return d == 64 ? run(std::integral_constant<int, 64>{}) : run(std::integral_constant<int, 128>{});
+}
+
+// e4m3 forward: d = 128, fixed-length square heads; tvt maps the transposed V^T copy.
+cudaError_t launch_fwd_fp8_tc(const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tvt, const FwdParams& p, cudaStream_t st)
+{
+    return launch_fwd_tc_impl<128, kModeFixed, true>(tq, tk, tvt, p, st);
 }
 
 }  // namespace fa

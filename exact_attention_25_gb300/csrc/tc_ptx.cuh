@@ -4,6 +4,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace fa {
@@ -246,6 +247,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0 in both fields), fp32 D,
+// dense, both operands K-major.  Same field layout as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------------------------------
 // MMA issue (single thread) and completion tracking.
 // ---------------------------------------------------------------------------------------
@@ -295,6 +303,31 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
         "setp.ne.b32 a, %4, 0;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, a;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// kind::f8f6f4 forms (8-bit operands, one MMA covers K = 32): otherwise as above.
+__device__ __forceinline__ void mma_ss_w_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred a, e;\n\t"
+        "setp.ne.b32 a, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, a;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_w_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred a, e;\n\t"
+        "setp.ne.b32 a, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, a;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -471,6 +504,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four floats to e4m3 (round to nearest even, saturating at 448), element k in byte k: the
+// order of 8-bit operand elements along K in a 32-bit TMEM column or shared-memory word.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a2, a3), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
 }
 
 }  // namespace fa

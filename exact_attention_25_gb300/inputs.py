@@ -128,3 +128,39 @@ def random_varlen(lens_q, lens_k, H: int, Hkv: int, d: int, dtype=torch.bfloat16
     if with_do:
         out["do"] = torch.randn((tq, H, d), generator=g).to(dtype)
     return out
+
+
+def random_fp8(B: int, H: int, N: int, d: int, seed: int = 0, in_scale: float = 1.0,
+               kind: str = "normal") -> dict:
+    """Seeded e4m3 inputs (torch.float8_e4m3fn, CPU) with per-tensor descale factors.
+
+    kind "normal": float32 standard-normal Q, K, V times ``in_scale`` (drawn in that order),
+    each divided by its descale factor amax / 448 so that its largest magnitude maps to the
+    largest e4m3 value, then cast (round to nearest even).
+    kind "integer": Q and K rows with at most four entries of +-1 at random positions (the
+    rest 0), so every score Q K^T is an integer in [-4, 4]; V as for "normal"; descale
+    factors 1 for Q and K.  With the softmax scale ln 2 the weights are powers of two."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, N, d)
+    out = {}
+
+    def quantize(x):
+        amax = float(x.abs().max())
+        ds = amax / 448.0 if amax > 0 else 1.0
+        return (x / ds).to(torch.float8_e4m3fn), ds
+
+    if kind == "normal":
+        for n in ("q", "k", "v"):
+            out[n], out[n + "_descale"] = quantize(torch.randn(shape, generator=g) * in_scale)
+    elif kind == "integer":
+        for n in ("q", "k"):
+            x = torch.zeros(shape)
+            cols = torch.randint(0, d, (B, H, N, 4), generator=g)
+            signs = torch.randint(0, 3, (B, H, N, 4), generator=g).float() - 1.0  # -1, 0, +1
+            x.scatter_(3, cols, signs)  # repeated columns keep one of their values
+            out[n], out[n + "_descale"] = x.to(torch.float8_e4m3fn), 1.0
+        out["v"], out["v_descale"] = quantize(torch.randn(shape, generator=g) * in_scale)
+    else:
+        raise ValueError(f"unknown kind {kind!r}")
+    return out

@@ -30,8 +30,8 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--stage", type=int, default=-1)
     ap.add_argument("--time", action="store_true", help="report CUDA-event timing")
-    ap.add_argument("--dtype", choices=["bf16", "fp32"], default="bf16",
-                    help="fixed layout: fp32 runs the SIMT kernels")
+    ap.add_argument("--dtype", choices=["bf16", "fp32", "fp8"], default="bf16",
+                    help="fixed layout: fp32 runs the SIMT kernels, fp8 the e4m3 forward")
     ap.add_argument("--Hkv", type=int, default=0,
                     help="packed layout with this many key/value heads (GQA); 0 = fixed layout")
     ap.add_argument("--Nq", type=int, default=0,
@@ -44,6 +44,8 @@ def main():
         return run_decode(a)
     if a.Hkv:
         return run_packed(a)
+    if a.dtype == "fp8":
+        return run_fp8(a)
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     shape = (a.B, a.H, a.N, a.d)
@@ -143,6 +145,38 @@ def run_packed(a):
     fl = 4.0 * a.B * a.H * pairs * a.d * (1.0 if a.which == "fwd" else 2.5)
     print(f"{a.which} packed B={a.B} H={a.H} Hkv={a.Hkv} Nq={nq} Nk={a.N} d={a.d} "
           f"causal={a.causal}: {ms:.4f} ms {fl / ms / 1e9:.1f} TFLOP/s")
+
+
+def run_fp8(a):
+    """The e4m3 forward (transpose of V, then the tensor-core kernel) on standard-normal codes
+    with unit descale factors; FLOPs by the same convention as the bf16 forward."""
+    import torch
+
+    import exact_attention_25_gb300 as fa
+    from exact_attention_25_gb300 import perfmodel
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    shape = (a.B, a.H, a.N, a.d)
+    q, k, v = (torch.randn(shape, generator=g, device="cuda").to(torch.float8_e4m3fn)
+               for _ in range(3))
+    o = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((a.B, a.H, a.N), device="cuda", dtype=torch.float32)
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(*shape), dtype=torch.uint8, device="cuda")
+    run = lambda: fa.fa_fwd_fp8(q, k, v, o, lse, a.d ** -0.5, 1.0, 1.0, 1.0, a.causal, ws)  # noqa: E731
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    fa.fa_device_status()
+    ms = e0.elapsed_time(e1) / a.iters
+    fl = perfmodel.fwd_flops(*shape, a.causal)
+    print(f"fwd fp8 B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: {ms:.4f} ms "
+          f"{fl / ms / 1e9:.1f} TFLOP/s (transpose + forward)")
 
 
 def run_decode(a):

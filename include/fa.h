@@ -115,6 +115,35 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
                void* stream);
 
+/* e4m3 (FP8) forward, per-tensor scaling (the FP8 mode of FlashAttention-3 named in the
+ * "FA2·FA3" section of "Flash Attention IO-awareness principle"; the page gives no
+ * algorithm, so the plainest reading is taken).
+ *
+ * What it computes.  q, k, v hold e4m3 codes (1 byte each, OCP FP8 E4M3: bias 7, no
+ * infinities, largest finite 448) standing for the values Q = q_descale * q, K = k_descale * k,
+ * V = v_descale * v.  The result is exact attention on those values, as fa_fwd computes it:
+ * O = softmax(scale * Q K^T [+ causal mask]) V in bf16 and lse (natural log of the scaled
+ * logits) in fp32.  Q K^T accumulates exactly (every e4m3 product is exact in fp32); the
+ * probabilities enter the P V product rounded to e4m3, so |O - O_exact| is bounded, element
+ * by element, by v_descale * sum_j max(2^-4 P_ij, 2^-10 max_j P_ij) |v_jc| plus bf16
+ * rounding of O.  O is divided by the fp32 sum of the unrounded probabilities.
+ *
+ *   - Layout: q, k, v [B, H, N, 128] contiguous bytes; o [B, H, N, 128] bf16; lse [B, H, N]
+ *     fp32 (may be null).  d must be 128 (else FA_ERR_UNSUPPORTED_D).
+ *   - workspace: at least fa_fwd_fp8_workspace_bytes(B, H, N, d) bytes, 16-byte aligned,
+ *     owned by the caller; it receives a transposed copy of v (each head's 128 x N codes,
+ *     keys padded to a multiple of 16) that the tensor-core kernel reads as a K-major
+ *     operand.  Its contents need no initialisation and mean nothing after the call.
+ *   - scale, q_descale, k_descale, v_descale: finite floats (else FA_ERR_INVALID_ARG);
+ *     scale * q_descale * k_descale multiplies the dot products of the stored e4m3 values.
+ *   - Errors, streams and ownership as fa_fwd; two kernels run on `stream` (the transpose,
+ *     then the forward).  Needs compute capability 10.3. */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, float q_descale, float k_descale, float v_descale,
+               int causal, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Packed variable-length batches with grouped key/value heads (bf16, tensor-core path).
  *
  * What it computes.  B independent sequences; sequence b has the query rows

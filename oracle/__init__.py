@@ -245,3 +245,87 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
             out["dk"][ks, h // G] += r["dk"]
             out["dv"][ks, h // G] += r["dv"]
     return out
+
+
+# --------------------------------------------------------------------------- e4m3 inputs
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of OCP FP8 E4M3 codes (uint8), from the format's definition: bit 7 the sign,
+    bits 6-3 the exponent with bias 7, bits 2-0 the mantissa; exponent field 0 holds the
+    subnormals m/8 * 2^-6; the codes S.1111.111 are NaN and there is no infinity, so the
+    largest finite value is 1.75 * 2^8 = 448."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+def _codes(t) -> np.ndarray:
+    """The bytes of a 1-byte tensor (torch float8 / uint8) or array, as uint8."""
+    if hasattr(t, "detach"):
+        import torch
+
+        t = t.detach().to("cpu").contiguous().view(torch.uint8).numpy()
+    return np.ascontiguousarray(t, dtype=np.uint8)
+
+
+def attention_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float,
+                  scale: float, causal: bool):
+    """Exact attention on the values that e4m3 codes stand for (per-tensor scaling):
+    Q = q_descale * e4m3(q8), K = k_descale * e4m3(k8), V = v_descale * e4m3(v8), all
+    ``[B, H, N, d]``.  Returns dict o, lse (Algorithm 0 on those values, as attention_fwd_head)
+    , ``pv_abs`` = sum_j P_ij |V_jc| (the scale of accumulation error) and ``bound``: per
+    element of O, the largest deviation that rounding every probability to
+    e4m3 before the P V product can cause when O is divided by the unrounded row sum,
+        bound_ic = sum_j max(2^-4 P_ij, 2^-10 max_j' P_ij') |V_jc|   (over the keys row i sees),
+    with 2^-4 the relative half-spacing of normal e4m3 values and 2^-10 half the subnormal
+    spacing (probabilities held relative to a stale row maximum only scale these terms by a
+    factor <= 1, and the row sum is at least 1 / max_j P_ij).  Rounding of O to bf16 comes on
+    top."""
+    q = e4m3_decode(_codes(q8)) * float(q_descale)
+    k = e4m3_decode(_codes(k8)) * float(k_descale)
+    v = e4m3_decode(_codes(v8)) * float(v_descale)
+    B, H, N, d = q.shape
+    o = np.empty((B, H, N, d))
+    lse = np.empty((B, H, N))
+    bound = np.empty((B, H, N, d))
+    pv_abs = np.empty((B, H, N, d))
+    for b in range(B):
+        for h in range(H):
+            ob, lb, P = attention_fwd_head(q[b, h], k[b, h], v[b, h], scale, causal, want_p=True)
+            seen = np.ones((N, N), dtype=bool)
+            if causal:
+                seen = np.tril(seen)
+            w = np.maximum(P / 16.0, P.max(axis=1, keepdims=True) / 1024.0) * seen
+            o[b, h], lse[b, h] = ob, lb
+            bound[b, h] = w @ np.abs(v[b, h])
+            pv_abs[b, h] = P @ np.abs(v[b, h])
+    return {"o": o, "lse": lse, "bound": bound, "pv_abs": pv_abs}
+
+
+def attention_fp8_rows(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float,
+                       scale: float, causal: bool, rows):
+    """attention_fp8 for the sampled query rows ``rows`` = [(b, h, i), ...] only, each from its
+    own row of scores (Algorithm 0 restricted to that row, causal keys j <= i).  Returns dict
+    o [n, d], lse [n], bound [n, d], pv_abs [n, d] in the order of ``rows``."""
+    qc, kc, vc = _codes(q8), _codes(k8), _codes(v8)
+    out = {"o": [], "lse": [], "bound": [], "pv_abs": []}
+    for b, h, i in rows:
+        qi = e4m3_decode(qc[b, h, i]) * float(q_descale)
+        n = i + 1 if causal else kc.shape[2]
+        kk = e4m3_decode(kc[b, h, :n]) * float(k_descale)
+        vv = e4m3_decode(vc[b, h, :n]) * float(v_descale)
+        s = scale * (kk @ qi)
+        m = s.max()
+        e = np.exp(s - m)
+        tot = e.sum()
+        P = e / tot
+        out["o"].append(P @ vv)
+        out["lse"].append(m + np.log(tot))
+        w = np.maximum(P / 16.0, P.max() / 1024.0)
+        out["bound"].append(w @ np.abs(vv))
+        out["pv_abs"].append(P @ np.abs(vv))
+    return {key: np.array(val) for key, val in out.items()}

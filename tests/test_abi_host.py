@@ -58,6 +58,29 @@ def fwd(lib, q=A, k=A, v=A, o=A2, lse=A2, B=1, H=1, N=8, d=64, scale=0.125, caus
     return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), causal, dtype, None)
 
 
+def fp8(lib, q=A, k=A, v=A, o=A2, lse=A2, B=1, H=1, N=8, d=128, scale=0.1, qd=1.0, kd=1.0,
+        vd=1.0, causal=0, ws=A, nbytes=1 << 20):
+    f = ctypes.c_float
+    return lib.fa_fwd_fp8(q, k, v, o, lse, B, H, N, d, f(scale), f(qd), f(kd), f(vd), causal, ws,
+                          nbytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), -2), (dict(N=0), -1), (dict(q=None), -1), (dict(ws=None), -4),
+    (dict(nbytes=16), -4), (dict(qd=math.inf), -1), (dict(vd=math.nan), -1),
+    (dict(scale=1e30, qd=1e30), -1), (dict(k=MIS), -3), (dict(ws=MIS), -3), (dict(causal=3), -1),
+])
+def test_fp8_forward_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert fp8(lib, **kw) == code
+
+
+def test_fp8_workspace_size_contract(lib):
+    # one transposed copy of V, keys padded to a multiple of 16
+    assert lib.fa_fwd_fp8_workspace_bytes(2, 3, 100, 128) >= 2 * 3 * 128 * 112
+    assert lib.fa_fwd_fp8_workspace_bytes(1, 1, 16, 128) >= 128 * 16
+    assert lib.fa_fwd_fp8_workspace_bytes(0, 1, 16, 128) == 0
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(d=96), -2), (dict(d=32), -2), (dict(N=0), -1), (dict(B=0), -1), (dict(H=-1), -1),
     (dict(q=None), -1), (dict(o=None), -1), (dict(dtype=5), -1), (dict(causal=2), -1),
