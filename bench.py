@@ -198,6 +198,39 @@ def profiled_traffic(kernel: str):
     return int(m.group(1))
 
 
+def fp8_forward_phase(fa, perfmodel, q, k, v, B, H, N, d, scale, causal, stream, args) -> dict:
+    """The e4m3 forward on the same workload: q, k, v quantised per tensor (descale = amax /
+    448) outside the timed region, then fa_fwd_fp8 (V transpose + tensor-core kernel) timed
+    with CUDA events on the launching stream over the same number of steps."""
+    import torch
+
+    def quantize(t):
+        ds = float(t.float().abs().max()) / 448.0 or 1.0
+        return (t.float() / ds).to(torch.float8_e4m3fn), ds
+
+    (q8, qd), (k8, kd), (v8, vd) = quantize(q), quantize(k), quantize(v)
+    o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse8 = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                      device=q.device)
+    run = lambda: fa.fa_fwd_fp8(q8, k8, v8, o8, lse8, scale, qd, kd, vd, causal, ws8, stream)  # noqa: E731
+    for _ in range(args.warmup):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_device_status(stream)
+    ms = e0.elapsed_time(e1) / args.steps
+    tflops = perfmodel.fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+    del q8, k8, v8, o8, lse8, ws8
+    return {"ms": round(ms, 4), "tflops": round(tflops, 2), "launches_per_step": 2,
+            "inputs": "the workload's q, k, v quantised to e4m3 per tensor (amax / 448)"}
+
+
 def run_gpu(args):
     import torch
 
@@ -325,6 +358,8 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(s0.elapsed_time(s1) / e2e_steps, dev)
     e2e_value = whole_job_tflops(f_fwd + f_bwd, ws, e2e_ms)
 
+    fp8 = fp8_forward_phase(fa, perfmodel, q, k, v, B, H, N, d, scale, w.causal, stream, args)
+
     peaks, peak_src = load_peaks()
     fwd_med = statistics.median(fwd_ms)
     bwd_med = statistics.median(bwd_ms)
@@ -368,6 +403,9 @@ def run_gpu(args):
             "kernel_ms": {k: round(v, 4) for k, v in kern_ms.items()},
             "kernel_tflops": {k: round(kern_flops[k] / (kern_ms[k] * 1e-3) / 1e12, 2)
                               for k in kern_flops},
+            "fp8_fwd": dict(fp8, frac_of_fp8_peak=round(
+                fp8["tflops"] / (2.0 * peaks.get("bf16_tflops", 1885.6)), 4),
+                fp8_peak="2 x measured bf16_tflops burst (the nominal fp8 / bf16 ratio)"),
         },
         "roofline": {
             "kernel": kern_names[dom_key],

@@ -64,3 +64,17 @@ def test_decode_wait_expires_and_context_survives(short_waits):
     o, lse = fa.forward_decode(q, k, v, cu_q, cu_k, 1, 500, causal=True, num_splits=2)
     fa.fa_device_status()
     assert torch.isfinite(o.float()).all()
+
+
+def test_fp8_forward_wait_expires_and_context_survives(short_waits):
+    from exact_attention_25_gb300.inputs import random_fp8
+
+    x = random_fp8(1, 2, 600, 128, seed=4)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    short_waits.fa_debug_set_flags(1)
+    fa.forward_fp8(q, k, v, causal=True)
+    _expect_timeout()
+    short_waits.fa_debug_set_flags(0)
+    o, lse = fa.forward_fp8(q, k, v, causal=True)
+    fa.fa_device_status()
+    assert torch.isfinite(o.float()).all()
