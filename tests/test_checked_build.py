@@ -123,6 +123,19 @@ def test_checked_matches_regular_bit_for_bit(checked, causal):
                 fa.fa_device_status()
         for a, b in zip(*res):
             assert torch.equal(a, b)
+    # the e4m3 forward
+    from exact_attention_25_gb300.inputs import random_fp8
+
+    z = random_fp8(2, 2, 300, 128, seed=6)
+    q8, k8, v8 = (z[n].cuda() for n in ("q", "k", "v"))
+    res = []
+    for path in (_lib.LIB_CHECKED_PATH, _lib.LIB_PATH):
+        with _lib.library(path):
+            res.append(fa.forward_fp8(q8, k8, v8, z["q_descale"], z["k_descale"], z["v_descale"],
+                                      causal=causal))
+            fa.fa_device_status()
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
 
 
 # (lens of the tensors, cu_q, cu_k, max_q, max_k): malformed offsets of several kinds

@@ -7,7 +7,8 @@
   * Standard-normal inputs quantised per tensor: |O - O_ref| within the oracle's rounding
     bound (sum_j max(2^-4 P_ij, 2^-10 max P_i) |V_jc|, derived from e4m3's spacing) plus bf16
     rounding of O and an accumulation allowance; lse within 1e-3 (its scores are exact).
-  * The bench-sized shape (B=2, H=32, N=8192, causal) on sampled rows, and determinism.
+  * Full-size shapes (B=2 H=32 N=8192 and the bench's B=1 H=32 N=32000, causal) on sampled
+    rows, and determinism.
 """
 import math
 
@@ -93,6 +94,27 @@ def test_bench_shape_sampled_rows_and_determinism():
                                   x["v_descale"], 128 ** -0.5, True, rows)
     o = o1.double().cpu().numpy()
     lse = lse1.double().cpu().numpy()
+    for n, (b, h, i) in enumerate(rows):
+        tol = (r["bound"][n] + 2.0 ** -8 * (np.abs(r["o"][n]) + r["bound"][n]) +
+               1e-4 * r["pv_abs"][n] + 1e-6)
+        assert np.all(np.abs(o[b, h, i] - r["o"][n]) <= tol), (b, h, i)
+        assert abs(lse[b, h, i] - r["lse"][n]) <= 1e-3, (b, h, i)
+
+
+def test_long_causal_sequence_sampled_rows():
+    """The bench's shape (B=1, H=32, N=32000, causal: up to 250 key blocks per query tile),
+    checked on sampled rows including the first and the last."""
+    B, H, N = 1, 32, 32000
+    x = random_fp8(B, H, N, 128, seed=5)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.forward_fp8(q, k, v, x["q_descale"], x["k_descale"], x["v_descale"],
+                            scale=128 ** -0.5, causal=True)
+    fa.fa_device_status()
+    rng = np.random.default_rng(1)
+    rows = [(0, int(rng.integers(H)), int(i)) for i in list(rng.integers(0, N, 16)) + [0, N - 1]]
+    r = oracle.attention_fp8_rows(x["q"], x["k"], x["v"], x["q_descale"], x["k_descale"],
+                                  x["v_descale"], 128 ** -0.5, True, rows)
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
     for n, (b, h, i) in enumerate(rows):
         tol = (r["bound"][n] + 2.0 ** -8 * (np.abs(r["o"][n]) + r["bound"][n]) +
                1e-4 * r["pv_abs"][n] + 1e-6)
