@@ -18,7 +18,7 @@ __all__ = [
     "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "forward_varlen",
     "backward_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
     "forward_decode", "fa_checked_build", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes",
-    "forward_fp8",
+    "forward_fp8", "fa_fwd_fp8_varlen", "fa_fwd_fp8_varlen_workspace_bytes", "forward_fp8_varlen",
 ]
 
 
@@ -173,6 +173,48 @@ def forward_fp8(q, k, v, q_descale: float = 1.0, k_descale: float = 1.0, v_desca
     ws = torch.empty(max(fa_fwd_fp8_workspace_bytes(B, H, N, d), 16), dtype=torch.uint8,
                      device=q.device)
     fa_fwd_fp8(q, k, v, o, lse, scale, q_descale, k_descale, v_descale, causal, ws, stream)
+    return o, lse
+
+
+def fa_fwd_fp8_varlen_workspace_bytes(B: int, max_seqlen_k: int, Hkv: int, d: int) -> int:
+    return int(load().fa_fwd_fp8_varlen_workspace_bytes(B, max_seqlen_k, Hkv, d))
+
+
+def fa_fwd_fp8_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                      max_seqlen_k: int, scale: float, q_descale: float, k_descale: float,
+                      v_descale: float, causal: bool, workspace, stream=None) -> None:
+    """C ``fa_fwd_fp8_varlen``: q [total_q, H, 128], k, v [total_k, Hkv, 128] e4m3 codes (any
+    1-byte dtype), o [total_q, H, 128] bf16, lse [H, total_q] fp32 or None, cu_seqlens_* int32
+    [B + 1] on the device."""
+    _check_tensors(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, workspace)
+    for t in (q, k, v):
+        if t.element_size() != 1:
+            raise ValueError("q, k and v must hold 1-byte e4m3 codes")
+    B, total_q, total_k, H, Hkv, d = _varlen_shapes(q, k, cu_seqlens_q, cu_seqlens_k)
+    nbytes = workspace.numel() * workspace.element_size()
+    check(load().fa_fwd_fp8_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B,
+        int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, H, Hkv, d, float(scale),
+        float(q_descale), float(k_descale), float(v_descale), int(bool(causal)), _ptr(workspace),
+        nbytes, _stream(stream)))
+
+
+def forward_fp8_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                       q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                       scale: float | None = None, causal: bool = False, stream=None):
+    """Allocate O (bf16), LSE and the workspace and run fa_fwd_fp8_varlen."""
+    import torch
+
+    total_q, H, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = d ** -0.5
+    B, Hkv = int(cu_seqlens_q.numel()) - 1, int(k.shape[1])
+    o = torch.empty((total_q, H, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(fa_fwd_fp8_varlen_workspace_bytes(B, max_seqlen_k, Hkv, d), 16),
+                     dtype=torch.uint8, device=q.device)
+    fa_fwd_fp8_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                      scale, q_descale, k_descale, v_descale, causal, ws, stream)
     return o, lse
 
 

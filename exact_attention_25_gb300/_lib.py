@@ -28,7 +28,8 @@ EXPORTS = (
     "fa_causal_block_counts", "fa_version", "fa_fwd_varlen", "fa_bwd_varlen_workspace_bytes",
     "fa_bwd_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
     "fa_fwd_varlen_strided", "fa_bwd_varlen_strided", "fa_fwd_gqa", "fa_bwd_gqa",
-    "fa_checked_build", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes",
+    "fa_checked_build", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_fwd_fp8_varlen",
+    "fa_fwd_fp8_varlen_workspace_bytes",
 )
 
 _lock = threading.Lock()
@@ -97,10 +98,15 @@ def load(path: str | None = None):
         lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_fwd_fp8_workspace_bytes.restype = sz
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, f, f, f, i, vp, sz, vp]
+        lib.fa_fwd_fp8_varlen_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_fwd_fp8_varlen_workspace_bytes.restype = sz
+        lib.fa_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f,
+                                          f, f, i, vp, sz, vp]
         for fn in ("fa_fwd", "fa_fwd_impl", "fa_bwd", "fa_bwd_impl", "fa_bwd_stage", "fa_device_status",
                    "fa_causal_block_counts", "fa_fwd_varlen", "fa_bwd_varlen", "fa_fwd_decode",
                    "fa_decode_num_splits", "fa_fwd_varlen_strided", "fa_bwd_varlen_strided",
-                   "fa_fwd_gqa", "fa_bwd_gqa", "fa_checked_build", "fa_fwd_fp8"):
+                   "fa_fwd_gqa", "fa_bwd_gqa", "fa_checked_build", "fa_fwd_fp8",
+                   "fa_fwd_fp8_varlen"):
             getattr(lib, fn).restype = ctypes.c_int
         if path is None:
             _lib = lib

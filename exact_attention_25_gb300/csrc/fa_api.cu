@@ -26,7 +26,8 @@ cudaError_t launch_decode(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           int num_sms);
 cudaError_t launch_fwd_fp8_tc(const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tvt, const FwdParams& p, cudaStream_t st);
-cudaError_t launch_vt_transpose(const void* v, void* vt, int BH, int N, int Npad, cudaStream_t st);
+cudaError_t launch_vt_transpose(const void* v, void* vt, const Layout& L, int Kpad, int* status,
+                                cudaStream_t st);
 
 // Device status word written by bounded waits that give up (0 = fine).
 __device__ int g_status_word;
@@ -930,14 +931,15 @@ namespace {
 
 long long fp8_pad_keys(int N) { return (static_cast<long long>(N) + 15) / 16 * 16; }
 
-// 3-D map of 8-bit codes, dimensions (x, y, z) with byte strides for y and z; box 128 x 128 x 1
-// (one 128-byte swizzle panel of 128 rows).
+// 3-D map of 8-bit codes, dimensions (x, y, z) with byte strides for y and z; box 128 bytes x
+// by_ x bz (128 rows of one 128-byte swizzle panel: by_ = 128, bz = 1, or bz = 128 rows along
+// z for tensors stored token by token).
 int make_map_u8(CUtensorMap* m, const void* base, cuuint64_t x, cuuint64_t y, cuuint64_t z,
-                cuuint64_t y_stride, cuuint64_t z_stride)
+                cuuint64_t y_stride, cuuint64_t z_stride, cuuint32_t by_ = 128, cuuint32_t bz = 1)
 {
     cuuint64_t dims[3] = {x, y, z};
     cuuint64_t strides[2] = {y_stride, z_stride};
-    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t box[3] = {128, by_, bz};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -998,7 +1000,69 @@ extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, 
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     p.debug_flags = g_debug_flags;
     p.L = fixed_layout(B, H, N, d);
-    cudaError_t e = fa::launch_vt_transpose(v, workspace, B * H, N, static_cast<int>(Npad), st);
+    cudaError_t e = fa::launch_vt_transpose(v, workspace, p.L, static_cast<int>(Npad), di->status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "V transpose launch");
+    e = fa::launch_fwd_fp8_tc(maps[0], maps[1], maps[2], p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "e4m3 forward launch");
+    return FA_OK;
+}
+
+extern "C" size_t fa_fwd_fp8_varlen_workspace_bytes(int B, int max_seqlen_k, int Hkv, int d)
+{
+    if (B < 1 || max_seqlen_k < 1 || Hkv < 1 || d < 1) return 0;
+    return align256(static_cast<size_t>(B) * Hkv * d * static_cast<size_t>(fp8_pad_keys(max_seqlen_k)));
+}
+
+extern "C" int fa_fwd_fp8_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                                 int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                                 int H, int Hkv, int d, float scale, float q_descale,
+                                 float k_descale, float v_descale, int causal, void* workspace,
+                                 size_t workspace_bytes, void* stream)
+{
+    int max_q = max_seqlen_q, max_k = max_seqlen_k;
+    int rc = check_varlen(cu_seqlens_q, cu_seqlens_k, B, &max_q, &max_k, total_q, total_k, H, Hkv,
+                          d, scale, causal);
+    if (rc) return rc;
+    if (d != 128) return fail(FA_ERR_UNSUPPORTED_D, "the e4m3 forward takes d = 128 only");
+    if (!finite(q_descale) || !finite(k_descale) || !finite(v_descale) ||
+        !finite(scale * q_descale * k_descale))
+        return fail(FA_ERR_INVALID_ARG, "descale factors (and their product with scale) must be finite");
+    if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA_ERR_MISALIGNED, "q, k, v, o must be 16-byte aligned (lse 4-byte)");
+    const long long Kpad = fp8_pad_keys(max_k);
+    if (static_cast<long long>(B) * Hkv * ((Kpad + 63) / 64) >= (1LL << 31))
+        return fail(FA_ERR_TOO_LARGE, "B * Hkv * ceil(max_seqlen_k / 64) must be < 2^31");
+    const size_t need = fa_fwd_fp8_varlen_workspace_bytes(B, max_k, Hkv, d);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
+    if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    if ((rc = get_encoder())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap maps[3];
+    // Q: (d, H, total_q), K: (d, Hkv, total_k) bytes, boxes of 128 tokens of one head;
+    // V^T: (Kpad keys, d, B*Hkv)
+    const cuuint64_t hq = static_cast<cuuint64_t>(H), hk = static_cast<cuuint64_t>(Hkv);
+    if ((rc = make_map_u8(&maps[0], q, 128, hq, static_cast<cuuint64_t>(total_q), 128, hq * 128, 1, 128)) ||
+        (rc = make_map_u8(&maps[1], k, 128, hk, static_cast<cuuint64_t>(total_k), 128, hk * 128, 1, 128)) ||
+        (rc = make_map_u8(&maps[2], workspace, static_cast<cuuint64_t>(Kpad), 128,
+                          static_cast<cuuint64_t>(B) * hk, static_cast<cuuint64_t>(Kpad),
+                          static_cast<cuuint64_t>(Kpad) * 128)))
+        return rc;
+    fa::FwdParams p{};
+    p.q = q; p.k = k; p.v = workspace; p.o = o; p.lse = lse;
+    p.N = total_q; p.BH = H; p.scale = scale;
+    p.scale_log2 = scale * q_descale * k_descale * fa::kLog2e;
+    p.v_descale = v_descale;
+    p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
+    p.debug_flags = g_debug_flags;
+    p.L = packed_layout(cu_seqlens_q, cu_seqlens_k, B, max_q, max_k, total_q, total_k, H, Hkv, d,
+                        packed_strides(H, Hkv, d));
+    cudaError_t e = fa::launch_vt_transpose(v, workspace, p.L, static_cast<int>(Kpad), di->status, st);
     if (e != cudaSuccess) return cuda_fail(e, "V transpose launch");
     e = fa::launch_fwd_fp8_tc(maps[0], maps[1], maps[2], p, st);
     if (e != cudaSuccess) return cuda_fail(e, "e4m3 forward launch");

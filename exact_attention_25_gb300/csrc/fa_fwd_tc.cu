@@ -16,10 +16,11 @@
 // [256 + 128t, 384 + 128t), whose column 64 accumulates the row sum of the bf16 P (the P V
 // product runs at N = 128 against V and a constant ones-column panel).
 //
-// The e4m3 variant (F8, d = 128, fixed-length square heads) runs the same schedule on 8-bit
-// operands with kind::f8f6f4 MMAs (K = 32 per MMA): Q and K tiles of 128 rows x 128 bytes,
-// P rounded to e4m3 (four per TMEM column, at columns [64, 96) of S_t), and V read from a
-// transposed copy V^T [d, keys] so that both operands of O += P V are K-major.  The
+// The e4m3 variant (F8, d = 128; fixed-length square heads or packed batches) runs the same
+// schedule on 8-bit operands with kind::f8f6f4 MMAs (K = 32 per MMA): Q and K tiles of 128
+// rows x 128 bytes, P rounded to e4m3 (four per TMEM column, at columns [64, 96) of S_t),
+// and V read from a transposed copy V^T [d, keys] per (sequence, key/value head) so that
+// both operands of O += P V are K-major.  The
 // descale factors of Q and K are folded into the softmax scale on the host; V's is applied
 // with 1/l in the epilogue.  O is normalised by the fp32 row sum l.
 #include <type_traits>
@@ -141,6 +142,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
     const int qhead = q_head_index<packed>(L, b, h);
     const int khead = k_head_index<packed>(L, b, general ? h / (L.H / L.Hkv) : h);
     const int shift = general ? nk - nq : 0;  // bottom-right causal alignment
+    // e4m3: the V^T matrix of this (sequence, key/value head)
+    const int vthead = b * L.Hkv + (general ? h / (L.H / L.Hkv) : h);
 
     // Key blocks visited by each query tile: a prefix 0..J_t-1 (under the causal mask, the
     // blocks whose first key some query of the tile sees).
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
                     // (watchdog test: the announced V tile never arrives)
                 } else if constexpr (F8) {
                     // V^T tile: the d rows of this head, keys [j BN, j BN + BN) (x in bytes)
-                    tma_load_3d_w(sV + s * C::TILE_BYTES, &tm_v, &bar_vfull[s], j * C::BN, 0, khead);
+                    tma_load_3d_w(sV + s * C::TILE_BYTES, &tm_v, &bar_vfull[s], j * C::BN, 0, vthead);
                 } else {
                     for (int pn = 0; pn < C::PANELS; ++pn)
                         tma_load_rows_w(sV + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v,
@@ -614,10 +617,12 @@ cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
     return d == 64 ? run(std::integral_constant<int, 64>{}) : run(std::integral_constant<int, 128>{});
 }
 
-// e4m3 forward: d = 128, fixed-length square heads; tvt maps the transposed V^T copy.
+// e4m3 forward, d = 128: fixed-length square heads or packed batches (grouped heads, Nq !=
+// Nk); tvt maps the transposed V^T copy.
 cudaError_t launch_fwd_fp8_tc(const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tvt, const FwdParams& p, cudaStream_t st)
 {
+    if (p.L.cu_q != nullptr) return launch_fwd_tc_impl<128, kModePacked, true>(tq, tk, tvt, p, st);
     return launch_fwd_tc_impl<128, kModeFixed, true>(tq, tk, tvt, p, st);
 }
 

@@ -164,3 +164,22 @@ def random_fp8(B: int, H: int, N: int, d: int, seed: int = 0, in_scale: float = 
     else:
         raise ValueError(f"unknown kind {kind!r}")
     return out
+
+
+def random_fp8_varlen(lens_q, lens_k, H: int, Hkv: int, d: int, seed: int = 0,
+                      in_scale: float = 1.0, kind: str = "normal") -> dict:
+    """Packed e4m3 batch: q [total_q, H, d], k and v [total_k, Hkv, d] drawn and quantised as
+    in random_fp8 (kind "normal" or "integer"), with the int32 offsets cu_q, cu_k ([B + 1],
+    CPU) of the sequence lengths ``lens_q`` / ``lens_k``."""
+    if len(lens_q) != len(lens_k):
+        raise ValueError("one query length and one key length per sequence")
+    cu_q = torch.tensor([0] + list(lens_q), dtype=torch.int64).cumsum(0).to(torch.int32)
+    cu_k = torch.tensor([0] + list(lens_k), dtype=torch.int64).cumsum(0).to(torch.int32)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    xq = random_fp8(1, 1, tq * H, d, seed=seed, in_scale=in_scale, kind=kind)
+    xk = random_fp8(1, 1, tk * Hkv, d, seed=seed + 1, in_scale=in_scale, kind=kind)
+    out = {"q": xq["q"].reshape(tq, H, d), "q_descale": xq["q_descale"],
+           "k": xk["k"].reshape(tk, Hkv, d), "k_descale": xk["k_descale"],
+           "v": xk["v"].reshape(tk, Hkv, d), "v_descale": xk["v_descale"],
+           "cu_q": cu_q, "cu_k": cu_k, "max_q": max(lens_q), "max_k": max(lens_k)}
+    return out

@@ -144,6 +144,26 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                int N, int d, float scale, float q_descale, float k_descale, float v_descale,
                int causal, void* workspace, size_t workspace_bytes, void* stream);
 
+/* e4m3 forward on packed variable-length batches with grouped key/value heads: what
+ * fa_fwd_fp8 computes, with the sequences, head grouping, bottom-right causal mask and
+ * empty-row rules of fa_fwd_varlen (see there).
+ *   - q [total_q, H, 128], k and v [total_k, Hkv, 128] e4m3 codes, contiguous; o
+ *     [total_q, H, 128] bf16; lse [H, total_q] fp32 (may be null); cu_seqlens_* int32 [B + 1]
+ *     on the device, read by the kernels (malformed offsets are clamped to the tensors).
+ *   - workspace: at least fa_fwd_fp8_varlen_workspace_bytes(B, max_seqlen_k, Hkv, d) bytes,
+ *     16-byte aligned; it receives V^T per (sequence, key/value head), each padded to
+ *     max_seqlen_k rounded up to 16 keys, so it grows with B * max_seqlen_k rather than
+ *     total_k.
+ *   - Errors as fa_fwd_varlen and fa_fwd_fp8, plus FA_ERR_TOO_LARGE when
+ *     B * Hkv * ceil(max_seqlen_k / 64) >= 2^31. */
+size_t fa_fwd_fp8_varlen_workspace_bytes(int B, int max_seqlen_k, int Hkv, int d);
+
+int fa_fwd_fp8_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int max_seqlen_q,
+                      int max_seqlen_k, int total_q, int total_k, int H, int Hkv, int d,
+                      float scale, float q_descale, float k_descale, float v_descale, int causal,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Packed variable-length batches with grouped key/value heads (bf16, tensor-core path).
  *
  * What it computes.  B independent sequences; sequence b has the query rows

@@ -329,3 +329,45 @@ def attention_fp8_rows(q8, k8, v8, q_descale: float, k_descale: float, v_descale
         out["bound"].append(w @ np.abs(vv))
         out["pv_abs"].append(P @ np.abs(vv))
     return {key: np.array(val) for key, val in out.items()}
+
+
+def attention_fp8_varlen(q8, k8, v8, cu_seqlens_q, cu_seqlens_k, q_descale: float,
+                         k_descale: float, v_descale: float, scale: float, causal: bool):
+    """attention_fp8 for a packed batch with grouped key/value heads: the sequences, the head
+    mapping h -> h // (H // Hkv) and the bottom-right causal mask (query i of a sequence with
+    nq queries and nk keys sees key j iff j <= i + nk - nq) of attention_varlen.  Algorithm 0
+    per (sequence, head) with S and P materialised in float64; a row that sees no key has
+    O = 0, lse = -inf and bound 0.  Returns dict o, bound, pv_abs ``[total_q, H, d]`` and lse
+    ``[H, total_q]``."""
+    q = e4m3_decode(_codes(q8)) * float(q_descale)
+    k = e4m3_decode(_codes(k8)) * float(k_descale)
+    v = e4m3_decode(_codes(v8)) * float(v_descale)
+    cu_q = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    total_q, H, d = q.shape
+    G = H // k.shape[1]
+    out = {"o": np.zeros((total_q, H, d)), "lse": np.full((H, total_q), -np.inf),
+           "bound": np.zeros((total_q, H, d)), "pv_abs": np.zeros((total_q, H, d))}
+    for b in range(len(cu_q) - 1):
+        qs, ks = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        nq, nk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        if nq == 0 or nk == 0:
+            continue
+        seen = np.ones((nq, nk), dtype=bool)
+        if causal:
+            seen = np.arange(nk)[None, :] <= np.arange(nq)[:, None] + (nk - nq)
+        live = seen.any(axis=1)
+        for h in range(H):
+            vv = v[ks, h // G]
+            S = np.where(seen, scale * (q[qs, h] @ k[ks, h // G].T), -np.inf)
+            m = np.where(live, S.max(axis=1, initial=-np.inf), 0.0)
+            e = np.where(seen, np.exp(S - m[:, None]), 0.0)
+            tot = e.sum(axis=1)
+            P = np.divide(e, tot[:, None], out=np.zeros_like(e), where=live[:, None])
+            w = np.maximum(P / 16.0, P.max(axis=1, keepdims=True) / 1024.0) * seen
+            rows = np.arange(cu_q[b], cu_q[b + 1])
+            out["o"][rows, h] = P @ vv
+            out["lse"][h, rows] = np.where(live, m + np.log(np.where(live, tot, 1.0)), -np.inf)
+            out["bound"][rows, h] = w @ np.abs(vv)
+            out["pv_abs"][rows, h] = P @ np.abs(vv)
+    return out

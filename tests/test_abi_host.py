@@ -74,6 +74,27 @@ def test_fp8_forward_rejects_bad_arguments_before_any_launch(lib, kw, code):
     assert fp8(lib, **kw) == code
 
 
+def fp8_varlen(lib, cu_q=A, cu_k=A, B=2, max_q=64, max_k=64, total_q=100, total_k=100, H=4,
+               Hkv=2, d=128, ws=A, nbytes=1 << 24, qd=1.0):
+    f = ctypes.c_float
+    return lib.fa_fwd_fp8_varlen(A, A, A, A2, A2, cu_q, cu_k, B, max_q, max_k, total_q, total_k,
+                                 H, Hkv, d, f(0.1), f(qd), f(1.0), f(1.0), 0, ws, nbytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), -2), (dict(B=0), -1), (dict(cu_q=None), -1), (dict(H=3), -1),
+    (dict(ws=None), -4), (dict(nbytes=256), -4), (dict(qd=math.inf), -1), (dict(ws=MIS), -3),
+])
+def test_fp8_varlen_forward_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert fp8_varlen(lib, **kw) == code
+
+
+def test_fp8_varlen_workspace_size_contract(lib):
+    # V^T per (sequence, key/value head), keys padded to 16
+    assert lib.fa_fwd_fp8_varlen_workspace_bytes(3, 100, 2, 128) >= 3 * 2 * 128 * 112
+    assert lib.fa_fwd_fp8_varlen_workspace_bytes(0, 100, 2, 128) == 0
+
+
 def test_fp8_workspace_size_contract(lib):
     # one transposed copy of V, keys padded to a multiple of 16
     assert lib.fa_fwd_fp8_workspace_bytes(2, 3, 100, 128) >= 2 * 3 * 128 * 112

@@ -162,6 +162,30 @@ def test_malformed_offsets_stay_inside_the_buffers(checked, case, causal):
         run_packed(x, cu_q, cu_k, max_q, max_k, causal, splits)
 
 
+@pytest.mark.parametrize("case", MALFORMED, ids=[c[0] for c in MALFORMED])
+def test_malformed_offsets_e4m3_stay_inside_the_buffers(checked, case):
+    """The packed e4m3 forward (its V transpose reads through the same clamped offsets)."""
+    from exact_attention_25_gb300.inputs import random_fp8_varlen
+
+    _, Tq, Tk, cq, ck, max_q, max_k = case
+    B = len(cq) - 1
+    x = random_fp8_varlen([Tq] + [0] * (B - 1), [Tk] + [0] * (B - 1), 4, 2, 128, seed=Tq)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    cu_q = torch.tensor(cq, dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(ck, dtype=torch.int32, device="cuda")
+    obuf, o = guarded((Tq, 4, 128), torch.bfloat16)
+    lflat, lse = guarded_lse(4, Tq)
+    need = fa.fa_fwd_fp8_varlen_workspace_bytes(B, max_k, 2, 128)
+    wbuf = torch.full((need + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    for causal in (False, True):
+        fa.fa_fwd_fp8_varlen(q, k, v, o, lse, cu_q, cu_k, max_q, max_k, 0.1, 1.0, 1.0, 1.0,
+                             causal, wbuf)
+        fa.fa_device_status()
+    assert_guards_intact(obuf, "o")
+    assert_flat_guards_intact(lflat, "lse")
+    assert (wbuf[need:] == 0xA5).all(), "write past the workspace"
+
+
 def expect_out_of_bounds(call):
     call()
     with pytest.raises(fa.FaError) as ei:

@@ -118,3 +118,41 @@ def test_bound_needs_its_subnormal_term():
     full = np.maximum(P / 16.0, P.max() / 1024.0) @ np.abs(v)
     assert np.all(err <= full)
     assert np.any(err > (P / 16.0) @ np.abs(v))
+
+
+def _dec(t, s):
+    return oracle.e4m3_decode(oracle._codes(t)) * s
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_e4m3_oracle_matches_the_c_oracle(causal):
+    """The packed e4m3 oracle (numpy, per sequence and head) against the C oracle's
+    attention_varlen on the decoded values: two implementations of the same definition,
+    including grouped heads, Nq != Nk in both directions and empty sequences."""
+    from exact_attention_25_gb300.inputs import random_fp8_varlen
+
+    x = random_fp8_varlen([3, 0, 40, 7, 12], [5, 9, 30, 0, 12], 4, 2, 128, seed=1)
+    r = oracle.attention_fp8_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"],
+                                    x["q_descale"], x["k_descale"], x["v_descale"], 0.09, causal)
+    ref = oracle.attention_varlen(_dec(x["q"], x["q_descale"]), _dec(x["k"], x["k_descale"]),
+                                  _dec(x["v"], x["v_descale"]), x["cu_q"], x["cu_k"], 0.09, causal)
+    assert np.allclose(r["o"], ref["o"], rtol=0, atol=1e-12)
+    assert np.array_equal(np.isneginf(r["lse"]), np.isneginf(ref["lse"]))
+    fin = np.isfinite(ref["lse"])
+    assert np.allclose(r["lse"][fin], ref["lse"][fin], rtol=0, atol=1e-12)
+
+
+def test_packed_e4m3_oracle_reduces_to_the_fixed_one():
+    """One square sequence with as many key/value heads as query heads is the fixed-length
+    problem: o, lse, bound and pv_abs agree with attention_fp8."""
+    from exact_attention_25_gb300.inputs import random_fp8_varlen
+
+    x = random_fp8_varlen([50], [50], 3, 3, 128, seed=2)
+    r = oracle.attention_fp8_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"],
+                                    x["q_descale"], x["k_descale"], x["v_descale"], 0.1, True)
+    f = oracle.attention_fp8(x["q"].permute(1, 0, 2)[None], x["k"].permute(1, 0, 2)[None],
+                             x["v"].permute(1, 0, 2)[None], x["q_descale"], x["k_descale"],
+                             x["v_descale"], 0.1, True)
+    for name in ("o", "bound", "pv_abs"):
+        assert np.allclose(r[name], f[name][0].transpose(1, 0, 2), rtol=1e-12, atol=1e-14), name
+    assert np.allclose(r["lse"], f["lse"][0], rtol=1e-12, atol=1e-12)
