@@ -42,6 +42,8 @@ def main():
     a = ap.parse_args()
     if a.Hkv and a.decode:
         return run_decode(a)
+    if a.Hkv and a.dtype == "fp8":
+        return run_packed_fp8(a)
     if a.Hkv:
         return run_packed(a)
     if a.dtype == "fp8":
@@ -177,6 +179,43 @@ def run_fp8(a):
     fl = perfmodel.fwd_flops(*shape, a.causal)
     print(f"fwd fp8 B={a.B} H={a.H} N={a.N} d={a.d} causal={a.causal}: {ms:.4f} ms "
           f"{fl / ms / 1e9:.1f} TFLOP/s (transpose + forward)")
+
+
+def run_packed_fp8(a):
+    """The packed e4m3 forward on the batch of run_packed (B sequences of N keys, the last Nq
+    positions as queries, H query heads over Hkv key/value heads), unit descale factors."""
+    import torch
+
+    import exact_attention_25_gb300 as fa
+
+    nq = a.Nq or a.N
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    mk = lambda rows, heads: torch.randn((rows, heads, a.d), generator=g, device="cuda").to(  # noqa: E731
+        torch.float8_e4m3fn)
+    q, k, v = mk(a.B * nq, a.H), mk(a.B * a.N, a.Hkv), mk(a.B * a.N, a.Hkv)
+    cu_q = torch.arange(0, a.B * nq + 1, nq, dtype=torch.int32, device="cuda")
+    cu_k = torch.arange(0, a.B * a.N + 1, a.N, dtype=torch.int32, device="cuda")
+    o = torch.empty((a.B * nq, a.H, a.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((a.H, a.B * nq), device="cuda", dtype=torch.float32)
+    ws = torch.empty(fa.fa_fwd_fp8_varlen_workspace_bytes(a.B, a.N, a.Hkv, a.d), dtype=torch.uint8,
+                     device="cuda")
+    run = lambda: fa.fa_fwd_fp8_varlen(q, k, v, o, lse, cu_q, cu_k, nq, a.N, a.d ** -0.5,  # noqa: E731
+                                       1.0, 1.0, 1.0, a.causal, ws)
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    fa.fa_device_status()
+    ms = e0.elapsed_time(e1) / a.iters
+    pairs = nq * a.N if not a.causal else sum(min(a.N, i + a.N - nq + 1) for i in range(nq))
+    fl = 4.0 * a.B * a.H * pairs * a.d
+    print(f"fwd fp8 packed B={a.B} H={a.H} Hkv={a.Hkv} Nq={nq} Nk={a.N} d={a.d} "
+          f"causal={a.causal}: {ms:.4f} ms {fl / ms / 1e9:.1f} TFLOP/s (transpose + forward)")
 
 
 def run_decode(a):

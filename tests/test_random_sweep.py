@@ -109,3 +109,29 @@ def test_random_fixed_length_problem(seed):
 
     check_fwd(o, lse, ref["o"], ref["lse"], torch.bfloat16, what, check_mean=N > 1)
     check_grads({"dq": dq, "dk": dk, "dv": dv}, ref, torch.bfloat16, what)
+
+
+@pytest.mark.parametrize("seed", range(max(1, N_CASES // 4)))
+def test_random_packed_e4m3_problem(seed):
+    """The packed e4m3 forward on the same kind of random batches (d = 128), within the
+    oracle's per-element rounding bound."""
+    from exact_attention_25_gb300.inputs import random_fp8_varlen
+
+    lens_q, lens_k, H, Hkv, _, causal, _ = draw_case(7000 + seed)
+    x = random_fp8_varlen(lens_q, lens_k, H, Hkv, 128, seed=seed,
+                          in_scale=float(np.random.default_rng(seed).choice([0.3, 1.0, 3.0])))
+    dev = {n: x[n].cuda() for n in ("q", "k", "v", "cu_q", "cu_k")}
+    scale = 128 ** -0.5
+    o, lse = fa.forward_fp8_varlen(dev["q"], dev["k"], dev["v"], dev["cu_q"], dev["cu_k"],
+                                   x["max_q"], x["max_k"], x["q_descale"], x["k_descale"],
+                                   x["v_descale"], scale=scale, causal=causal)
+    fa.fa_device_status()
+    r = oracle.attention_fp8_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"],
+                                    x["q_descale"], x["k_descale"], x["v_descale"], scale, causal)
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    tol = r["bound"] + 2.0 ** -8 * (np.abs(r["o"]) + r["bound"]) + 1e-4 * r["pv_abs"] + 1e-6
+    what = f"seed={seed} lens_q={lens_q} lens_k={lens_k} H={H} Hkv={Hkv} causal={causal}"
+    assert np.all(np.abs(o - r["o"]) <= tol), what
+    assert np.array_equal(np.isneginf(lse), np.isneginf(r["lse"])), what
+    fin = np.isfinite(r["lse"])
+    assert np.abs(lse[fin] - r["lse"][fin]).max(initial=0.0) <= 1e-3, what
