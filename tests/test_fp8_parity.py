@@ -134,3 +134,15 @@ def test_fp8_argument_errors():
     with pytest.raises(fa.FaError) as ei:
         fa.fa_fwd_fp8(q, k, v, o, None, 0.1, math.inf, 1.0, 1.0, False, ws)
     assert ei.value.code == -1
+
+
+def test_fp8_without_lse_gives_the_same_o():
+    x = random_fp8(1, 2, 300, 128, seed=9)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    args = (x["q_descale"], x["k_descale"], x["v_descale"])
+    o_ref, _ = fa.forward_fp8(q, k, v, *args, causal=True)
+    o = torch.empty_like(o_ref)
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(1, 2, 300, 128), dtype=torch.uint8, device="cuda")
+    fa.fa_fwd_fp8(q, k, v, o, None, 128 ** -0.5, *args, True, ws)
+    fa.fa_device_status()
+    assert torch.equal(o, o_ref)
