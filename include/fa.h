@@ -297,9 +297,11 @@ void fa_set_wait_limit_ns(unsigned long long ns);
 void fa_debug_set_flags(int flags);
 
 /* 1 if this library is the checked build (libfa_checked.so, compiled with FA_CHECKED), else 0.
- * A checked build tests every element the kernels read or write directly in global memory
- * (outputs, gradients, statistics, decode partials; tiles moved by TMA are bounded by their
- * tensor maps) against the extent of its buffer implied by the call's sizes and strides:
+ * A checked build tests every element that the tensor-core, decode, backward-preprocess and
+ * e4m3-transpose kernels read or write directly in global memory (outputs, gradients,
+ * statistics, decode partials, V and its transposed copy; tiles moved by TMA are bounded by
+ * their tensor maps; the fp32 SIMT kernels index only from their grid and take no offsets)
+ * against the extent of its buffer implied by the call's sizes and strides:
  * an access outside it is skipped and fa_device_status() then returns FA_ERR_OUT_OF_BOUNDS.
  * Its results are otherwise identical to the regular build's.  With fa_debug_set_flags(2)
  * the checked build takes every extent one row short, so the check must fire (test hook). */
