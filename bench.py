@@ -319,7 +319,14 @@ def run_gpu(args):
     s_out = torch.cuda.Stream(device=dev)
 
     def e2e_run(n):
-        ev_in = [torch.cuda.Event() for _ in range(n)]
+        """n pipelined steps.  Each step's copies are split along the order in which the path
+        needs and produces the tensors: the forward starts once q, k and v have landed (dO
+        arrives during it), O and LSE go back while the backward runs, dK and dV while dQ is
+        computed, dQ last."""
+        ev_qkv = [torch.cuda.Event() for _ in range(n)]
+        ev_do = [torch.cuda.Event() for _ in range(n)]
+        ev_fwd = [torch.cuda.Event() for _ in range(n)]
+        ev_dkv = [torch.cuda.Event() for _ in range(n)]
         ev_comp = [torch.cuda.Event() for _ in range(n)]
         ev_out = [torch.cuda.Event() for _ in range(n)]
         for i in range(n):
@@ -327,19 +334,33 @@ def run_gpu(args):
             if i >= 2:
                 s_in.wait_event(ev_comp[i - 2])  # this set's inputs are no longer read
             with torch.cuda.stream(s_in):
-                for dst, src in ((bq, hq), (bk, hk), (bv, hv), (bdo, hdo)):
+                for dst, src in ((bq, hq), (bk, hk), (bv, hv)):
                     dst.copy_(src, non_blocking=True)
-            ev_in[i].record(s_in)
-            stream.wait_event(ev_in[i])
+                ev_qkv[i].record(s_in)
+                bdo.copy_(hdo, non_blocking=True)
+                ev_do[i].record(s_in)
+            stream.wait_event(ev_qkv[i])
             if i >= 2:
                 stream.wait_event(ev_out[i - 2])  # this set's results have been copied out
             fa.fa_fwd(bq, bk, bv, bo, blse, scale, w.causal, stream)
-            fa.fa_bwd(bq, bk, bv, bo, bdo, blse, bdq, bdk, bdv, scale, w.causal, wsp, stream)
+            ev_fwd[i].record(stream)
+            stream.wait_event(ev_do[i])
+            for st in range(2):  # preprocess, then dK/dV
+                fa.fa_bwd_stage(bq, bk, bv, bo, bdo, blse, bdq, bdk, bdv, scale, w.causal, wsp, st,
+                                stream)
+            ev_dkv[i].record(stream)
+            fa.fa_bwd_stage(bq, bk, bv, bo, bdo, blse, bdq, bdk, bdv, scale, w.causal, wsp, 2,
+                            stream)
             ev_comp[i].record(stream)
-            s_out.wait_event(ev_comp[i])
             with torch.cuda.stream(s_out):
-                for dst, src in ((ho, bo), (hlse, blse), (hdq, bdq), (hdk, bdk), (hdv, bdv)):
+                s_out.wait_event(ev_fwd[i])
+                for dst, src in ((ho, bo), (hlse, blse)):
                     dst.copy_(src, non_blocking=True)
+                s_out.wait_event(ev_dkv[i])
+                for dst, src in ((hdk, bdk), (hdv, bdv)):
+                    dst.copy_(src, non_blocking=True)
+                s_out.wait_event(ev_comp[i])
+                hdq.copy_(bdq, non_blocking=True)
             ev_out[i].record(s_out)
         return ev_out[-1]
 
@@ -422,7 +443,9 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "pinned_host_memory": host_node,
                 "overlap": "step i+1's host->device and step i-1's device->host copies run on "
-                           "their own streams while step i computes (two device buffer sets)"},
+                           "their own streams while step i computes (two device buffer sets); "
+                           "within a step the forward starts once q, k, v have landed, O and "
+                           "LSE are copied back during the backward and dK, dV during dQ"},
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
     }
