@@ -42,13 +42,20 @@ class FaError(RuntimeError):
         self.code = code
 
 
+def default_path() -> str:
+    """libfa.so, or the bounds-checked libfa_checked.so when the environment sets
+    FA_CHECKED=1 (every call then reports out-of-range accesses through fa_device_status)."""
+    return LIB_CHECKED_PATH if os.environ.get("FA_CHECKED") == "1" else LIB_PATH
+
+
 def load(path: str | None = None):
-    """Load libfa.so (built by ``exact_attention_25_gb300.build``); raise if absent."""
+    """Load the library (built by ``exact_attention_25_gb300.build``; see default_path);
+    raise if absent."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or LIB_PATH
+        p = path or default_path()
         if not os.path.exists(p):
             raise FileNotFoundError(
                 f"{p} is missing: build it with exact_attention_25_gb300.build.build() "

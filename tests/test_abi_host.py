@@ -18,7 +18,7 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 @pytest.fixture(scope="module")
 def lib():
     build.build()
-    return _lib.load()
+    return _lib.load(_lib.LIB_PATH)  # the regular library, whatever FA_CHECKED says
 
 
 def declared_functions():
