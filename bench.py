@@ -198,6 +198,51 @@ def profiled_traffic(kernel: str):
     return int(m.group(1))
 
 
+def workload_config(w, ws: int) -> dict:
+    """The `config` object of both arms' JSON lines: the workload the metric is quoted on."""
+    return {
+        "workload": f"long-sequence causal attention forward+backward, B={w.B} H={w.H} "
+                    f"N={w.N} d={w.d} bf16",
+        "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": bool(w.causal), "scale": w.scale,
+        "l2": "inputs (262 MB per tensor) larger than the 129 MB L2; no flush",
+        "parallelism": f"replicas{ws}" if ws > 1 else "single GPU",
+    }
+
+
+def roofline_entry(kernel: str, achieved_tflops: float, peaks: dict, peak_src: str,
+                   traffic) -> dict:
+    """Roofline object of the dominant kernel.  `frac` is against the measured burst bf16
+    peak (the timed region is well under a second); `frac_sustained` against the measured
+    sustained (power-capped) figure, for comparison."""
+    peak = peaks.get("bf16_tflops", 1885.6)
+    sustained = peaks.get("bf16_tflops_sustained")
+    out = {
+        "kernel": kernel,
+        "bound": "tensor",
+        "achieved": round(achieved_tflops, 2),
+        "peak": peak,
+        "peak_kind": f"bf16_tflops burst ({peak_src})",
+        "unit": "TFLOP/s",
+        "frac": round(achieved_tflops / peak, 4),
+        "traffic": traffic,
+        "traffic_unit": "DRAM bytes per launch (ncu, full-size workload)",
+    }
+    if sustained:
+        out["peak_sustained"] = sustained
+        out["frac_sustained"] = round(achieved_tflops / sustained, 4)
+    return out
+
+
+def oracle_full_step_seconds(w, tflops: float) -> float:
+    """Seconds the oracle would take for one whole step of workload `w` (forward + backward
+    of every head at full length) at the rate `tflops` it reached on its sample."""
+    from exact_attention_25_gb300 import perfmodel
+
+    flops = (perfmodel.fwd_flops(w.B, w.H, w.N, w.d, w.causal) +
+             perfmodel.bwd_flops(w.B, w.H, w.N, w.d, w.causal))
+    return flops / (tflops * 1e12)
+
+
 def fp8_forward_phase(fa, perfmodel, q, k, v, B, H, N, d, scale, causal, stream, args) -> dict:
     """The e4m3 forward on the same workload: q, k, v quantised per tensor (descale = amax /
     448) outside the timed region, then fa_fwd_fp8 (V transpose + tensor-core kernel) timed
@@ -395,9 +440,6 @@ def run_gpu(args):
                   "bwd_dq": "fa_bwd_dq_tc_kernel<128>"}
     dom_key = max(kern_flops, key=lambda k: kern_ms[k])
     dom_tflops = kern_flops[dom_key] / (kern_ms[dom_key] * 1e-3) / 1e12
-    # Denominator: the measured burst bf16 peak.  The timed region is well under a second
-    # and the clocks stay at their maximum (see "clocks"), the burst condition.
-    peak = peaks.get("bf16_tflops", 1885.6)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -411,12 +453,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
-        "config": {
-            "workload": "long-sequence causal attention forward+backward, B=1 H=32 N=32000 d=128 bf16",
-            "B": B, "H": H, "N": N, "d": d, "causal": True, "scale": scale,
-            "l2": "inputs (262 MB per tensor) larger than the 129 MB L2; no flush",
-            "parallelism": f"replicas{ws}" if ws > 1 else "single GPU",
-        },
+        "config": workload_config(w, ws),
         "phases": {
             "fwd_ms": round(fwd_med, 4), "fwd_tflops": round(fwd_tflops, 2),
             "bwd_ms": round(bwd_med, 4), "bwd_tflops": round(bwd_tflops, 2),
@@ -428,17 +465,8 @@ def run_gpu(args):
                 fp8["tflops"] / (2.0 * peaks.get("bf16_tflops", 1885.6)), 4),
                 fp8_peak="2 x measured bf16_tflops burst (the nominal fp8 / bf16 ratio)"),
         },
-        "roofline": {
-            "kernel": kern_names[dom_key],
-            "bound": "tensor",
-            "achieved": round(dom_tflops, 2),
-            "peak": peak,
-            "peak_kind": f"bf16_tflops burst ({peak_src})",
-            "unit": "TFLOP/s",
-            "frac": round(dom_tflops / peak, 4),
-            "traffic": profiled_traffic(kern_names[dom_key]),
-            "traffic_unit": "DRAM bytes per launch (ncu, full-size workload)",
-        },
+        "roofline": roofline_entry(kern_names[dom_key], dom_tflops, peaks, peak_src,
+                                   profiled_traffic(kern_names[dom_key])),
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "pinned_host_memory": host_node,
@@ -492,8 +520,10 @@ def cpu_baseline(target_s: float = 15.0) -> dict:
     el = time.perf_counter() - t
     flops = reps * (perfmodel.fwd_flops(1, heads, n_s, w.d, True) +
                     perfmodel.bwd_flops(1, heads, n_s, w.d, True))
-    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+    tflops = flops / el / 1e12
+    return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": round(el, 3),
+            "full_step_seconds_extrapolated": round(oracle_full_step_seconds(w, tflops), 1),
             "sample": f"{reps} x fp64 oracle forward+backward of the first {n_s} tokens of {heads} "
                       f"heads (causal prefix, d=128) of the workload; FLOPs by the causal "
                       f"convention"}
@@ -532,11 +562,11 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "long-sequence causal attention forward+backward, B=1 H=32 N=32000 "
-                               "d=128 (bounded CPU sample)", "B": 1, "H": heads, "N": n_s, "d": w.d,
-                   "causal": True},
+        "config": workload_config(w, ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample,
+                         "full_step_seconds_extrapolated":
+                             round(oracle_full_step_seconds(w, value), 1)},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
