@@ -16,13 +16,14 @@
 // TMEM: S^T [0, 128), dP^T [128, 256), acc dV [256, 256 + d), acc dK [256 + d, 256 + 2d).  The
 // elementwise pass of block i runs in two phases.  Phase 1 loads warpgroup h's 64 columns of
 // S^T, computes P^T and writes it as bf16 pairs over the first 32 of them; phase 2 loads dP^T,
-// computes dS^T and writes it likewise into the dP^T buffer.  Issue order, block i
-// (tcgen05.mma operations of one CTA execute in issue order, so a product that overwrites a
-// buffer runs after the one that reads it):
-//   wait P^T(i) | dV += P^T(i) dO_i | S^T(i+1) -> S buffer |
-//   wait dS^T(i) | dK += dS^T(i) Q_i | dP^T(i+1) -> dP buffer
-// so the dV product starts as soon as phase 1 is done, and phase 1 of block i+1 overlaps
-// dK(i) and dP^T(i+1) on the pipe.  Q_i is read by S^T(i) and last by dK(i) (3-stage ring);
+// computes dS^T and writes it likewise into the dP^T buffer.  Each phase writes its results in
+// two halves of 32 query columns per warpgroup and signals each half on its own barrier (all
+// eight warps arrive).  Issue order, block i (tcgen05.mma operations of one CTA execute in
+// issue order, so a product that overwrites a buffer runs after the one that reads it):
+//   wait P^T(i) half 0 | dV += (half 0) | wait half 1 | dV += (half 1) | S^T(i+1) -> S buffer |
+//   wait dS^T(i) half 0 | dK += (half 0) | wait half 1 | dK += (half 1) | dP^T(i+1) -> dP buffer
+// so the dV product starts while the second half of phase 1 is computed, and phase 1 of
+// block i+1 overlaps dK(i) and dP^T(i+1) on the pipe.  Q_i is read by S^T(i) and last by dK(i) (3-stage ring);
 // dO_i by dP^T(i) and last by dV(i) (2 stages).
 #include <type_traits>
 
@@ -56,15 +57,20 @@ __device__ __forceinline__ void dkv_issue_nt(uint32_t d_tmem, uint64_t adesc, ui
     }
 }
 
-// acc += (bf16 pairs in TMEM buffer `buf`) * (MN-major 128-row tile): 8 k-steps of 16 streamed
-// rows; warpgroup h's pairs of rows [64h, 64h+64) sit at buf + 64h + [0, 32).
-__device__ __forceinline__ void dkv_issue_acc(uint32_t acc, uint32_t buf, uint64_t bdesc,
-                                              uint32_t idesc, bool first)
+// acc += (bf16 pairs in TMEM buffer `buf`) * (MN-major 128-row tile), one half of the 8 k-steps
+// of 16 streamed rows: warpgroup h's pairs of rows [64h, 64h+64) sit at buf + 64h + [0, 32), and
+// HALF selects rows [64h + 32 HALF, 64h + 32 HALF + 32) of both warpgroups (k-steps 2 HALF,
+// 2 HALF + 1, 4 + 2 HALF, 5 + 2 HALF), the columns each warpgroup finishes in that half.
+template <int HALF>
+__device__ __forceinline__ void dkv_issue_acc_half(uint32_t acc, uint32_t buf, uint64_t bdesc,
+                                                   uint32_t idesc, bool first)
 {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
+    for (int j = 0; j < 4; ++j) {
+        const int ks = (j < 2 ? 0 : 4) + 2 * HALF + (j & 1);
         mma_ts_w(acc, buf + (ks < 4 ? 8u * ks : 64u + 8u * (ks - 4)), sdesc_adv(bdesc, ks * 2048),
                  idesc, (first && ks == 0) ? 0u : 1u);
+    }
 }
 
 template <int D, int MODE>
@@ -90,8 +96,8 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_gempty[C::GSTAGES];
     __shared__ __align__(8) uint64_t bar_s;     // S^T of the next block landed
     __shared__ __align__(8) uint64_t bar_dp;    // dP^T of the next block landed
-    __shared__ __align__(8) uint64_t bar_p[2];  // warpgroup h wrote its P^T
-    __shared__ __align__(8) uint64_t bar_e[2];  // warpgroup h wrote its dS^T
+    __shared__ __align__(8) uint64_t bar_p[2];  // both warpgroups wrote half x of their P^T
+    __shared__ __align__(8) uint64_t bar_e[2];  // both warpgroups wrote half x of their dS^T
     __shared__ __align__(8) uint64_t bar_acc;   // accumulators final
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ __align__(16) float sL2[2][64];  // -L2 per query column [warpgroup][col]
@@ -140,9 +146,9 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         }
         mbar_init(&bar_s, 1);
         mbar_init(&bar_dp, 1);
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(&bar_p[h], 4);  // one elected arrive per warp of the warpgroup
-            mbar_init(&bar_e[h], 4);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bar_p[x], 8);  // one elected arrive per elementwise warp
+            mbar_init(&bar_e[x], 8);
         }
         mbar_init(&bar_acc, 1);
         mbar_init(&bar_drain, 1);
@@ -240,9 +246,16 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             mma_commit_w(&bar_dp);
             return true;
         };
-        auto wait_pair = [&](uint64_t* bars, int it) {
-            return warp_wait_all(&bars[0], it & 1, wd, kSiteBwdMmaDS) &&
-                   warp_wait_all(&bars[1], it & 1, wd, kSiteBwdMmaDS);
+        // acc += (TMEM operand) * (MN-major tile), each half issued as soon as both warpgroups
+        // have written it
+        auto do_acc = [&](uint64_t* bars, int it, uint32_t acc, uint32_t buf, uint64_t bdesc) {
+            if (!warp_wait_all(&bars[0], it & 1, wd, kSiteBwdMmaDS)) return false;
+            tc_fence_after();
+            dkv_issue_acc_half<0>(acc, buf, bdesc, kIdAcc, it == 0);
+            if (!warp_wait_all(&bars[1], it & 1, wd, kSiteBwdMmaDS)) return false;
+            tc_fence_after();
+            dkv_issue_acc_half<1>(acc, buf, bdesc, kIdAcc, it == 0);
+            return true;
         };
 
         bool ok = warp_wait_all(&bar_res, 0, wd, kSiteBwdMmaKV);
@@ -250,16 +263,18 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         if (ok && n_it > 0) ok = do_s(0) && do_dp(0);
         for (int it = 0; ok && it < n_it; ++it) {
             // dV += P^T(it) dO_it, then S^T(it + 1) over the P^T it just read
-            if (!wait_pair(bar_p, it)) { ok = false; break; }
-            tc_fence_after();
-            dkv_issue_acc(tDV, tS, sdesc_adv(mG0, (it % C::GSTAGES) * C::TILE_BYTES), kIdAcc, it == 0);
+            if (!do_acc(bar_p, it, tDV, tS, sdesc_adv(mG0, (it % C::GSTAGES) * C::TILE_BYTES))) {
+                ok = false;
+                break;
+            }
             mma_commit_w(&bar_gempty[it % C::GSTAGES]);
             committed_g = it + 1;
             if (it + 1 < n_it && !do_s(it + 1)) { ok = false; break; }
             // dK += dS^T(it) Q_it, then dP^T(it + 1) over the dS^T it just read
-            if (!wait_pair(bar_e, it)) { ok = false; break; }
-            tc_fence_after();
-            dkv_issue_acc(tDK, tDP, sdesc_adv(mQ0, (it % C::QSTAGES) * C::TILE_BYTES), kIdAcc, it == 0);
+            if (!do_acc(bar_e, it, tDK, tDP, sdesc_adv(mQ0, (it % C::QSTAGES) * C::TILE_BYTES))) {
+                ok = false;
+                break;
+            }
             mma_commit_w(&bar_qempty[it % C::QSTAGES]);
             committed_q = it + 1;
             if (it + 1 < n_it && !do_dp(it + 1)) { ok = false; break; }
@@ -312,37 +327,41 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             tmem_wait_ld();
             reg_fence32(pv);
             reg_fence32(pv + 32);
+            // in two halves of 32 columns, each signalled on its own barrier so that the MMA
+            // warp can start the dV product on the first while the second is computed
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 nl = *reinterpret_cast<const float4*>(&sL2[h][c]);
-                float pa, pb, pc, pd;
-                f2_split(f2_fma(f2_make(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), c2x2,
-                                f2_make(nl.x, nl.y)),
-                         pa, pb);
-                f2_split(f2_fma(f2_make(__uint_as_float(pv[c + 2]), __uint_as_float(pv[c + 3])), c2x2,
-                                f2_make(nl.z, nl.w)),
-                         pc, pd);
-                pv[c] = __float_as_uint(ex2(pa));
-                pv[c + 1] = __float_as_uint(ex2(pb));
-                pv[c + 2] = __float_as_uint(ex2(pc));
-                pv[c + 3] = __float_as_uint(ex2(pd));
-            }
-            if (diag) {  // key > query is masked
+            for (int x = 0; x < 2; ++x) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (krow > q0 + 64 * h + c + shift) pv[c] = 0u;
-            }
-            {
-                uint32_t pk[32];
+                for (int c = 32 * x; c < 32 * x + 32; c += 4) {
+                    const float4 nl = *reinterpret_cast<const float4*>(&sL2[h][c]);
+                    float pa, pb, pc, pd;
+                    f2_split(f2_fma(f2_make(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                    c2x2, f2_make(nl.x, nl.y)),
+                             pa, pb);
+                    f2_split(f2_fma(f2_make(__uint_as_float(pv[c + 2]), __uint_as_float(pv[c + 3])),
+                                    c2x2, f2_make(nl.z, nl.w)),
+                             pc, pd);
+                    pv[c] = __float_as_uint(ex2(pa));
+                    pv[c + 1] = __float_as_uint(ex2(pb));
+                    pv[c + 2] = __float_as_uint(ex2(pc));
+                    pv[c + 3] = __float_as_uint(ex2(pd));
+                }
+                if (diag) {  // key > query is masked
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    pk[c] = pack_bf16x2(__uint_as_float(pv[2 * c]), __uint_as_float(pv[2 * c + 1]));
-                tmem_st32(tS, pk);
+                    for (int c = 32 * x; c < 32 * x + 32; ++c)
+                        if (krow > q0 + 64 * h + c + shift) pv[c] = 0u;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    pk[c] = pack_bf16x2(__uint_as_float(pv[32 * x + 2 * c]),
+                                        __uint_as_float(pv[32 * x + 2 * c + 1]));
+                tmem_st16(tS + 16u * x, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_p[x]);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_p[h]);
             // ---- phase 2: dS^T = P^T o (dP^T - Delta), written back as bf16 pairs
             if (!warp_wait_all(&bar_dp, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
@@ -370,11 +389,11 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
                     pk[c / 2 + 1] = pack_bf16x2(dc, dd);
                 }
                 tmem_st16(tDP + 16u * cb, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_e[cb]);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_e[h]);
         }
         // ------------------------------------------------------------- epilogue
         // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.

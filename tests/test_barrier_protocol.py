@@ -149,10 +149,13 @@ def dkv_protocol(n, qs=3, gs=2):
         if it + 1 < n:
             mma += [wg(it + 1), (C, "dp")]
     progs = {"producer": prod, "mma": mma}
+    # each warpgroup signals each half of its columns on the half's barrier, which both
+    # warpgroups arrive on
     for h in (0, 1):
         progs[f"wg{h}"] = [x for j in range(n)
-                           for x in ((W, "s", j), (A, ("p", h)), (W, "dp", j), (A, ("e", h)))]
-    counts = {"s": 1, "dp": 1, ("p", 0): 1, ("p", 1): 1, ("e", 0): 1, ("e", 1): 1}
+                           for x in ((W, "s", j), (A, ("p", 0)), (A, ("p", 1)),
+                                     (W, "dp", j), (A, ("e", 0)), (A, ("e", 1)))]
+    counts = {"s": 1, "dp": 1, ("p", 0): 2, ("p", 1): 2, ("e", 0): 2, ("e", 1): 2}
     counts |= {(x, i): 1 for x in ("qfull", "qempty") for i in range(qs)}
     counts |= {(x, i): 1 for x in ("gfull", "gempty") for i in range(gs)}
     return progs, counts
