@@ -163,8 +163,10 @@ def dkv_protocol(n, qs=3, gs=2):
 
 # ----------------------------------------------------------------------------- forward kernel
 
-def fwd_protocol(j0, j1, stages=2):
-    """fa_fwd_tc_kernel: producer (K then V per block), MMA issuer, one softmax group per tile."""
+def fwd_protocol(j0, j1, stages=2, split=True):
+    """fa_fwd_tc_kernel: producer (K then V per block), MMA issuer, one softmax group per tile.
+    split: P signalled in two halves (d = 64, e4m3), else at once (bf16, d = 128)."""
+    halves = (0, 1) if split else (1,)
     jmax = max(j0, j1)
     jt = (j0, j1)
     prod = [(C, "q")]
@@ -185,8 +187,8 @@ def fwd_protocol(j0, j1, stages=2):
         mma.append((W, ("vfull", j % stages), j // stages))
         k_next = False
         for t in (0, 1):
-            if j < jt[t]:
-                mma.append((W, ("pfull", t), j))
+            if j < jt[t]:  # the P V product in halves, each after its half of P
+                mma += [(W, ("pfull", t, x), j) for x in halves]
                 if j + 1 == jt[t]:
                     mma.append((C, ("ofinal", t)))
                 else:
@@ -201,13 +203,14 @@ def fwd_protocol(j0, j1, stages=2):
     for t in (0, 1):
         g = []
         for j in range(jt[t]):
-            g += [(W, ("sfull", t), j), (A, ("pfull", t))]
+            g += [(W, ("sfull", t), j)] + [(A, ("pfull", t, x)) for x in halves]
         if jt[t] > 0:
             g.append((W, ("ofinal", t), 0))
         progs[f"softmax{t}"] = g
     counts = {"q": 1}
     counts |= {(x, i): 1 for x in ("kfull", "kempty", "vfull", "vempty") for i in range(stages)}
-    counts |= {(x, t): 1 for x in ("sfull", "pfull", "ofinal") for t in (0, 1)}
+    counts |= {(x, t): 1 for x in ("sfull", "ofinal") for t in (0, 1)}
+    counts |= {("pfull", t, x): 1 for t in (0, 1) for x in (0, 1)}
     return progs, counts
 
 
@@ -269,10 +272,10 @@ def test_dkv_protocol(n):
     explore(lambda: dkv_protocol(n))
 
 
-@pytest.mark.parametrize("stages", [2, 4])  # d = 128 and d = 64
+@pytest.mark.parametrize("stages,split", [(2, False), (4, True)])  # bf16 d = 128; d = 64, e4m3
 @pytest.mark.parametrize("j0,j1", [(1, 1), (1, 2), (2, 3), (3, 3), (4, 5), (0, 1), (6, 7)])
-def test_fwd_protocol(j0, j1, stages):
-    explore(lambda: fwd_protocol(j0, j1, stages))
+def test_fwd_protocol(j0, j1, stages, split):
+    explore(lambda: fwd_protocol(j0, j1, stages, split))
 
 
 @pytest.mark.parametrize("stages", [3, 6])  # d = 128 and d = 64
