@@ -344,12 +344,16 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             // arrive for block it, so a waiter is never a full phase behind
             if (!warp_wait_all(&bar_dp[it & 1], (it >> 1) & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
+            // all 64 columns of dP in one round trip to Tensor Memory
+            uint32_t dva[64];
+            tmem_ld32(tDPb, dva);
+            tmem_ld32(tDPb + 32u, dva + 32);
+            tmem_wait_ld();
+            reg_fence32(dva);
+            reg_fence32(dva + 32);
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
-                uint32_t dv[32];
-                tmem_ld32(tDPb + 32u * cb, dv);
-                tmem_wait_ld();
-                reg_fence32(dv);
+                const uint32_t* dv = dva + 32 * cb;
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
