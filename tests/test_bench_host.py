@@ -34,3 +34,26 @@ def test_oracle_extrapolation_scales_with_the_workload_flops():
     flops = perfmodel.fwd_flops(1, 32, 32000, 128, True) * 3.5  # forward + 2.5 x forward
     assert bench.oracle_full_step_seconds(w, 1.0) == pytest.approx(flops / 1e12)
     assert bench.oracle_full_step_seconds(w, 2.0) == pytest.approx(flops / 2e12)
+
+
+def test_committed_traffic_matches_the_algorithmic_bytes():
+    """The DRAM bytes per launch that the committed ncu summary gives for the bench's three
+    tensor-core kernels (full-size workload) lie within a few per cent of each kernel's
+    compulsory traffic: every input read once, every output written once (a kernel that
+    re-read K/V or Q/dO tiles from DRAM would show several times more)."""
+    import re
+
+    text = open(bench.PROFILE_SUMMARY).read()
+    got = {m.group(1): int(m.group(2))
+           for m in re.finditer(r"traffic (\S+) bytes_per_launch=(\d+)", text)}
+    assert set(got) == set(bench.KERNEL_SOURCES)
+    B, H, N, d = 1, 32, 32000, 128
+    t = B * H * N * d * 2          # one bf16 [B, H, N, d] tensor
+    rows = B * H * N
+    expect = {
+        "fa_fwd_tc_kernel<128>": 3 * t + t + 4 * rows,           # Q, K, V -> O, LSE
+        "fa_bwd_dkv_tc_kernel<128>": 4 * t + 8 * rows + 2 * t,   # Q, K, V, dO, LSE2, Delta -> dK, dV
+        "fa_bwd_dq_tc_kernel<128>": 4 * t + 8 * rows + t,        # same inputs -> dQ
+    }
+    for k, bytes_ in got.items():
+        assert 0.95 <= bytes_ / expect[k] <= 1.05, (k, bytes_, expect[k])
