@@ -14,7 +14,9 @@
 // TMEM columns: S_t at [128t, 128t+128) (fp32), P_t (bf16 pairs) aliased on the upper half
 // of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised); at d = 64, O_t at
 // [256 + 128t, 384 + 128t), whose column 64 accumulates the row sum of the bf16 P (the P V
-// product runs at N = 128 against V and a constant ones-column panel).
+// product runs at N = 128 against V and a constant ones-column panel).  At d = 64 and for
+// e4m3 the softmax warps signal P in two halves of 64 keys and the MMA warp issues each half
+// of the P V product as soon as it has landed (FwdCfg::SPLIT_P).
 //
 // The e4m3 variant (F8, d = 128; fixed-length square heads or packed batches) runs the same
 // schedule on 8-bit operands with kind::f8f6f4 MMAs (K = 32 per MMA): Q and K tiles of 128
