@@ -150,12 +150,11 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-# The DRAM traffic of the dominant kernel comes from an ncu capture whose summary is committed
-# under profiles/: one line per kernel, "traffic <kernel> bytes_per_launch=<B> source_sha256=<h>".
-# It is reported only while the kernel's sources still hash to <h>; after any change it is null
-# until a new capture is summarised.
-PROFILE_SUMMARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
-                               "launches_fwd_bwd_b1h32_n32000_d128_causal.md")
+# The DRAM traffic of the dominant kernel comes from ncu captures summarised under profiles/:
+# profiles/traffic.json maps each kernel to {"bytes_per_launch": B, "source_sha256": h}.  A
+# figure is reported only while the kernel's sources still hash to h; after any change it is
+# null until a new capture is recorded.
+TRAFFIC_JSON = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "fa_fwd_tc_kernel<128>": "fa_fwd_tc.cu",
     "fa_bwd_dkv_tc_kernel<128>": "fa_bwd_dkv_tc.cu",
@@ -182,20 +181,17 @@ def kernel_source_sha256(kernel: str) -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None if absent or
-    taken from different sources."""
-    import re
-
+def profiled_traffic(kernel: str, path: str = TRAFFIC_JSON):
+    """DRAM bytes per launch of `kernel` from the committed traffic file, or None if the file
+    or the kernel's entry is absent, or the entry was taken from different sources."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(path) as f:
+            entry = json.load(f)["kernels"][kernel]
+    except (OSError, ValueError, KeyError, TypeError):
         return None
-    m = re.search(r"traffic " + re.escape(kernel) + r" bytes_per_launch=(\d+) source_sha256=(\w+)",
-                  text)
-    if not m or m.group(2) != kernel_source_sha256(kernel):
+    if entry.get("source_sha256") != kernel_source_sha256(kernel):
         return None
-    return int(m.group(1))
+    return int(entry["bytes_per_launch"])
 
 
 def workload_config(w, ws: int) -> dict:

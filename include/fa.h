@@ -263,15 +263,20 @@ int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k);
  * counterpart on the pages; it exists for code that is not allowed to call cudaMalloc or any
  * allocating routine, for example a plugin running inside a host framework that owns every
  * byte of device memory, or a latency-critical loop that must not take the device-wide
- * synchronisation an allocation can imply.  It computes exactly what fa_bwd computes, with
- * the same arguments except the workspace: its scratch (Delta and the base-2 LSE) lives in a
- * fixed 8 MiB array inside the library, which every GPU that loads the library holds until
- * the process exits.
+ * synchronisation an allocation can imply.  It computes exactly what fa_bwd computes (the
+ * same kernels, so the same bits), with the same arguments except the workspace: its scratch
+ * (Delta and the base-2 LSE) lives in a fixed 8 MiB array inside the library, which every GPU
+ * that loads the library holds until the process exits.
  *   - Limit: B*H*N <= 1048576 rows (1 << 20); larger shapes return FA_ERR_TOO_LARGE and must
  *     use fa_bwd with a workspace.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     once per device, with that device current); make that first call before any stream
- *     capture.  The call allocates nothing.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current).  The CUDA runtime
+ *     may load the library's device code, and with it back the array, at the first call of
+ *     any entry point on a device; make that first call, and the first fa_bwd_noalloc call,
+ *     before any stream capture.  Every later fa_bwd_noalloc call allocates nothing.
+ *   - The looked-up address is kept for the life of the process: the library must not be
+ *     used on a device after cudaDeviceReset (the same holds for every entry point, which
+ *     keep the device's status-word address and kernel attributes).
  *   - Every call shares the one array and overwrites all of it that it uses before reading
  *     it, so nothing carries over between calls; calls that overlap on the GPU (for example
  *     on two streams at once) race on the array and must be serialised by the caller. */

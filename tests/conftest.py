@@ -11,6 +11,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long CPU work (full-size oracle comparisons)")
+    # enforced by the pytest-timeout plugin where it is installed; registered so that the mark
+    # is known either way (tests that spawn processes also bound their own waits)
+    config.addinivalue_line("markers", "timeout(seconds): upper bound on a test's run time")
 
 
 def pytest_collection_modifyitems(config, items):

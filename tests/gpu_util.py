@@ -1,6 +1,9 @@
 """Comparison helpers shared by the GPU parity tests (tolerances of the problem statement)."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -100,3 +103,30 @@ def guarded_empty(shape, dtype, device="cuda", pad=4096):
             assert ok, "write outside the output"
 
     return view, check
+
+
+def oracle_threads(bytes_per_thread: float) -> int:
+    """Host threads for an oracle call whose threads each hold ``bytes_per_thread`` of
+    scratch (one head's S and P): every core, but no more than half of the memory the host
+    reports available allows."""
+    n = os.cpu_count() or 1
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+                    n = max(1, min(n, int(0.5 * avail // bytes_per_thread)))
+                    break
+    except OSError:
+        pass
+    return n
+
+
+def record_stats(what: str, stats: dict) -> None:
+    """Print the statistics of one comparison; with FA_PARITY_STATS set to a file path, also
+    append them there as one JSON line."""
+    print(what, stats)
+    path = os.environ.get("FA_PARITY_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, **stats}) + "\n")

@@ -1,5 +1,7 @@
 """Host-side pieces of bench.py's JSON line, on CPU: the workload config both arms print, the
 roofline object of the dominant kernel and the oracle's extrapolated full-step time."""
+import json
+
 import pytest
 
 import bench
@@ -37,15 +39,12 @@ def test_oracle_extrapolation_scales_with_the_workload_flops():
 
 
 def test_committed_traffic_matches_the_algorithmic_bytes():
-    """The DRAM bytes per launch that the committed ncu summary gives for the bench's three
+    """The DRAM bytes per launch that the committed traffic file gives for the bench's three
     tensor-core kernels (full-size workload) lie within a few per cent of each kernel's
     compulsory traffic: every input read once, every output written once (a kernel that
     re-read K/V or Q/dO tiles from DRAM would show several times more)."""
-    import re
-
-    text = open(bench.PROFILE_SUMMARY).read()
-    got = {m.group(1): int(m.group(2))
-           for m in re.finditer(r"traffic (\S+) bytes_per_launch=(\d+)", text)}
+    with open(bench.TRAFFIC_JSON) as f:
+        got = {k: e["bytes_per_launch"] for k, e in json.load(f)["kernels"].items()}
     assert set(got) == set(bench.KERNEL_SOURCES)
     B, H, N, d = 1, 32, 32000, 128
     t = B * H * N * d * 2          # one bf16 [B, H, N, d] tensor
@@ -57,3 +56,31 @@ def test_committed_traffic_matches_the_algorithmic_bytes():
     }
     for k, bytes_ in got.items():
         assert 0.95 <= bytes_ / expect[k] <= 1.05, (k, bytes_, expect[k])
+
+
+def test_traffic_reader_takes_only_entries_of_the_current_sources(tmp_path):
+    """profiled_traffic returns a kernel's bytes only while the recorded hash equals the hash
+    of the kernel's current sources; a stale hash, a missing entry or a missing or malformed
+    file gives None."""
+    k = "fa_bwd_dq_tc_kernel<128>"
+    cur = bench.kernel_source_sha256(k)
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"kernels": {k: {"bytes_per_launch": 1234, "source_sha256": cur}}}))
+    assert bench.profiled_traffic(k, str(path)) == 1234
+    path.write_text(json.dumps({"kernels": {k: {"bytes_per_launch": 1234,
+                                                "source_sha256": "0" * 64}}}))
+    assert bench.profiled_traffic(k, str(path)) is None
+    assert bench.profiled_traffic("fa_fwd_tc_kernel<128>", str(path)) is None
+    path.write_text("not json")
+    assert bench.profiled_traffic(k, str(path)) is None
+    assert bench.profiled_traffic(k, str(tmp_path / "absent.json")) is None
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    """The hash that guards a traffic figure changes with the kernel's code only."""
+    import re
+
+    k = "fa_bwd_dq_tc_kernel<128>"
+    h = bench.kernel_source_sha256(k)
+    assert re.fullmatch(r"[0-9a-f]{64}", h)
+    assert bench.kernel_source_sha256(k) == h

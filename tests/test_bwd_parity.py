@@ -1,7 +1,8 @@
 """Backward parity: dQ, dK, dV from the CUDA library (through the C ABI, with O and LSE from the
 library's own forward) against the fp64 oracle backward, which recomputes its own P.  Covers
 ragged tails, the fp32 path, the SIMT cross-check, canaries, determinism and the named
-workloads at full size (oracle on sampled heads / rows, plus identities at every head)."""
+workloads at full size (every head at N = 4096; at N = 32000 the oracle's row mode on 64
+sampled query rows and 64 key rows; identities at every head)."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,8 @@ import torch
 import exact_attention_25_gb300 as fa
 import oracle
 from exact_attention_25_gb300.inputs import WORKLOADS, generate, random_qkv
-from tests.gpu_util import TOL_GRAD_REL_L2, check_grads, f64, guarded_empty, rel_l2
+from tests.gpu_util import (TOL_GRAD_REL_L2, check_fwd, check_grads, f64, guarded_empty,
+                            oracle_threads, record_stats, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -88,17 +90,23 @@ def test_gradients_stay_inside_their_buffers_and_are_deterministic(d):
 
 
 def test_workload_bwd_b4h16_n4096_d128_causal():
+    """Every head of the backward workload against the oracle backward: dQ, dK and dV by
+    relative L2 over the whole tensors (and the forward's O and LSE that fed them)."""
     w = WORKLOADS["bf16_b4h16_n4096_d128_causal_bwd"]
     x = generate(w)
     got = run(x, w.causal)
     g = {n: got[n].cpu() for n in ("dq", "dk", "dv")}
-    rng = np.random.default_rng(99)
-    heads = sorted({(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(2)})
-    for b, h in heads:
-        ref = oracle.attention_bwd_head(x["q"][b, h], x["k"][b, h], x["v"][b, h], x["do"][b, h],
-                                        w.scale, w.causal)
-        stats = check_grads({n: g[n][b, h] for n in g}, ref, torch.bfloat16, f"b={b} h={h}")
-        print(w.name, b, h, stats)
+    # each oracle thread holds P and dP of one head
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal,
+                               nthreads=oracle_threads(16.0 * w.N * (w.N + 2 * w.d) + 64e6))
+    stats = check_grads(g, ref, torch.bfloat16, w.name)
+    for n in ("dq", "dk", "dv"):
+        per_head = [rel_l2(g[n][b, h], ref[n][b, h]) for b in range(w.B) for h in range(w.H)]
+        stats["worst_head_" + n] = max(per_head)
+    stats["heads"] = w.B * w.H
+    stats["fwd"] = check_fwd(got["o"].cpu(), got["lse"].cpu(), ref["o"], ref["lse"],
+                             torch.bfloat16, w.name + " forward")
+    record_stats(w.name, stats)
     check_gradient_identities(x, g, w)
 
 
@@ -113,19 +121,36 @@ def check_gradient_identities(x, g, w):
     assert torch.allclose(dv_sum, do_sum, rtol=2e-2, atol=0.25), float((dv_sum - do_sum).abs().max())
 
 
+def long_sequence_key_rows(x, w, n_heads=4, per_head=16):
+    """Key rows whose dK and dV are compared at N = 32000: for the first n_heads sampled heads,
+    that head's sampled rows plus seeded extra rows up to per_head, and the last row of the
+    sequence (n_heads x per_head rows in all).  One pass of the oracle's row mode over a head
+    gives all of its key rows at once."""
+    by_head = {}
+    for h, i in x["samples"]:
+        by_head.setdefault(h, []).append(i)
+    rng = np.random.default_rng(20260)
+    out = {}
+    for h in sorted(by_head)[:n_heads]:
+        rows = set(by_head[h]) | {w.N - 1}
+        while len(rows) < per_head:
+            rows.add(int(rng.integers(0, w.N)))
+        out[h] = sorted(rows)[:per_head] if len(rows) > per_head else sorted(rows)
+    return by_head, out
+
+
 def test_workload_long_sequence_sampled_rows():
     w = WORKLOADS["bf16_b1h32_n32000_d128_causal_fwdbwd"]
     x = generate(w)
     got = run(x, w.causal)
     g = {n: got[n].cpu() for n in ("dq", "dk", "dv")}
-    by_head = {}
-    for h, i in x["samples"]:
-        by_head.setdefault(h, []).append(i)
+    by_head, key_rows = long_sequence_key_rows(x, w)
+    assert sum(len(r) for r in key_rows.values()) == 64
     gq, rq = [], []
-    key_heads = sorted(by_head)[:2]   # dK/dV rows need a full pass over one head: 2 heads
     gk, rk, gv, rv = [], [], [], []
-    for h, rows in sorted(by_head.items()):
-        krows = rows[:4] if h in key_heads else []
+    for h in sorted(set(by_head) | set(key_rows)):
+        rows = by_head.get(h, [])
+        krows = key_rows.get(h, [])
         res = oracle.attention_rows_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], x["do"][0, h],
                                          w.scale, w.causal, rows, krows)
         gq.append(f64(g["dq"][0, h, rows]))
@@ -138,6 +163,7 @@ def test_workload_long_sequence_sampled_rows():
     e_q = rel_l2(np.concatenate(gq), np.concatenate(rq))
     e_k = rel_l2(np.concatenate(gk), np.concatenate(rk))
     e_v = rel_l2(np.concatenate(gv), np.concatenate(rv))
-    print("N=32000 sampled rel-L2 dq/dk/dv:", e_q, e_k, e_v)
+    record_stats(w.name, {"dq_rows": sum(len(r) for r in gq), "dkv_rows": 64, "dq": e_q,
+                          "dk": e_k, "dv": e_v})
     assert e_q <= TOL_GRAD_REL_L2 and e_k <= TOL_GRAD_REL_L2 and e_v <= TOL_GRAD_REL_L2
     check_gradient_identities(x, g, w)

@@ -2,6 +2,7 @@
 own copy of the workload (the heads of a problem are independent, so there is no data-path
 collective), the job's time is the slowest rank's, and the whole-job rate counts every rank's
 work.  No GPU is involved."""
+import datetime
 import os
 import socket
 
@@ -22,7 +23,10 @@ def _rank_main(rank, world, port, out):
 
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # a bounded rendezvous and collectives: a rank that never arrives fails the test instead of
+    # hanging it (whether or not the pytest-timeout plugin is installed)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=60))
     try:
         local_ms = 10.0 + 5.0 * rank          # rank 1 is the slow one
         ms = bench.max_over_ranks(local_ms)
