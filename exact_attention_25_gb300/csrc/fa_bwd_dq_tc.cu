@@ -8,9 +8,9 @@
 // and dQ_i = scale * acc.  S and P are recomputed ("Flash Attention IO-awareness principle",
 // recomputation); nothing N x N reaches device memory and there are no atomics.
 //
-// Roles (10 warps): warps 0-7 elementwise, warpgroup h owning key columns [64h, 64h+64) of
-// every block (thread = query row = TMEM lane); warp 8 TMA producer; warp 9 TMEM allocator and
-// MMA issuer (whole warp, one elected lane issues).
+// Roles (18 warps): warps 0-15 elementwise, warpgroup h owning key columns [32h, 32h+32) of
+// every block (thread = query row = TMEM lane); warp 16 TMA producer; warp 17 TMEM allocator
+// and MMA issuer (whole warp, one elected lane issues).
 //
 // TMEM: one S buffer, two dP buffers, the accumulator.  The bf16 dS of block j overwrites the
 // dP buffer it came from (j % 2), so the S buffer is free as soon as the elementwise warps have
@@ -25,7 +25,7 @@
 // of a TMA load under full load: K_j is read by S(j) and last by acc(j) (3-stage ring), V_j by
 // dP(j) only (2 stages).
 // TMEM columns: S [0, 128), dP buffers [128, 256) and [256, 384), acc [384, 384 + d).
-// Within a dP buffer, warpgroup h's dS (32 columns of bf16 pairs) lands at [64h, 64h + 32),
+// Within a dP buffer, warpgroup h's dS (16 columns of bf16 pairs) lands at [32h, 32h + 16),
 // the first half of the columns it loaded itself.
 #include <type_traits>
 
@@ -42,10 +42,28 @@ struct DqCfg {
     static constexpr int KSTAGES = 3;
     static constexpr int VSTAGES = 2;
     static constexpr int SMEM_BYTES = (2 + KSTAGES + VSTAGES) * TILE_BYTES + 1024;
-    static constexpr int THREADS = 320;
+    // Elementwise warpgroups: warpgroup h owns key columns [COLS h, COLS h + COLS) of every
+    // block.  Nothing in the elementwise pass reduces across columns (L2 and Delta are known per
+    // row), so the columns split across warpgroups with no exchange.  Four warpgroups (four
+    // elementwise warps per sub-partition) measured 1.3 % faster than two at B1 H32 N32000 d128
+    // causal and 1.8 % for the d = 64 backward.
+    static constexpr int EW = 4;
+    static constexpr int EW_WARPS = 4 * EW;
+    static constexpr int COLS = 128 / EW;         // key columns per warpgroup
+    static constexpr int ACC_COLS = D / EW;       // accumulator columns each warpgroup stores
+    static constexpr int WARP_TMA = EW_WARPS, WARP_MMA = EW_WARPS + 1;
+    static constexpr int THREADS = 32 * (EW_WARPS + 2);
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 384;  // dP buffer b at COL_DP + 128 b
 };
+
+// TMEM column (relative to a dP buffer) of the bf16 pairs of keys [16 ks, 16 ks + 16): warpgroup
+// h writes the pairs of its COLS keys over the first COLS / 2 of the columns it loaded.
+template <int COLS>
+__host__ __device__ constexpr uint32_t dq_ds_col(int ks)
+{
+    return static_cast<uint32_t>(COLS * ((16 * ks) / COLS) + ((16 * ks) % COLS) / 2);
+}
 
 // D/16 k-steps of a 128 x 128 product of two K-major 128-row tiles, the first overwriting.
 template <int D, int PANEL>
@@ -83,11 +101,11 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_s;      // S of the next block landed
     __shared__ __align__(8) uint64_t bar_sfree;  // every elementwise warp loaded S
     __shared__ __align__(8) uint64_t bar_dp[2];  // dP landed in dP buffer b
-    // warpgroup h wrote the dS of a block of parity b (and read its S, dP): bar_e[h][b].  Both
-    // products of block j + 1 are issued before the MMA warp waits for dS(j), so one barrier per
-    // warpgroup could complete twice before that wait; per parity it cannot (block j + 2's dP
-    // is issued only after the wait).
-    __shared__ __align__(8) uint64_t bar_e[2][2];
+    // every elementwise warp wrote its dS of a block of parity b (and read its S, dP): bar_e[b].
+    // Both products of block j + 1 are issued before the MMA warp waits for dS(j), so a single
+    // barrier could complete twice before that wait; per parity it cannot (block j + 2's dP is
+    // issued only after the wait).
+    __shared__ __align__(8) uint64_t bar_e[2];
     __shared__ __align__(8) uint64_t bar_acc;   // accumulator final
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_slot;
@@ -129,21 +147,21 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             mbar_init(&bar_vempty[s], 1);
         }
         mbar_init(&bar_s, 1);
-        mbar_init(&bar_sfree, 8);  // one elected arrive per elementwise warp
+        mbar_init(&bar_sfree, C::EW_WARPS);  // one elected arrive per elementwise warp
         mbar_init(&bar_dp[0], 1);
         mbar_init(&bar_dp[1], 1);
-        for (int h = 0; h < 2; ++h)
-            for (int b = 0; b < 2; ++b) mbar_init(&bar_e[h][b], 4);  // one arrive per warp
+        mbar_init(&bar_e[0], C::EW_WARPS);
+        mbar_init(&bar_e[1], C::EW_WARPS);
         mbar_init(&bar_acc, 1);
         mbar_init(&bar_drain, 1);
         abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 9) {
+    if (warp == C::WARP_MMA) {
         tmem_alloc(&tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == C::WARP_TMA && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_g);
         tma_prefetch_desc(&tm_k);
@@ -155,7 +173,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
 
-    if (warp == 8) {
+    if (warp == C::WARP_TMA) {
         // ------------------------------------------------------------- TMA producer
         mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn) {
@@ -192,7 +210,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             mbar_wait(&bar_kfull[it % C::KSTAGES], (it / C::KSTAGES) & 1, wd_drain, kSiteBwdDrain);
         for (int it = max(0, issued_v - C::VSTAGES); it < issued_v; ++it)
             mbar_wait(&bar_vfull[it % C::VSTAGES], (it / C::VSTAGES) & 1, wd_drain, kSiteBwdDrain);
-    } else if (warp == 9) {
+    } else if (warp == C::WARP_MMA) {
         // ------------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdNT = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: both K-major
         constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);   // acc += (TMEM) * (MN-major)
@@ -215,8 +233,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             const uint64_t kb = sdesc_adv(mK0, (it % C::KSTAGES) * C::TILE_BYTES);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)  // 16 keys per k-step; dS pairs of keys [16ks, +16)
-                mma_ts_w(tAcc, sb + (ks < 4 ? 8u * ks : 64u + 8u * (ks - 4)),
-                         sdesc_adv(kb, ks * 2048), kIdAcc, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_ts_w(tAcc, sb + dq_ds_col<C::COLS>(ks), sdesc_adv(kb, ks * 2048), kIdAcc,
+                         (it > 0 || ks > 0) ? 1u : 0u);
         };
         auto wait_k = [&](int it) {
             return warp_wait_all(&bar_kfull[it % C::KSTAGES], (it / C::KSTAGES) & 1, wd,
@@ -257,8 +275,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             }
         }
         for (int it = 0; ok && it < n_it; ++it) {
-            if (!warp_wait_all(&bar_e[0][it & 1], (it >> 1) & 1, wd, kSiteBwdMmaDS) ||
-                !warp_wait_all(&bar_e[1][it & 1], (it >> 1) & 1, wd, kSiteBwdMmaDS)) {
+            if (!warp_wait_all(&bar_e[it & 1], (it >> 1) & 1, wd, kSiteBwdMmaDS)) {
                 ok = false;
                 break;
             }
@@ -283,12 +300,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             mbar_wait(&bar_vempty[it % C::VSTAGES], (it / C::VSTAGES) & 1, wd_drain, kSiteBwdDrain);
         if (ok) mbar_wait(&bar_acc, 0, wd_drain, kSiteBwdDrain);
     } else {
-        // ------------------------------------------------------------- elementwise (warps 0-7)
-        const int h = warp >> 2;          // key columns [64h, 64h + 64) of every block
+        // ------------------------------------------------------------- elementwise (warps 0-15)
+        constexpr int CW = C::COLS;       // key columns of this warpgroup in every block
+        const int h = warp >> 2;          // key columns [CW h, CW h + CW) of every block
         const int r = threadIdx.x & 127;  // query row within the block = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tbase + lane_base + C::COL_S + 64u * h;
-        const uint32_t tDP = tbase + lane_base + C::COL_DP + 64u * h;
+        const uint32_t tS = tbase + lane_base + C::COL_S + static_cast<uint32_t>(CW * h);
+        const uint32_t tDP = tbase + lane_base + C::COL_DP + static_cast<uint32_t>(CW * h);
         const uint32_t tAcc = tbase + lane_base + C::COL_ACC;
         const size_t row_base = static_cast<size_t>(qhead) * L.Rq + sr.q0;
         const int qrow = q0 + r;  // row within the sequence
@@ -301,7 +319,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const uint64_t nl2 = f2_make(nL2, nL2), nd2 = f2_make(nDl, nDl);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int k0 = it * 128 + 64 * h;  // first key of this warpgroup's columns
+            const int k0 = it * 128 + CW * h;  // first key of this warpgroup's columns
             const uint32_t tDPb = tDP + 128u * (it & 1);  // dP(it), then dS(it)
             // element-wise mask: blocks straddling the causal diagonal (key > query + shift) and
             // keys beyond the sequence
@@ -312,17 +330,17 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             // ---- phase 1: P = exp2(c S - L2) on S, which landed a block ago
             if (!warp_wait_all(&bar_s, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
-            uint32_t pv[64];
-            tmem_ld32(tS, pv);
-            tmem_ld32(tS + 32u, pv + 32);
+            uint32_t pv[CW];
+#pragma unroll
+            for (int c = 0; c < CW; c += 32) tmem_ld32(tS + c, pv + c);
             tmem_wait_ld();
-            reg_fence32(pv);
-            reg_fence32(pv + 32);
+#pragma unroll
+            for (int c = 0; c < CW; c += 32) reg_fence32(pv + c);
             tc_fence_before();  // S is in registers: the buffer may take S(it + 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_sfree);
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < CW; c += 2) {
                 const uint64_t x2 =
                     f2_fma(f2_make(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), c2x2, nl2);
                 float pa, pb;
@@ -334,25 +352,25 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             }
             if (diag || tail) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < CW; ++c) {
                     const int key = k0 + c;
                     if ((diag && key > qrow + shift) || key >= nk) pv[c] = 0u;
                 }
             }
-            // ---- phase 2: dS = P o (dP - Delta), bf16 pairs over the first 32 columns of dP
-            // one barrier per dP buffer: dP(it + 2) is issued only after this warpgroup's
+            // ---- phase 2: dS = P o (dP - Delta), bf16 pairs over the first CW / 2 columns of dP
+            // one barrier per dP buffer: dP(it + 2) is issued only after every elementwise warp's
             // arrive for block it, so a waiter is never a full phase behind
             if (!warp_wait_all(&bar_dp[it & 1], (it >> 1) & 1, wd, kSiteBwdEltS)) { ok = false; break; }
             tc_fence_after();
-            // all 64 columns of dP in one round trip to Tensor Memory
-            uint32_t dva[64];
-            tmem_ld32(tDPb, dva);
-            tmem_ld32(tDPb + 32u, dva + 32);
-            tmem_wait_ld();
-            reg_fence32(dva);
-            reg_fence32(dva + 32);
+            // all CW columns of dP in one round trip to Tensor Memory
+            uint32_t dva[CW];
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
+            for (int c = 0; c < CW; c += 32) tmem_ld32(tDPb + c, dva + c);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < CW; c += 32) reg_fence32(dva + c);
+#pragma unroll
+            for (int cb = 0; cb < CW / 32; ++cb) {
                 const uint32_t* dv = dva + 32 * cb;
                 uint32_t pk[16];
 #pragma unroll
@@ -370,32 +388,40 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_e[h][it & 1]);
+            if (lane == 0) mbar_arrive(&bar_e[it & 1]);
         }
         // ------------------------------------------------------------- epilogue
-        // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
+        // Warpgroup h stores accumulator columns [h*AC, (h+1)*AC) of its rows, AC = D / EW.
+        constexpr int AC = C::ACC_COLS;
         if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
             tc_fence_after();
             const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
                                static_cast<size_t>(qhead) * L.dq_hs;
             __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(p.dq) + off;
             const bool in = qrow >= nq || in_extent(off, D, L.dq_ext, p.status);
+            constexpr int CH = AC < 32 ? AC : 32;  // columns per Tensor Memory load
 #pragma unroll 1
-            for (int ch = 0; ch < D / 64; ++ch) {
-                const int c0 = h * (D / 2) + 32 * ch;
-                uint32_t a[32];
-                tmem_ld32(tAcc + c0, a);
-                tmem_wait_ld();
-                reg_fence32(a);
-                uint32_t packed[16];
+            for (int ch = 0; ch < AC / CH; ++ch) {
+                const int c0 = h * AC + CH * ch;
+                uint32_t a[CH];
+                if constexpr (CH == 32) {
+                    tmem_ld32(tAcc + c0, a);
+                    tmem_wait_ld();
+                    reg_fence32(a);
+                } else {
+                    tmem_ld16(tAcc + c0, a);
+                    tmem_wait_ld();
+                    reg_fence16(a);
+                }
+                uint32_t packed[CH / 2];
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
+                for (int c = 0; c < CH / 2; ++c)
                     packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale,
                                             __uint_as_float(a[2 * c + 1]) * p.scale);
                 if (qrow < nq && in) {
                     uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < CH / 8; ++c)
                         dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
                                             packed[4 * c + 3]);
                 }
@@ -406,14 +432,14 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             const size_t off = static_cast<size_t>(sr.q0 + qrow) * L.dq_rs +
                                static_cast<size_t>(qhead) * L.dq_hs;
             if (in_extent(off, D, L.dq_ext, p.status))
-                for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c)
+                for (int c = h * AC; c < (h + 1) * AC; ++c)
                     static_cast<__nv_bfloat16*>(p.dq)[off + c] = __float2bfloat16_rn(0.0f);
         }
         tc_fence_before();
     }
 
     __syncthreads();
-    if (warp == 9) {
+    if (warp == C::WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);
     }

@@ -12,9 +12,9 @@ differs from the parity asked for.  The model flags
     (a missed or an early phase: the parity test cannot tell them apart), and
   * a schedule in which no role can move while some have not finished (deadlock).
 Random schedules explore the interleavings that the kernels' timing normally hides; the dQ
-kernel's dS barrier was one barrier per warpgroup until this model (and a variant that moved
-the K/V waits) showed that the warpgroups can complete two of its phases before the MMA warp
-waits for the first.
+kernel's dS barrier was a single barrier per warpgroup until this model (and a variant that
+moved the K/V waits) showed that the warpgroups can complete two of its phases before the MMA
+warp waits for the first; it is now one barrier per block parity.
 """
 from __future__ import annotations
 
@@ -74,8 +74,10 @@ def run(progs: dict, counts: dict, rng: random.Random) -> None:
 
 # ----------------------------------------------------------------------------- dQ kernel
 
-def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False):
-    """fa_bwd_dq_tc_kernel: producer (V then K per block), MMA issuer, 2 elementwise groups."""
+def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False, groups=4):
+    """fa_bwd_dq_tc_kernel: producer (V then K per block), MMA issuer, `groups` elementwise
+    warpgroups that all arrive on one dS barrier per block parity (each warpgroup is one actor
+    here: its warps' arrivals come after the same waits)."""
     prod, mma = [], []
     for j in range(n):
         if j >= vs:
@@ -86,7 +88,7 @@ def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False):
         prod.append((C, ("kfull", j % ks)))
     wk = lambda j: (W, ("kfull", j % ks), j // ks)  # noqa: E731
     wv = lambda j: (W, ("vfull", j % vs), j // vs)  # noqa: E731
-    ebar = (lambda h, j: (("e", h, j & 1), j >> 1)) if e_per_parity else (lambda h, j: (("e", h, 0), j))
+    ebar = (lambda j: (("e", j & 1), j >> 1)) if e_per_parity else (lambda j: (("e", 0), j))
 
     def dp(j):
         return [(C, ("dp", j & 1)), (C, ("vempty", j % vs))]
@@ -100,9 +102,8 @@ def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False):
     for it in range(n):
         if kv_waits_first and it + 2 < n:
             mma += [wv(it + 2), wk(it + 2)]
-        for h in (0, 1):
-            b, k = ebar(h, it)
-            mma.append((W, b, k))
+        b, k = ebar(it)
+        mma.append((W, b, k))
         mma.append((C, ("kempty", it % ks)))
         if it + 2 < n:
             if not kv_waits_first:
@@ -113,23 +114,25 @@ def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False):
             else:
                 mma += s(it + 2)
     progs = {"producer": prod, "mma": mma}
-    for h in (0, 1):
+    for h in range(groups):
         g = []
         for j in range(n):
-            b, _ = ebar(h, j)
+            b, _ = ebar(j)
             g += [(W, "s", j), (A, "sfree"), (W, ("dp", j & 1), j >> 1), (A, b)]
         progs[f"wg{h}"] = g
-    counts = {"s": 1, "sfree": 2, ("dp", 0): 1, ("dp", 1): 1}
+    counts = {"s": 1, "sfree": groups, ("dp", 0): 1, ("dp", 1): 1}
     counts |= {(x, i): 1 for x in ("vfull", "vempty") for i in range(vs)}
     counts |= {(x, i): 1 for x in ("kfull", "kempty") for i in range(ks)}
-    counts |= {("e", h, b): 1 for h in (0, 1) for b in (0, 1)}
+    counts |= {("e", b): groups for b in (0, 1)}
     return progs, counts
 
 
 # ----------------------------------------------------------------------------- dK/dV kernel
 
-def dkv_protocol(n, qs=3, gs=2):
-    """fa_bwd_dkv_tc_kernel: producer (Q then dO per block), MMA issuer, 2 elementwise groups."""
+def dkv_protocol(n, qs=3, gs=2, groups=2, chunks=2):
+    """fa_bwd_dkv_tc_kernel: producer (Q then dO per block), MMA issuer, `groups` elementwise
+    warpgroups that each signal their columns in `chunks` chunks, chunk x on barrier x, which
+    every warpgroup arrives on."""
     prod, mma = [], []
     for j in range(n):
         if j >= qs:
@@ -142,20 +145,19 @@ def dkv_protocol(n, qs=3, gs=2):
     wg = lambda j: (W, ("gfull", j % gs), j // gs)  # noqa: E731
     mma += [wq(0), (C, "s"), wg(0), (C, "dp")]
     for it in range(n):
-        mma += [(W, ("p", 0), it), (W, ("p", 1), it), (C, ("gempty", it % gs))]
+        mma += [(W, ("p", x), it) for x in range(chunks)] + [(C, ("gempty", it % gs))]
         if it + 1 < n:
             mma += [wq(it + 1), (C, "s")]
-        mma += [(W, ("e", 0), it), (W, ("e", 1), it), (C, ("qempty", it % qs))]
+        mma += [(W, ("e", x), it) for x in range(chunks)] + [(C, ("qempty", it % qs))]
         if it + 1 < n:
             mma += [wg(it + 1), (C, "dp")]
     progs = {"producer": prod, "mma": mma}
-    # each warpgroup signals each half of its columns on the half's barrier, which both
-    # warpgroups arrive on
-    for h in (0, 1):
+    for h in range(groups):
         progs[f"wg{h}"] = [x for j in range(n)
-                           for x in ((W, "s", j), (A, ("p", 0)), (A, ("p", 1)),
-                                     (W, "dp", j), (A, ("e", 0)), (A, ("e", 1)))]
-    counts = {"s": 1, "dp": 1, ("p", 0): 2, ("p", 1): 2, ("e", 0): 2, ("e", 1): 2}
+                           for x in ([(W, "s", j)] + [(A, ("p", c)) for c in range(chunks)] +
+                                     [(W, "dp", j)] + [(A, ("e", c)) for c in range(chunks)])]
+    counts = {"s": 1, "dp": 1}
+    counts |= {(x, c): groups for x in ("p", "e") for c in range(chunks)}
     counts |= {(x, i): 1 for x in ("qfull", "qempty") for i in range(qs)}
     counts |= {(x, i): 1 for x in ("gfull", "gempty") for i in range(gs)}
     return progs, counts
@@ -262,14 +264,16 @@ def explore(make, seeds=SCHEDULES):
         run(progs, counts, random.Random(seed))
 
 
+@pytest.mark.parametrize("groups", [2, 4])
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7])
-def test_dq_protocol(n):
-    explore(lambda: dq_protocol(n))
+def test_dq_protocol(n, groups):
+    explore(lambda: dq_protocol(n, groups=groups))
 
 
+@pytest.mark.parametrize("groups,chunks", [(2, 2), (4, 1)])
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7])
-def test_dkv_protocol(n):
-    explore(lambda: dkv_protocol(n))
+def test_dkv_protocol(n, groups, chunks):
+    explore(lambda: dkv_protocol(n, groups=groups, chunks=chunks))
 
 
 @pytest.mark.parametrize("stages,split", [(2, False), (4, True)])  # bf16 d = 128; d = 64, e4m3
@@ -285,9 +289,9 @@ def test_decode_protocol(J, stages):
 
 
 def test_model_catches_a_barrier_two_phases_ahead():
-    """The dQ protocol with one dS barrier per warpgroup (instead of one per block parity) lets
-    the elementwise warps complete block j+1 before the MMA warp waits for block j: the model
-    must find that schedule."""
+    """The dQ protocol with a single dS barrier (instead of one per block parity) lets the
+    elementwise warps complete block j+1 before the MMA warp waits for block j: the model must
+    find that schedule."""
     with pytest.raises(Hazard):
         explore(lambda: dq_protocol(6, e_per_parity=False))
 
