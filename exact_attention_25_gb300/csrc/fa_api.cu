@@ -194,8 +194,21 @@ fa::Layout fixed_layout(int B, int H, int N, int d)
     L.B = B; L.H = H; L.Hkv = H;
     L.Nq = L.Nk = N;
     L.Rq = L.Rk = N;
+    L.order_group = 1;
     put_strides(L, fixed_strides(N, d), d);
     return L;
+}
+
+// Heads per group of the tensor-core kernels' tile order (tile_order): under the causal mask,
+// as many heads as keep the rows that one head's tiles stream (K and V, or Q and dO: 4 N d bytes
+// in bf16) within 32 MB of L2, at most 16; without the mask every tile costs the same and the
+// plain head-major order (1) keeps the fewest heads resident.
+int order_group(int N, int d, int causal)
+{
+    if (!causal) return 1;
+    const long long per_head = 4LL * N * d;
+    const long long g = (32LL << 20) / (per_head > 0 ? per_head : 1);
+    return static_cast<int>(g < 1 ? 1 : (g > 16 ? 16 : g));
 }
 
 // The four bf16 maps of the tensor-core kernels: q, k, v, and (backward) dout.
@@ -236,6 +249,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     p.debug_flags = g_debug_flags;
     p.L = fixed_layout(B, H, N, d);
+    p.L.order_group = order_group(N, d, causal);
     cudaError_t e;
     if (dtype == FA_F32 || impl == 1) {
         e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st);
@@ -283,6 +297,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     p.debug_flags = g_debug_flags;
     p.L = fixed_layout(B, H, N, d);
+    p.L.order_group = order_group(N, d, causal);
     const int is_f32 = dtype == FA_F32;
     cudaError_t e = cudaSuccess;
     if (stage <= 0) {
@@ -463,6 +478,7 @@ fa::Layout gqa_layout(int B, int H, int Hkv, int Nq, int Nk, int d, Strides* st)
     L.B = B; L.H = H; L.Hkv = Hkv;
     L.Nq = Nq; L.Nk = Nk;
     L.Rq = Nq; L.Rk = Nk;
+    L.order_group = 1;
     put_strides(L, *st, d);
     return L;
 }
@@ -488,6 +504,7 @@ extern "C" int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
     p.debug_flags = g_debug_flags;
     Strides st;
     p.L = gqa_layout(B, H, Hkv, Nq, Nk, d, &st);
+    p.L.order_group = order_group(Nk, d, causal);
     CUtensorMap maps[4];
     if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d, st))) return rc;
     cudaError_t e = fa::launch_fwd_tc(d, maps[0], maps[1], maps[2], p, static_cast<cudaStream_t>(stream));
@@ -527,6 +544,7 @@ extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const voi
     p.debug_flags = g_debug_flags;
     Strides st;
     p.L = gqa_layout(B, H, Hkv, Nq, Nk, d, &st);
+    p.L.order_group = order_group(Nk, d, causal);
     CUtensorMap maps[4];
     if ((rc = make_maps(maps, q, k, v, dout, p.L, d, st))) return rc;
     cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, cs, di->sms);
@@ -607,6 +625,7 @@ fa::Layout packed_layout(const int* cu_q, const int* cu_k, int B, int max_q, int
     L.B = B; L.H = H; L.Hkv = Hkv;
     L.Nq = max_q; L.Nk = max_k;
     L.Rq = total_q; L.Rk = total_k;
+    L.order_group = 1;  // sequences of different lengths: head-major
     put_strides(L, st, d);
     return L;
 }
@@ -1000,6 +1019,7 @@ extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, 
     p.causal = causal; p.status = di->status; p.wait_limit_ns = g_wait_limit_ns;
     p.debug_flags = g_debug_flags;
     p.L = fixed_layout(B, H, N, d);
+    p.L.order_group = order_group(N, d, causal);
     cudaError_t e = fa::launch_vt_transpose(v, workspace, p.L, static_cast<int>(Npad), di->status, st);
     if (e != cudaSuccess) return cuda_fail(e, "V transpose launch");
     e = fa::launch_fwd_fp8_tc(maps[0], maps[1], maps[2], p, st);

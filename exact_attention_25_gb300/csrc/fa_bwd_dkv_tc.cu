@@ -73,6 +73,54 @@ __device__ __forceinline__ void dkv_issue_acc_half(uint32_t acc, uint32_t buf, u
     }
 }
 
+// One work tile: key block kb of (sequence b, key/value head hk), for tile index `id` of the launch
+// grid, in the order of tile_order: within a head the first key blocks (most query blocks under
+// the causal mask) rank first.  Its streamed blocks are, for each query head g of the group,
+// the query blocks s_begin.. that see a key of the block.
+struct DkvTile {
+    SeqRows sr;
+    int b, hk;
+    int k0, k1;     // key rows [k0, k1) of the sequence
+    int khead;      // head index of the key-side tensors
+    int shift;      // bottom-right causal alignment (nk - nq), 0 in the square layout
+    int s_begin;    // first query block that sees a key of the block
+    int n_per;      // query blocks per query head of the group
+    int n_it;       // streamed blocks: G * n_per
+    bool valid;     // the block holds at least one key of its sequence
+};
+
+template <int MODE>
+__device__ __forceinline__ DkvTile dkv_tile(const BwdParams& p, int id)
+{
+    const Layout& L = p.L;
+    constexpr bool packed = mode_packed(MODE);
+    constexpr bool general = mode_general(MODE);
+    const int kblk_max = (L.Nk + 127) / 128;
+    int bkv, rank;
+    tile_order(id, L.B * L.Hkv, kblk_max, L.order_group, bkv, rank);
+    DkvTile t;
+    t.b = bkv / L.Hkv;
+    t.hk = bkv % L.Hkv;
+    t.sr = seq_rows<packed>(L, t.b);
+    const int nq = t.sr.nq, nk = t.sr.nk;
+    t.k0 = rank * 128;
+    t.k1 = min(nk, t.k0 + 128);
+    t.valid = t.k0 < nk;
+    t.khead = k_head_index<packed>(L, t.b, t.hk);
+    t.shift = general ? nk - nq : 0;
+    const int nqblk = (nq + 127) / 128;
+    int sb = 0;
+    if (p.causal && t.valid)
+        while (sb < nqblk && causal_class_shifted(sb * 128, min(nq, sb * 128 + 128), t.k0, t.k1,
+                                                  t.shift) == kTileSkip)
+            ++sb;
+    t.s_begin = sb;
+    t.n_per = nqblk - sb;
+    const int G = general ? L.H / L.Hkv : 1;
+    t.n_it = t.valid ? G * t.n_per : 0;
+    return t;
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     fa_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -89,7 +137,8 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     uint8_t* sQ = sV + C::TILE_BYTES;               // QSTAGES tiles
     uint8_t* sG = sQ + C::QSTAGES * C::TILE_BYTES;  // GSTAGES tiles (dO)
 
-    __shared__ __align__(8) uint64_t bar_res;
+    __shared__ __align__(8) uint64_t bar_res;     // K_j and V_j of a tile landed
+    __shared__ __align__(8) uint64_t bar_kvfree;  // every S^T and dP^T product of a tile has run
     __shared__ __align__(8) uint64_t bar_qfull[C::QSTAGES];
     __shared__ __align__(8) uint64_t bar_qempty[C::QSTAGES];
     __shared__ __align__(8) uint64_t bar_gfull[C::GSTAGES];
@@ -98,8 +147,15 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     __shared__ __align__(8) uint64_t bar_dp;    // dP^T of the next block landed
     __shared__ __align__(8) uint64_t bar_p[2];  // both warpgroups wrote half x of their P^T
     __shared__ __align__(8) uint64_t bar_e[2];  // both warpgroups wrote half x of their dS^T
-    __shared__ __align__(8) uint64_t bar_acc;   // accumulators final
+    __shared__ __align__(8) uint64_t bar_acc;   // accumulators of a tile final
     __shared__ __align__(8) uint64_t bar_drain;
+    // Tile queue: the producer warp takes further tiles from the launch grid by cluster launch
+    // control and publishes their indices (-1: none left) in a two-slot queue.
+    __shared__ __align__(16) __int128 clc_resp;
+    __shared__ __align__(8) uint64_t bar_clc;        // cancellation response landed
+    __shared__ __align__(8) uint64_t bar_tfull[2];   // tile index published
+    __shared__ __align__(8) uint64_t bar_tempty[2];  // tile index read by every other warp
+    __shared__ int tile_ids[2];
     __shared__ __align__(16) float sL2[2][64];  // -L2 per query column [warpgroup][col]
     __shared__ __align__(16) float sDl[2][64];  // -Delta per query column
     __shared__ uint32_t tmem_slot;
@@ -110,32 +166,11 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     const Layout& L = p.L;
     constexpr bool packed = mode_packed(MODE);  // tensors stored token by token
     constexpr bool general = mode_general(MODE);  // grouped heads, Nq != Nk
-    const int kblk_max = (L.Nk + 127) / 128;
-    // Head-major order; within a head the first key blocks (most query blocks under the causal
-    // mask) go first.
-    const int bkv = static_cast<int>(blockIdx.x) / kblk_max;
-    const int b = bkv / L.Hkv, hk = bkv % L.Hkv;
-    const int kb = static_cast<int>(blockIdx.x) % kblk_max;
-    const SeqRows sr = seq_rows<packed>(L, b);
-    const int nq = sr.nq, nk = sr.nk;
-    const int k0 = kb * 128, k1 = min(nk, k0 + 128);
-    if (k0 >= nk) return;  // beyond this sequence's keys (whole CTA, before any sync)
-    const int khead = k_head_index<packed>(L, b, hk);
-    const int G = general ? L.H / L.Hkv : 1;  // query heads sharing this key/value head
-    const int shift = general ? nk - nq : 0;  // bottom-right causal alignment
-    const int nqblk = (nq + 127) / 128;
-    int s_begin = 0;  // query blocks [s_begin, nqblk) see a key of [k0, k1)
-    if (p.causal)
-        while (s_begin < nqblk &&
-               causal_class_shifted(s_begin * 128, min(nq, s_begin * 128 + 128), k0, k1, shift) ==
-                   kTileSkip)
-            ++s_begin;
-    // Streamed blocks: for each query head g of the group, query blocks s_begin.. in order.
-    const int n_per = nqblk - s_begin;
-    const int n_it = G * n_per;
+    const int G = general ? L.H / L.Hkv : 1;  // query heads sharing a key/value head
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_res, 1);
+        mbar_init(&bar_kvfree, 1);
         for (int s = 0; s < C::QSTAGES; ++s) {
             mbar_init(&bar_qfull[s], 1);
             mbar_init(&bar_qempty[s], 1);
@@ -152,6 +187,11 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         }
         mbar_init(&bar_acc, 1);
         mbar_init(&bar_drain, 1);
+        mbar_init(&bar_clc, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_tfull[s], 1);
+            mbar_init(&bar_tempty[s], 9);  // the eight elementwise warps and the MMA warp
+        }
         abort_flag = 0;
         mbar_fence_init();
     }
@@ -171,41 +211,107 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
 
+    // Every role walks the same tile sequence: this CTA's own index (ordinal 0), then the
+    // published ones.  Ordinal o >= 1 uses queue slot o & 1 as that slot's use (o - 1) >> 1, so
+    // it waits for phase parity ((o - 1) >> 1) & 1.  Streamed blocks are counted over the whole
+    // sequence (g) for the rings and the per-block barriers, tiles with streamed blocks (at) for
+    // the per-tile barriers.
+    auto next_tile = [&](int ti, int& next) {  // consumers: index of tile ordinal ti + 1
+        const int s1 = (ti + 1) & 1;
+        if (!warp_wait_all(&bar_tfull[s1], (ti >> 1) & 1, wd, kSiteBwdTile)) return false;
+        next = tile_ids[s1];
+        __syncwarp();
+        mbar_arrive_w(&bar_tempty[s1]);
+        return true;
+    };
+
     if (warp == 8) {
         // ------------------------------------------------------------- TMA producer
-        mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-            tma_load_rows_w(sK + pn * C::PANEL_BYTES, &tm_k, &bar_res, 64 * pn, sr.k0 + k0, khead, packed);
-            tma_load_rows_w(sV + pn * C::PANEL_BYTES, &tm_v, &bar_res, 64 * pn, sr.k0 + k0, khead, packed);
-        }
-        int issued_q = 0, issued_g = 0;
-        for (int it = 0; it < n_it; ++it) {
-            const int g = general ? it / n_per : 0;
-            const int row = sr.q0 + (s_begin + it - g * n_per) * 128;
-            const int qhead = q_head_index<packed>(L, b, hk * G + g);
-            // Q first: S^T(it) is issued before dP^T(it)
-            const int sq = it % C::QSTAGES;
-            if (!warp_wait_all(&bar_qempty[sq], ((it / C::QSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
+        int id = static_cast<int>(blockIdx.x), ti = 0, g = 0, at = 0;
+        int issued_q = 0, issued_g = 0, issued_res = 0;
+        bool clc_pending = false;  // a cancellation request whose response has not landed
+        bool ok = true;
+        for (;;) {
+            const DkvTile t = dkv_tile<MODE>(p, id);
+            if (t.n_it > 0) {
+                // K_j, V_j of this tile once the previous tile's S^T and dP^T products have run
+                if (at > 0 && !warp_wait_all(&bar_kvfree, (at - 1) & 1, wd, kSiteBwdLoadEmpty)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx_w(&bar_res, 2 * C::TILE_BYTES);
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    tma_load_rows_w(sK + pn * C::PANEL_BYTES, &tm_k, &bar_res, 64 * pn,
+                                    t.sr.k0 + t.k0, t.khead, packed);
+                    tma_load_rows_w(sV + pn * C::PANEL_BYTES, &tm_v, &bar_res, 64 * pn,
+                                    t.sr.k0 + t.k0, t.khead, packed);
+                }
+                issued_res = at + 1;
+                for (int it = 0; it < t.n_it; ++it) {
+                    const int gg = g + it;
+                    const int gh = general ? it / t.n_per : 0;
+                    const int row = t.sr.q0 + (t.s_begin + it - gh * t.n_per) * 128;
+                    const int qhead = q_head_index<packed>(L, t.b, t.hk * G + gh);
+                    // Q first: S^T(it) is issued before dP^T(it)
+                    const int sq = gg % C::QSTAGES;
+                    if (!warp_wait_all(&bar_qempty[sq], ((gg / C::QSTAGES) & 1) ^ 1, wd,
+                                       kSiteBwdLoadEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx_w(&bar_qfull[sq], C::TILE_BYTES);
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_rows_w(sQ + sq * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q,
+                                        &bar_qfull[sq], 64 * pn, row, qhead, packed);
+                    issued_q = gg + 1;
+                    const int sg = gg % C::GSTAGES;
+                    if (!warp_wait_all(&bar_gempty[sg], ((gg / C::GSTAGES) & 1) ^ 1, wd,
+                                       kSiteBwdLoadEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx_w(&bar_gfull[sg], C::TILE_BYTES);
+                    if (!(gg == 0 && (p.debug_flags & kDebugDropFirstLoad)))
+                        for (int pn = 0; pn < C::PANELS; ++pn)
+                            tma_load_rows_w(sG + sg * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_g,
+                                            &bar_gfull[sg], 64 * pn, row, qhead, packed);
+                    issued_g = gg + 1;
+                }
+                if (!ok) break;
+                g += t.n_it;
+                ++at;
+            }
+            // Take the next tile now, a few blocks before this one ends (a tile taken earlier
+            // would wait for this CTA while another SM could already run it).  The request for
+            // ordinal ti + 1 is use ti of the response barrier.
+            clc_try_cancel_w(&clc_resp, &bar_clc);
+            clc_pending = true;
+            if (!warp_wait_all(&bar_clc, ti & 1, wd, kSiteBwdTile)) {
+                ok = false;
                 break;
-            mbar_arrive_expect_tx_w(&bar_qfull[sq], C::TILE_BYTES);
-            for (int pn = 0; pn < C::PANELS; ++pn)
-                tma_load_rows_w(sQ + sq * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bar_qfull[sq],
-                              64 * pn, row, qhead, packed);
-            issued_q = it + 1;
-            const int sg = it % C::GSTAGES;
-            if (!warp_wait_all(&bar_gempty[sg], ((it / C::GSTAGES) & 1) ^ 1, wd, kSiteBwdLoadEmpty))
+            }
+            clc_pending = false;
+            const int next = clc_cancelled_x(&clc_resp);
+            __syncwarp();
+            const int s1 = (ti + 1) & 1;
+            if (!warp_wait_all(&bar_tempty[s1], ((ti >> 1) & 1) ^ 1, wd, kSiteBwdTile)) {
+                ok = false;
                 break;
-            mbar_arrive_expect_tx_w(&bar_gfull[sg], C::TILE_BYTES);
-            if (!(it == 0 && (p.debug_flags & kDebugDropFirstLoad)))
-                for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_rows_w(sG + sg * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_g,
-                                  &bar_gfull[sg], 64 * pn, row, qhead, packed);
-            issued_g = it + 1;
+            }
+            if (lane == 0) {
+                tile_ids[s1] = next;
+                mbar_arrive(&bar_tfull[s1]);
+            }
+            __syncwarp();
+            if (next < 0) break;
+            id = next;
+            ++ti;
         }
-        // drain: no copy may still be in flight when the CTA exits
+        // drain: no copy or cancellation response may still be in flight when the CTA exits
         volatile int no_abort = 0;
         const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
-        mbar_wait(&bar_res, 0, wd_drain, kSiteBwdDrain);
+        if (clc_pending) mbar_wait(&bar_clc, ti & 1, wd_drain, kSiteBwdDrain);
+        if (issued_res > 0) mbar_wait(&bar_res, (issued_res - 1) & 1, wd_drain, kSiteBwdDrain);
         for (int it = max(0, issued_q - C::QSTAGES); it < issued_q; ++it)
             mbar_wait(&bar_qfull[it % C::QSTAGES], (it / C::QSTAGES) & 1, wd_drain, kSiteBwdDrain);
         for (int it = max(0, issued_g - C::GSTAGES); it < issued_g; ++it)
@@ -222,64 +328,89 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         const uint64_t mQ0 = sdesc_sw128(smem_u32(sQ), C::PANEL_BYTES, 1024);   // MN-major
         const uint64_t dG0 = sdesc_sw128(smem_u32(sG), 16, 1024);
         const uint64_t mG0 = sdesc_sw128(smem_u32(sG), C::PANEL_BYTES, 1024);
-        auto wait_q = [&](int it) {
-            return warp_wait_all(&bar_qfull[it % C::QSTAGES], (it / C::QSTAGES) & 1, wd,
+        auto wait_q = [&](int gg) {
+            return warp_wait_all(&bar_qfull[gg % C::QSTAGES], (gg / C::QSTAGES) & 1, wd,
                                  kSiteBwdMmaQ);
         };
-        auto wait_g = [&](int it) {
-            return warp_wait_all(&bar_gfull[it % C::GSTAGES], (it / C::GSTAGES) & 1, wd,
+        auto wait_g = [&](int gg) {
+            return warp_wait_all(&bar_gfull[gg % C::GSTAGES], (gg / C::GSTAGES) & 1, wd,
                                  kSiteBwdMmaQ);
         };
-        auto do_s = [&](int it) {  // S^T(it) -> S buffer
-            if (!wait_q(it)) return false;
+        auto do_s = [&](int gg) {  // S^T(gg) -> S buffer
+            if (!wait_q(gg)) return false;
             tc_fence_after();
             dkv_issue_nt<D, C::PANEL_BYTES>(tS, dKd,
-                                            sdesc_adv(dQ0, (it % C::QSTAGES) * C::TILE_BYTES), kIdNT);
+                                            sdesc_adv(dQ0, (gg % C::QSTAGES) * C::TILE_BYTES), kIdNT);
             mma_commit_w(&bar_s);
             return true;
         };
-        auto do_dp = [&](int it) {  // dP^T(it) -> dP buffer
-            if (!wait_g(it)) return false;
+        auto do_dp = [&](int gg) {  // dP^T(gg) -> dP buffer
+            if (!wait_g(gg)) return false;
             tc_fence_after();
             dkv_issue_nt<D, C::PANEL_BYTES>(tDP, dVd,
-                                            sdesc_adv(dG0, (it % C::GSTAGES) * C::TILE_BYTES), kIdNT);
+                                            sdesc_adv(dG0, (gg % C::GSTAGES) * C::TILE_BYTES), kIdNT);
             mma_commit_w(&bar_dp);
             return true;
         };
         // acc += (TMEM operand) * (MN-major tile), each half issued as soon as both warpgroups
         // have written it
-        auto do_acc = [&](uint64_t* bars, int it, uint32_t acc, uint32_t buf, uint64_t bdesc) {
-            if (!warp_wait_all(&bars[0], it & 1, wd, kSiteBwdMmaDS)) return false;
+        auto do_acc = [&](uint64_t* bars, int gg, bool first, uint32_t acc, uint32_t buf,
+                          uint64_t bdesc) {
+            if (!warp_wait_all(&bars[0], gg & 1, wd, kSiteBwdMmaDS)) return false;
             tc_fence_after();
-            dkv_issue_acc_half<0>(acc, buf, bdesc, kIdAcc, it == 0);
-            if (!warp_wait_all(&bars[1], it & 1, wd, kSiteBwdMmaDS)) return false;
+            dkv_issue_acc_half<0>(acc, buf, bdesc, kIdAcc, first);
+            if (!warp_wait_all(&bars[1], gg & 1, wd, kSiteBwdMmaDS)) return false;
             tc_fence_after();
-            dkv_issue_acc_half<1>(acc, buf, bdesc, kIdAcc, it == 0);
+            dkv_issue_acc_half<1>(acc, buf, bdesc, kIdAcc, first);
             return true;
         };
 
-        bool ok = warp_wait_all(&bar_res, 0, wd, kSiteBwdMmaKV);
+        int id = static_cast<int>(blockIdx.x), ti = 0, g = 0, at = 0;
         int committed_q = 0, committed_g = 0;
-        if (ok && n_it > 0) ok = do_s(0) && do_dp(0);
-        for (int it = 0; ok && it < n_it; ++it) {
-            // dV += P^T(it) dO_it, then S^T(it + 1) over the P^T it just read
-            if (!do_acc(bar_p, it, tDV, tS, sdesc_adv(mG0, (it % C::GSTAGES) * C::TILE_BYTES))) {
-                ok = false;
-                break;
+        bool ok = true;
+        for (;;) {
+            const int n = dkv_tile<MODE>(p, id).n_it;
+            if (n > 0) {
+                if (!warp_wait_all(&bar_res, at & 1, wd, kSiteBwdMmaKV)) { ok = false; break; }
+                // the first products of this tile run while the elementwise warps still read
+                // out the previous tile's accumulators
+                ok = do_s(g) && do_dp(g);
+                if (ok && n == 1) mma_commit_w(&bar_kvfree);  // every S^T, dP^T of the tile issued
+                for (int it = 0; ok && it < n; ++it) {
+                    const int gg = g + it;
+                    // dV += P^T(gg) dO_gg, then S^T(gg + 1) over the P^T it just read
+                    if (!do_acc(bar_p, gg, it == 0, tDV, tS,
+                                sdesc_adv(mG0, (gg % C::GSTAGES) * C::TILE_BYTES))) {
+                        ok = false;
+                        break;
+                    }
+                    mma_commit_w(&bar_gempty[gg % C::GSTAGES]);
+                    committed_g = gg + 1;
+                    if (it + 1 < n && !do_s(gg + 1)) { ok = false; break; }
+                    // dK += dS^T(gg) Q_gg, then dP^T(gg + 1) over the dS^T it just read
+                    if (!do_acc(bar_e, gg, it == 0, tDK, tDP,
+                                sdesc_adv(mQ0, (gg % C::QSTAGES) * C::TILE_BYTES))) {
+                        ok = false;
+                        break;
+                    }
+                    mma_commit_w(&bar_qempty[gg % C::QSTAGES]);
+                    committed_q = gg + 1;
+                    if (it + 1 < n) {
+                        if (!do_dp(gg + 1)) { ok = false; break; }
+                        if (it + 2 == n) mma_commit_w(&bar_kvfree);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_w(&bar_acc);
+                g += n;
+                ++at;
             }
-            mma_commit_w(&bar_gempty[it % C::GSTAGES]);
-            committed_g = it + 1;
-            if (it + 1 < n_it && !do_s(it + 1)) { ok = false; break; }
-            // dK += dS^T(it) Q_it, then dP^T(it + 1) over the dS^T it just read
-            if (!do_acc(bar_e, it, tDK, tDP, sdesc_adv(mQ0, (it % C::QSTAGES) * C::TILE_BYTES))) {
-                ok = false;
-                break;
-            }
-            mma_commit_w(&bar_qempty[it % C::QSTAGES]);
-            committed_q = it + 1;
-            if (it + 1 < n_it && !do_dp(it + 1)) { ok = false; break; }
+            int next = -1;
+            if (!next_tile(ti, next)) { ok = false; break; }
+            if (next < 0) break;
+            id = next;
+            ++ti;
         }
-        if (ok) mma_commit_w(&bar_acc);
         volatile int no_abort = 0;
         const Watchdog wd_drain{&no_abort, p.status, p.wait_limit_ns};
         mma_commit_w(&bar_drain);
@@ -288,7 +419,10 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             mbar_wait(&bar_qempty[it % C::QSTAGES], (it / C::QSTAGES) & 1, wd_drain, kSiteBwdDrain);
         for (int it = max(0, committed_g - C::GSTAGES); it < committed_g; ++it)
             mbar_wait(&bar_gempty[it % C::GSTAGES], (it / C::GSTAGES) & 1, wd_drain, kSiteBwdDrain);
-        if (ok) mbar_wait(&bar_acc, 0, wd_drain, kSiteBwdDrain);
+        if (ok && at > 0) {
+            mbar_wait(&bar_acc, (at - 1) & 1, wd_drain, kSiteBwdDrain);
+            mbar_wait(&bar_kvfree, (at - 1) & 1, wd_drain, kSiteBwdDrain);
+        }
     } else {
         // ------------------------------------------------------------- elementwise (warps 0-7)
         const int h = warp >> 2;          // query columns [64h, 64h + 64) of every block
@@ -297,152 +431,180 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
         const uint32_t tS = tbase + lane_base + C::COL_S + 64u * h;
         const uint32_t tDP = tbase + lane_base + C::COL_DP + 64u * h;
         const uint32_t tDV = tbase + lane_base + C::COL_DV, tDK = tbase + lane_base + C::COL_DK;
-        const int krow = k0 + r;  // key row within the sequence
         const uint64_t c2x2 = f2_make(p.scale_log2, p.scale_log2);
+        int id = static_cast<int>(blockIdx.x), ti = 0, g = 0, at = 0;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int g = general ? it / n_per : 0;
-            const int q0 = (s_begin + it - g * n_per) * 128;  // first query of the block
-            const size_t row_base =
-                static_cast<size_t>(q_head_index<packed>(L, b, hk * G + g)) * L.Rq + sr.q0;
-            // stage -L2 and -Delta of this warpgroup's 64 query columns (negated, so the passes
-            // below are fma / add only; queries beyond N get P = 0).  The first barrier keeps
-            // the previous block's values until every thread of the warpgroup is done with them.
-            named_bar_sync(1 + h, 128);
-            if (r < 64) {
-                const int qi = q0 + 64 * h + r;
-                const bool in = qi < nq && in_extent(row_base + qi, 1, L.stat_ext, p.status);
-                sL2[h][r] = in ? -p.lse2[row_base + qi] : -INFINITY;
-                sDl[h][r] = in ? -p.delta[row_base + qi] : 0.0f;
-            }
-            named_bar_sync(1 + h, 128);
-            const bool diag = p.causal && causal_class_shifted(q0, min(nq, q0 + 128), k0, k1,
-                                                               shift) == kTileMasked;
-            // ---- phase 1: P^T = exp2(c S^T - L2), written back as bf16 pairs
-            if (!warp_wait_all(&bar_s, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t pv[64];
-            tmem_ld32(tS, pv);
-            tmem_ld32(tS + 32u, pv + 32);
-            tmem_wait_ld();
-            reg_fence32(pv);
-            reg_fence32(pv + 32);
-            // in two halves of 32 columns, each signalled on its own barrier so that the MMA
-            // warp can start the dV product on the first while the second is computed
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-#pragma unroll
-                for (int c = 32 * x; c < 32 * x + 32; c += 4) {
-                    const float4 nl = *reinterpret_cast<const float4*>(&sL2[h][c]);
-                    float pa, pb, pc, pd;
-                    f2_split(f2_fma(f2_make(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
-                                    c2x2, f2_make(nl.x, nl.y)),
-                             pa, pb);
-                    f2_split(f2_fma(f2_make(__uint_as_float(pv[c + 2]), __uint_as_float(pv[c + 3])),
-                                    c2x2, f2_make(nl.z, nl.w)),
-                             pc, pd);
-                    pv[c] = __float_as_uint(ex2(pa));
-                    pv[c + 1] = __float_as_uint(ex2(pb));
-                    pv[c + 2] = __float_as_uint(ex2(pc));
-                    pv[c + 3] = __float_as_uint(ex2(pd));
+        for (;;) {
+            const DkvTile t = dkv_tile<MODE>(p, id);
+            const int nq = t.sr.nq, nk = t.sr.nk, n_it = t.n_it;
+            const int krow = t.k0 + r;  // key row within the sequence
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int gg = g + it;
+                const int gh = general ? it / t.n_per : 0;
+                const int q0 = (t.s_begin + it - gh * t.n_per) * 128;  // first query of the block
+                const size_t row_base =
+                    static_cast<size_t>(q_head_index<packed>(L, t.b, t.hk * G + gh)) * L.Rq +
+                    t.sr.q0;
+                // stage -L2 and -Delta of this warpgroup's 64 query columns (negated, so the
+                // passes below are fma / add only; queries beyond N get P = 0).  The first
+                // barrier keeps the previous block's values until every thread of the warpgroup
+                // is done with them.
+                named_bar_sync(1 + h, 128);
+                if (r < 64) {
+                    const int qi = q0 + 64 * h + r;
+                    const bool in = qi < nq && in_extent(row_base + qi, 1, L.stat_ext, p.status);
+                    sL2[h][r] = in ? -p.lse2[row_base + qi] : -INFINITY;
+                    sDl[h][r] = in ? -p.delta[row_base + qi] : 0.0f;
                 }
-                if (diag) {  // key > query is masked
-#pragma unroll
-                    for (int c = 32 * x; c < 32 * x + 32; ++c)
-                        if (krow > q0 + 64 * h + c + shift) pv[c] = 0u;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    pk[c] = pack_bf16x2(__uint_as_float(pv[32 * x + 2 * c]),
-                                        __uint_as_float(pv[32 * x + 2 * c + 1]));
-                tmem_st16(tS + 16u * x, pk);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_p[x]);
-            }
-            // ---- phase 2: dS^T = P^T o (dP^T - Delta), written back as bf16 pairs
-            if (!warp_wait_all(&bar_dp, it & 1, wd, kSiteBwdEltS)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                uint32_t dv[32];
-                tmem_ld32(tDP + 32u * cb, dv);
+                named_bar_sync(1 + h, 128);
+                const bool diag = p.causal && causal_class_shifted(q0, min(nq, q0 + 128), t.k0,
+                                                                   t.k1, t.shift) == kTileMasked;
+                // ---- phase 1: P^T = exp2(c S^T - L2), written back as bf16 pairs
+                if (!warp_wait_all(&bar_s, gg & 1, wd, kSiteBwdEltS)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t pv[64];
+                tmem_ld32(tS, pv);
+                tmem_ld32(tS + 32u, pv + 32);
                 tmem_wait_ld();
-                reg_fence32(dv);
-                uint32_t pk[16];
+                reg_fence32(pv);
+                reg_fence32(pv + 32);
+                // in two halves of 32 columns, each signalled on its own barrier so that the MMA
+                // warp can start the dV product on the first while the second is computed
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const int i = 32 * cb + c;
-                    const float4 nd = *reinterpret_cast<const float4*>(&sDl[h][i]);
-                    float da, db, dc, dd;
-                    f2_split(f2_mul(f2_make(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])),
-                                    f2_add(f2_make(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
-                                           f2_make(nd.x, nd.y))),
-                             da, db);
-                    f2_split(f2_mul(f2_make(__uint_as_float(pv[i + 2]), __uint_as_float(pv[i + 3])),
-                                    f2_add(f2_make(__uint_as_float(dv[c + 2]), __uint_as_float(dv[c + 3])),
-                                           f2_make(nd.z, nd.w))),
-                             dc, dd);
-                    pk[c / 2] = pack_bf16x2(da, db);
-                    pk[c / 2 + 1] = pack_bf16x2(dc, dd);
-                }
-                tmem_st16(tDP + 16u * cb, pk);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_e[cb]);
-            }
-        }
-        // ------------------------------------------------------------- epilogue
-        // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
-        if (ok && n_it > 0 && warp_wait_all(&bar_acc, 0, wd, kSiteBwdEltAcc)) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t tAcc = which == 0 ? tDV : tDK;
-                const float mul = which == 0 ? 1.0f : p.scale;
-                const long long rs = which == 0 ? L.dv_rs : L.dk_rs;
-                const long long hs = which == 0 ? L.dv_hs : L.dk_hs;
-                const size_t off = static_cast<size_t>(sr.k0 + krow) * rs +
-                                   static_cast<size_t>(khead) * hs;
-                __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + off;
-                const bool in = krow >= nk ||
-                                in_extent(off, D, which == 0 ? L.dv_ext : L.dk_ext, p.status);
-#pragma unroll 1
-                for (int ch = 0; ch < D / 64; ++ch) {
-                    const int c0 = h * (D / 2) + 32 * ch;
-                    uint32_t a[32];
-                    tmem_ld32(tAcc + c0, a);
-                    tmem_wait_ld();
-                    reg_fence32(a);
-                    uint32_t packed[16];
+                for (int x = 0; x < 2; ++x) {
+#pragma unroll
+                    for (int c = 32 * x; c < 32 * x + 32; c += 4) {
+                        const float4 nl = *reinterpret_cast<const float4*>(&sL2[h][c]);
+                        float pa, pb, pc, pd;
+                        f2_split(f2_fma(f2_make(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                        c2x2, f2_make(nl.x, nl.y)),
+                                 pa, pb);
+                        f2_split(f2_fma(f2_make(__uint_as_float(pv[c + 2]),
+                                                __uint_as_float(pv[c + 3])),
+                                        c2x2, f2_make(nl.z, nl.w)),
+                                 pc, pd);
+                        pv[c] = __float_as_uint(ex2(pa));
+                        pv[c + 1] = __float_as_uint(ex2(pb));
+                        pv[c + 2] = __float_as_uint(ex2(pc));
+                        pv[c + 3] = __float_as_uint(ex2(pd));
+                    }
+                    if (diag) {  // key > query is masked
+#pragma unroll
+                        for (int c = 32 * x; c < 32 * x + 32; ++c)
+                            if (krow > q0 + 64 * h + c + t.shift) pv[c] = 0u;
+                    }
+                    uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        packed[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
-                                                __uint_as_float(a[2 * c + 1]) * mul);
-                    if (krow < nk && in) {
-                        uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+                        pk[c] = pack_bf16x2(__uint_as_float(pv[32 * x + 2 * c]),
+                                            __uint_as_float(pv[32 * x + 2 * c + 1]));
+                    tmem_st16(tS + 16u * x, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_p[x]);
+                }
+                // ---- phase 2: dS^T = P^T o (dP^T - Delta), written back as bf16 pairs
+                if (!warp_wait_all(&bar_dp, gg & 1, wd, kSiteBwdEltS)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
-                                                packed[4 * c + 3]);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t dv[32];
+                    tmem_ld32(tDP + 32u * cb, dv);
+                    tmem_wait_ld();
+                    reg_fence32(dv);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const int i = 32 * cb + c;
+                        const float4 nd = *reinterpret_cast<const float4*>(&sDl[h][i]);
+                        float da, db, dc, dd;
+                        f2_split(f2_mul(f2_make(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])),
+                                        f2_add(f2_make(__uint_as_float(dv[c]),
+                                                       __uint_as_float(dv[c + 1])),
+                                               f2_make(nd.x, nd.y))),
+                                 da, db);
+                        f2_split(f2_mul(f2_make(__uint_as_float(pv[i + 2]),
+                                                __uint_as_float(pv[i + 3])),
+                                        f2_add(f2_make(__uint_as_float(dv[c + 2]),
+                                                       __uint_as_float(dv[c + 3])),
+                                               f2_make(nd.z, nd.w))),
+                                 dc, dd);
+                        pk[c / 2] = pack_bf16x2(da, db);
+                        pk[c / 2 + 1] = pack_bf16x2(dc, dd);
                     }
+                    tmem_st16(tDP + 16u * cb, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_e[cb]);
                 }
             }
-        } else if (n_it == 0 && krow < nk) {
-            // a key block that no query sees (a sequence without queries) has zero gradient
-            const size_t offk = static_cast<size_t>(sr.k0 + krow) * L.dk_rs +
-                                static_cast<size_t>(khead) * L.dk_hs;
-            const size_t offv = static_cast<size_t>(sr.k0 + krow) * L.dv_rs +
-                                static_cast<size_t>(khead) * L.dv_hs;
-            const bool ink = in_extent(offk, D, L.dk_ext, p.status);
-            const bool inv = in_extent(offv, D, L.dv_ext, p.status);
-            for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c) {
-                if (ink) static_cast<__nv_bfloat16*>(p.dk)[offk + c] = __float2bfloat16_rn(0.0f);
-                if (inv) static_cast<__nv_bfloat16*>(p.dv)[offv + c] = __float2bfloat16_rn(0.0f);
+            int next = -1;
+            if (ok && !next_tile(ti, next)) ok = false;
+            // ------------------------------------------------------------- epilogue
+            // Warpgroup h stores accumulator columns [h*D/2, (h+1)*D/2) of its rows.
+            if (n_it > 0) {
+                if (ok && warp_wait_all(&bar_acc, at & 1, wd, kSiteBwdEltAcc)) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t tAcc = which == 0 ? tDV : tDK;
+                        const float mul = which == 0 ? 1.0f : p.scale;
+                        const long long rs = which == 0 ? L.dv_rs : L.dk_rs;
+                        const long long hs = which == 0 ? L.dv_hs : L.dk_hs;
+                        const size_t off = static_cast<size_t>(t.sr.k0 + krow) * rs +
+                                           static_cast<size_t>(t.khead) * hs;
+                        __nv_bfloat16* dst_row =
+                            static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + off;
+                        const bool in = krow >= nk ||
+                                        in_extent(off, D, which == 0 ? L.dv_ext : L.dk_ext, p.status);
+#pragma unroll 1
+                        for (int ch = 0; ch < D / 64; ++ch) {
+                            const int c0 = h * (D / 2) + 32 * ch;
+                            uint32_t a[32];
+                            tmem_ld32(tAcc + c0, a);
+                            tmem_wait_ld();
+                            reg_fence32(a);
+                            uint32_t packed_v[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                packed_v[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
+                                                          __uint_as_float(a[2 * c + 1]) * mul);
+                            if (krow < nk && in) {
+                                uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    dst[c] = make_uint4(packed_v[4 * c], packed_v[4 * c + 1],
+                                                        packed_v[4 * c + 2], packed_v[4 * c + 3]);
+                            }
+                        }
+                    }
+                    // the accumulators are in registers: the next tile's first products may
+                    // overwrite them (the MMA warp issues those only after this warp's next
+                    // arrive)
+                    tc_fence_before();
+                } else {
+                    ok = false;
+                }
+                g += n_it;
+                ++at;
+            } else if (t.valid && krow < nk) {
+                // a key block that no query sees (a sequence without queries) has zero gradient
+                const size_t offk = static_cast<size_t>(t.sr.k0 + krow) * L.dk_rs +
+                                    static_cast<size_t>(t.khead) * L.dk_hs;
+                const size_t offv = static_cast<size_t>(t.sr.k0 + krow) * L.dv_rs +
+                                    static_cast<size_t>(t.khead) * L.dv_hs;
+                const bool ink = in_extent(offk, D, L.dk_ext, p.status);
+                const bool inv = in_extent(offv, D, L.dv_ext, p.status);
+                for (int c = h * (D / 2); c < (h + 1) * (D / 2); ++c) {
+                    if (ink) static_cast<__nv_bfloat16*>(p.dk)[offk + c] = __float2bfloat16_rn(0.0f);
+                    if (inv) static_cast<__nv_bfloat16*>(p.dv)[offv + c] = __float2bfloat16_rn(0.0f);
+                }
             }
+            if (!ok || next < 0) break;
+            id = next;
+            ++ti;
         }
         tc_fence_before();
     }

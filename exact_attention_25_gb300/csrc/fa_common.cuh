@@ -23,6 +23,7 @@ enum WaitSite : int {
     kSiteFwdSoftmaxS,
     kSiteFwdSoftmaxO,
     kSiteFwdDrain,
+    kSiteFwdTile,  // the next tile's index (persistent kernels)
     kSiteBwdLoadEmpty = 16,
     kSiteBwdMmaKV,
     kSiteBwdMmaQ,
@@ -31,6 +32,7 @@ enum WaitSite : int {
     kSiteBwdEltS,
     kSiteBwdEltAcc,
     kSiteBwdDrain,
+    kSiteBwdTile,
 };
 
 // Test hook: the producer announces the bytes of its first streamed tile but never issues
@@ -76,6 +78,24 @@ __host__ __device__ inline int causal_tile_class(int q0, int q1, int k0, int k1)
     return kTileMasked;
 }
 
+// Order of the work tiles of a launch over `heads` heads of `nblk` tiles each, tile rank 0
+// being the heaviest of a head under the causal mask.  Heads go in groups of `gsize` consecutive
+// heads; within a group the tiles go by rank, the group's heads interleaved, and groups follow
+// one another.  So the heaviest tiles of a group start first and its light ones fill the end,
+// instead of the last head's heaviest tile starting when everything else is nearly done, while
+// the tiles resident at one time still share the key/value (or query) rows of a few heads in
+// L2.  gsize = 1 is plain head-major order.  Tile `id` in [0, heads * nblk) maps to one (head,
+// rank) pair, and every pair is reached once.
+__host__ __device__ inline void tile_order(int id, int heads, int nblk, int gsize, int& head,
+                                           int& rank)
+{
+    const int g0 = id / (gsize * nblk) * gsize;   // first head of the tile's group
+    const int gh = min(gsize, heads - g0);        // heads in that group (the last may be short)
+    const int p = id - g0 * nblk;                 // position within the group
+    rank = p / gh;
+    head = g0 + p % gh;
+}
+
 // Where the rows of one (sequence, head) problem live.  Two layouts:
 //   fixed length  q/o/dO/dQ [B, H, Nq, d], k/v/dK/dV [B, Hkv, Nk, d]: head index b*H + h (or
 //                 b*Hkv + hk), row offset 0;
@@ -114,6 +134,7 @@ struct Layout {
     // Element extents of those buffers and of the per-row statistics (lse, Delta, base-2
     // LSE), checked in checked builds only.
     long long o_ext, do_ext, dq_ext, dk_ext, dv_ext, stat_ext;
+    int order_group;  // heads per group of the tensor-core kernels' tile order (tile_order)
 };
 
 // Rows of sequence b: global row offsets q0 / k0 and lengths nq / nk.  Packed offsets and

@@ -445,6 +445,46 @@ __device__ __forceinline__ void tmem_wait_st()
 }
 
 // ---------------------------------------------------------------------------------------
+// Cluster launch control (sm_100 family): a running CTA asks the hardware to cancel the launch of
+// a CTA of the same grid that has not started yet and takes over that CTA's work.  The 16-byte
+// response lands in shared memory and completes `bar` as a transaction of 16 bytes.  After a
+// response that reports no cancellation, no further request may be made.
+// ---------------------------------------------------------------------------------------
+// Warp-collective: one elected lane makes the request and announces the 16 bytes on `bar`.  The
+// proxy fence orders earlier generic reads of the response buffer before the new response.
+__device__ __forceinline__ void clc_try_cancel_w(void* resp, uint64_t* bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e fence.proxy.async.shared::cta;\n\t"
+        "@e clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+        " [%0], [%1];\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], 16;\n\t}" ::"r"(smem_u32(resp)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The x index of the CTA whose launch the response cancelled, or -1 if none was (the grid has no
+// CTA left to start).  Call after the response's barrier phase completed.
+__device__ __forceinline__ int clc_cancelled_x(const __int128* resp)
+{
+    const __int128 v = *resp;
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, %1;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "q"(v));
+    if (!ok) return -1;
+    asm volatile("clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, %1;"
+                 : "=r"(x)
+                 : "q"(v));
+    return static_cast<int>(x);
+}
+
+// ---------------------------------------------------------------------------------------
 // Small math helpers.
 // ---------------------------------------------------------------------------------------
 // Hardware base-2 exponential (MUFU.EX2); exp2(-inf) = +0.

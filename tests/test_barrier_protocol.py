@@ -127,6 +127,95 @@ def dq_protocol(n, ks=3, vs=2, e_per_parity=True, kv_waits_first=False, groups=4
     return progs, counts
 
 
+def dq_persistent_protocol(tiles, ks=3, vs=2, groups=4, use_of=lambda o: (o - 1) >> 1,
+                           qfree_commits=True):
+    """The persistent dQ kernel over a sequence of work tiles (key-block counts, 0 for a tile
+    without keys): the producer loads each tile's Q/dO once the previous tile's S and dP products
+    ran (qfree), streams K/V through the rings with block indices counted over the whole
+    sequence, then requests the next tile (cluster launch control; the response arrives
+    asynchronously) and publishes its index in a two-slot queue; the MMA warp and the elementwise
+    groups read every index and release its slot; the accumulator barrier completes once per
+    tile with keys."""
+    prod, mma = [], []
+    wk = lambda j: (W, ("kfull", j % ks), j // ks)  # noqa: E731
+    wv = lambda j: (W, ("vfull", j % vs), j // vs)  # noqa: E731
+
+    def dp(j):
+        return [wv(j), (C, ("dp", j & 1)), (C, ("vempty", j % vs))]
+
+    def s(j):
+        return ([(W, "sfree", j - 1)] if j > 0 else []) + [wk(j), (C, "s")]
+
+    # ordinal o >= 1 is use (o - 1) >> 1 of queue slot o & 1 (and of response slot o & 1)
+    def take(ti):  # consumers: read the index of ordinal ti + 1, release its slot
+        o = ti + 1
+        return [(W, ("tfull", o & 1), use_of(o)), (A, ("tempty", o & 1))]
+
+    g = at = 0
+    for ti, n in enumerate(tiles):
+        if n > 0:
+            if at > 0:
+                prod.append((W, "qfree", at - 1))
+            prod.append((C, "res"))
+            for it in range(n):
+                j = g + it
+                if j >= vs:
+                    prod.append((W, ("vempty", j % vs), j // vs - 1))
+                prod.append((C, ("vfull", j % vs)))
+                if j >= ks:
+                    prod.append((W, ("kempty", j % ks), j // ks - 1))
+                prod.append((C, ("kfull", j % ks)))
+            g += n
+            at += 1
+        o = ti + 1
+        # the next tile is requested after this tile's loads; the response lands asynchronously
+        prod += [(C, "clc"), (W, "clc", ti)]
+        if use_of(o) > 0:
+            prod.append((W, ("tempty", o & 1), use_of(o) - 1))
+        prod.append((A, ("tfull", o & 1)))
+    g = at = 0
+    for ti, n in enumerate(tiles):
+        if n > 0:
+            mma.append((W, "res", at))
+            mma += s(g) + dp(g)
+            if n > 1:
+                mma += dp(g + 1) + s(g + 1)
+            if n <= 2 and qfree_commits:
+                mma.append((C, "qfree"))
+            for it in range(n):
+                j = g + it
+                mma += [(W, ("e", j & 1), j >> 1), (C, ("kempty", j % ks))]
+                if it + 2 < n:
+                    mma += dp(j + 2) + s(j + 2)
+                    if it + 3 == n and qfree_commits:
+                        mma.append((C, "qfree"))
+            mma.append((C, "acc"))
+            g += n
+            at += 1
+        mma += take(ti)
+    progs = {"producer": prod, "mma": mma}
+    for h in range(groups):
+        prog, g, at = [], 0, 0
+        for ti, n in enumerate(tiles):
+            for it in range(n):
+                j = g + it
+                prog += [(W, "s", j), (A, "sfree"), (W, ("dp", j & 1), j >> 1), (A, ("e", j & 1))]
+            prog += take(ti)
+            if n > 0:
+                prog.append((W, "acc", at))
+                g += n
+                at += 1
+        progs[f"wg{h}"] = prog
+    counts = {"s": 1, "sfree": groups, ("dp", 0): 1, ("dp", 1): 1, "acc": 1, "res": 1, "qfree": 1}
+    counts |= {(x, i): 1 for x in ("vfull", "vempty") for i in range(vs)}
+    counts |= {(x, i): 1 for x in ("kfull", "kempty") for i in range(ks)}
+    counts |= {("e", b): groups for b in (0, 1)}
+    counts |= {("tfull", b): 1 for b in (0, 1)}
+    counts["clc"] = 1
+    counts |= {("tempty", b): groups + 1 for b in (0, 1)}
+    return progs, counts
+
+
 # ----------------------------------------------------------------------------- dK/dV kernel
 
 def dkv_protocol(n, qs=3, gs=2, groups=2, chunks=2):
@@ -216,6 +305,172 @@ def fwd_protocol(j0, j1, stages=2, split=True):
     return progs, counts
 
 
+def fwd_persistent_protocol(tiles, stages=2, split=True):
+    """The persistent forward over a sequence of query-tile pairs, each given as (J0, J1), the key
+    blocks its two query tiles visit (0 for an empty slot or a tile that sees no key).  K/V blocks
+    are counted over the whole sequence for the rings; each query-tile slot counts its own S
+    products for its S and P barriers and its finished pairs for its O barrier; the producer loads
+    a pair's Q tiles once the previous pair's S products have run (qfree); tile indices go through
+    the two-slot queue as in the backward."""
+    halves = (0, 1) if split else (1,)
+    wk = lambda j: (W, ("kfull", j % stages), j // stages)  # noqa: E731
+
+    def take(ti):
+        o = ti + 1
+        return [(W, ("tfull", o & 1), (o - 1) >> 1), (A, ("tempty", o & 1))]
+
+    prod, mma = [], []
+    gk = at = 0
+    for ti, (j0, j1) in enumerate(tiles):
+        jmax = max(j0, j1)
+        if jmax > 0:
+            if at > 0:
+                prod.append((W, "qfree", at - 1))
+            prod.append((C, "q"))
+            for j in range(gk, gk + jmax):
+                if j >= stages:
+                    prod.append((W, ("kempty", j % stages), j // stages - 1))
+                prod.append((C, ("kfull", j % stages)))
+                if j >= stages:
+                    prod.append((W, ("vempty", j % stages), j // stages - 1))
+                prod.append((C, ("vfull", j % stages)))
+            gk += jmax
+            at += 1
+        o = ti + 1
+        prod += [(C, "clc"), (W, "clc", ti)]
+        if (o - 1) >> 1 > 0:
+            prod.append((W, ("tempty", o & 1), ((o - 1) >> 1) - 1))
+        prod.append((A, ("tfull", o & 1)))
+    gk = at = 0
+    cs = [0, 0]
+    for ti, (j0, j1) in enumerate(tiles):
+        jt = (j0, j1)
+        jmax = max(jt)
+        if jmax > 0:
+            mma += [(W, "q", at), wk(gk)]
+            for t in (0, 1):
+                if jt[t] > 0:
+                    mma.append((C, ("sfull", t)))
+            mma.append((C, ("kempty", gk % stages)))
+            if jmax == 1:
+                mma.append((C, "qfree"))
+            for j in range(jmax):
+                gj = gk + j
+                mma.append((W, ("vfull", gj % stages), gj // stages))
+                k_next = False
+                for t in (0, 1):
+                    if j < jt[t]:
+                        mma += [(W, ("pfull", t, x), cs[t] + j) for x in halves]
+                        if j + 1 == jt[t]:
+                            mma.append((C, ("ofinal", t)))
+                        else:
+                            if not k_next:
+                                mma.append(wk(gj + 1))
+                            k_next = True
+                            mma.append((C, ("sfull", t)))
+                if k_next:
+                    mma.append((C, ("kempty", (gj + 1) % stages)))
+                if j + 2 == jmax:
+                    mma.append((C, "qfree"))
+                mma.append((C, ("vempty", gj % stages)))
+            cs = [cs[0] + j0, cs[1] + j1]
+            gk += jmax
+            at += 1
+        mma += take(ti)
+    progs = {"producer": prod, "mma": mma}
+    for t in (0, 1):
+        g, c, co = [], 0, 0
+        for ti, jts in enumerate(tiles):
+            for j in range(jts[t]):
+                g += [(W, ("sfull", t), c + j)] + [(A, ("pfull", t, x)) for x in halves]
+            g += take(ti)
+            if jts[t] > 0:
+                g.append((W, ("ofinal", t), co))
+                c += jts[t]
+                co += 1
+        progs[f"softmax{t}"] = g
+    counts = {"q": 1, "qfree": 1, "clc": 1}
+    counts |= {(x, i): 1 for x in ("kfull", "kempty", "vfull", "vempty") for i in range(stages)}
+    counts |= {(x, t): 1 for x in ("sfull", "ofinal") for t in (0, 1)}
+    counts |= {("pfull", t, x): 1 for t in (0, 1) for x in (0, 1)}
+    counts |= {("tfull", b): 1 for b in (0, 1)}
+    counts |= {("tempty", b): 3 for b in (0, 1)}  # both softmax groups and the MMA warp
+    return progs, counts
+
+
+def dkv_persistent_protocol(tiles, qs=3, gs=2):
+    """The persistent dK/dV kernel over a sequence of key-block tiles (streamed query blocks per
+    tile): K/V resident per tile and reloaded once its S^T and dP^T products have run (kvfree);
+    Q/dO rings and per-block barriers counted over the whole sequence."""
+    def take(ti):
+        o = ti + 1
+        return [(W, ("tfull", o & 1), (o - 1) >> 1), (A, ("tempty", o & 1))]
+
+    wq = lambda j: (W, ("qfull", j % qs), j // qs)  # noqa: E731
+    wg = lambda j: (W, ("gfull", j % gs), j // gs)  # noqa: E731
+    prod, mma = [], []
+    g = at = 0
+    for ti, n in enumerate(tiles):
+        if n > 0:
+            if at > 0:
+                prod.append((W, "kvfree", at - 1))
+            prod.append((C, "res"))
+            for j in range(g, g + n):
+                if j >= qs:
+                    prod.append((W, ("qempty", j % qs), j // qs - 1))
+                prod.append((C, ("qfull", j % qs)))
+                if j >= gs:
+                    prod.append((W, ("gempty", j % gs), j // gs - 1))
+                prod.append((C, ("gfull", j % gs)))
+            g += n
+            at += 1
+        o = ti + 1
+        prod += [(C, "clc"), (W, "clc", ti)]
+        if (o - 1) >> 1 > 0:
+            prod.append((W, ("tempty", o & 1), ((o - 1) >> 1) - 1))
+        prod.append((A, ("tfull", o & 1)))
+    g = at = 0
+    for ti, n in enumerate(tiles):
+        if n > 0:
+            mma += [(W, "res", at), wq(g), (C, "s"), wg(g), (C, "dp")]
+            if n == 1:
+                mma.append((C, "kvfree"))
+            for it in range(n):
+                j = g + it
+                mma += [(W, ("p", 0), j), (W, ("p", 1), j), (C, ("gempty", j % gs))]
+                if it + 1 < n:
+                    mma += [wq(j + 1), (C, "s")]
+                mma += [(W, ("e", 0), j), (W, ("e", 1), j), (C, ("qempty", j % qs))]
+                if it + 1 < n:
+                    mma += [wg(j + 1), (C, "dp")]
+                    if it + 2 == n:
+                        mma.append((C, "kvfree"))
+            mma.append((C, "acc"))
+            g += n
+            at += 1
+        mma += take(ti)
+    progs = {"producer": prod, "mma": mma}
+    for h in (0, 1):
+        prog, g, at = [], 0, 0
+        for ti, n in enumerate(tiles):
+            for j in range(g, g + n):
+                prog += [(W, "s", j), (A, ("p", 0)), (A, ("p", 1)), (W, "dp", j), (A, ("e", 0)),
+                         (A, ("e", 1))]
+            prog += take(ti)
+            if n > 0:
+                prog.append((W, "acc", at))
+                g += n
+                at += 1
+        progs[f"wg{h}"] = prog
+    counts = {"s": 1, "dp": 1, "acc": 1, "res": 1, "kvfree": 1, "clc": 1}
+    counts |= {(x, c): 2 for x in ("p", "e") for c in (0, 1)}
+    counts |= {(x, i): 1 for x in ("qfull", "qempty") for i in range(qs)}
+    counts |= {(x, i): 1 for x in ("gfull", "gempty") for i in range(gs)}
+    counts |= {("tfull", b): 1 for b in (0, 1)}
+    counts |= {("tempty", b): 3 for b in (0, 1)}  # both elementwise groups and the MMA warp
+    return progs, counts
+
+
 # ----------------------------------------------------------------------------- decode kernel
 
 def decode_protocol(J, stages=3):
@@ -270,6 +525,27 @@ def test_dq_protocol(n, groups):
     explore(lambda: dq_protocol(n, groups=groups))
 
 
+@pytest.mark.parametrize("tiles", [[1], [3], [1, 1, 1], [2, 5], [0, 3, 0, 0, 1], [4, 1, 2, 3, 1],
+                                   [1, 2, 1, 2, 1, 2, 1]])
+def test_dq_persistent_protocol(tiles):
+    explore(lambda: dq_persistent_protocol(tiles))
+
+
+def test_persistent_model_catches_a_missing_qfree_commit():
+    """Without the MMA warp's commit after a tile's last S and dP products, the producer never
+    loads the next tile's Q and dO: the model must report the deadlock."""
+    with pytest.raises(Hazard, match="deadlock"):
+        explore(lambda: dq_persistent_protocol([3, 3], qfree_commits=False), seeds=5)
+
+
+def test_persistent_model_catches_a_slot_phase_off_by_one():
+    """Ordinal o is use (o - 1) >> 1 of its slot: counting it as use o >> 1 makes the first use
+    of slot 0 wait for a parity that a fresh barrier already shows as complete, so a consumer
+    could read a tile index before it is written."""
+    with pytest.raises(Hazard):
+        explore(lambda: dq_persistent_protocol([1, 1, 1, 1], use_of=lambda o: o >> 1))
+
+
 @pytest.mark.parametrize("groups,chunks", [(2, 2), (4, 1)])
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7])
 def test_dkv_protocol(n, groups, chunks):
@@ -280,6 +556,19 @@ def test_dkv_protocol(n, groups, chunks):
 @pytest.mark.parametrize("j0,j1", [(1, 1), (1, 2), (2, 3), (3, 3), (4, 5), (0, 1), (6, 7)])
 def test_fwd_protocol(j0, j1, stages, split):
     explore(lambda: fwd_protocol(j0, j1, stages, split))
+
+
+@pytest.mark.parametrize("stages,split", [(2, False), (4, True)])
+@pytest.mark.parametrize("tiles", [[(1, 1)], [(3, 4)], [(1, 2), (2, 3), (1, 0)], [(0, 0), (2, 2), (0, 1)],
+                                   [(4, 5), (1, 1), (3, 3), (2, 0)], [(1, 1)] * 6,
+                                   [(6, 7), (2, 3), (5, 5)]])
+def test_fwd_persistent_protocol(tiles, stages, split):
+    explore(lambda: fwd_persistent_protocol(tiles, stages, split), seeds=150)
+
+
+@pytest.mark.parametrize("tiles", [[1], [3], [2, 1, 2], [0, 4, 0, 1], [5, 2, 3, 1], [1] * 6])
+def test_dkv_persistent_protocol(tiles):
+    explore(lambda: dkv_persistent_protocol(tiles))
 
 
 @pytest.mark.parametrize("stages", [3, 6])  # d = 128 and d = 64
