@@ -441,6 +441,17 @@ int fa_causal_block_counts(int q_block, int Br, int Bc, int N, int* n_full, int*
     return FA_OK;
 }
 
+int fa_tile_order(int id, int heads, int nblk, int gsize, int* head, int* rank)
+{
+    if (heads < 1 || nblk < 1 || gsize < 1 || id < 0 ||
+        static_cast<long long>(id) >= static_cast<long long>(heads) * nblk || !head || !rank)
+        return fail(FA_ERR_INVALID_ARG, "bad tile-order arguments");
+    fa::tile_order(id, heads, nblk, gsize, *head, *rank);
+    return FA_OK;
+}
+
+int fa_order_group(int N, int d, int causal) { return order_group(N, d, causal); }
+
 const char* fa_version(void) { return "fa-gb300 0.1 (sm_103a)"; }
 
 }  // extern "C"

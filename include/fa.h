@@ -324,6 +324,21 @@ const char* fa_last_error(void);
  * classification every kernel uses ("개선 3", two-stage causal split).  Host-only. */
 int fa_causal_block_counts(int q_block, int Br, int Bc, int N, int* n_full, int* n_masked);
 
+/* Order of the work tiles of the tensor-core kernels, host copy (tests and schedulers).  A
+ * launch over `heads` heads of `nblk` tiles each runs tile index `id` (its CTA index, or the index
+ * of a CTA whose launch it took over) as (*head, *rank), rank 0 being a head's heaviest tile
+ * under the causal mask.  Heads go in groups of `gsize`: within a group the tiles go by rank, the
+ * group's heads interleaved, so a group's heaviest tiles start first and its light ones fill the
+ * end; gsize = 1 is head-major order.  Returns FA_OK, or FA_ERR_INVALID_ARG for arguments out of
+ * range.  Host-only. */
+int fa_tile_order(int id, int heads, int nblk, int gsize, int* head, int* rank);
+
+/* The group size the fixed-length entry points pass to their kernels for sequences of N rows and
+ * head dimension d: 1 without the causal mask (every tile costs the same); under it, as many
+ * heads as keep one head's streamed rows (4 N d bytes) within 32 MB of L2, at most 16.
+ * Host-only. */
+int fa_order_group(int N, int d, int causal);
+
 /* Library version string. */
 const char* fa_version(void);
 

@@ -291,3 +291,43 @@ def test_grouped_fixed_length_rejects_bad_arguments(lib):
 
     assert bcall(ws=None) == -4
     assert bcall(nbytes=16) == -4
+
+
+def _order(lib, id_, heads, nblk, gsize):
+    h, r = ctypes.c_int(), ctypes.c_int()
+    assert lib.fa_tile_order(id_, heads, nblk, gsize, ctypes.byref(h), ctypes.byref(r)) == 0
+    return h.value, r.value
+
+
+@pytest.mark.parametrize("heads,nblk,gsize", [(1, 1, 1), (64, 32, 16), (64, 32, 8), (7, 5, 3),
+                                              (32, 250, 1), (5, 9, 16), (3, 4, 2)])
+def test_tile_order_reaches_every_tile_once_heaviest_first_within_groups(lib, heads, nblk, gsize):
+    """Every (head, rank) pair is reached by exactly one tile index; within a group of heads the
+    ranks never decrease along the launch order (the heaviest tiles start first), the group's
+    heads are interleaved, and groups follow one another."""
+    seen = [_order(lib, i, heads, nblk, gsize) for i in range(heads * nblk)]
+    assert sorted(seen) == [(h, r) for h in range(heads) for r in range(nblk)]
+    for i, (h, r) in enumerate(seen):
+        g0 = (h // gsize) * gsize
+        gh = min(gsize, heads - g0)
+        # the explicit position of (h, r): its group's start, then rank-major, head-minor
+        assert i == g0 * nblk + r * gh + (h - g0), (i, h, r)
+    if gsize == 1:  # head-major
+        assert seen == [(h, r) for h in range(heads) for r in range(nblk)]
+
+
+def test_tile_order_rejects_out_of_range_arguments(lib):
+    h, r = ctypes.c_int(), ctypes.c_int()
+    for args in ((-1, 2, 2, 1), (4, 2, 2, 1), (0, 0, 2, 1), (0, 2, 0, 1), (0, 2, 2, 0)):
+        assert lib.fa_tile_order(*args, ctypes.byref(h), ctypes.byref(r)) == -1
+
+
+def test_order_group_follows_the_l2_budget(lib):
+    """Head-major without the causal mask; under it as many heads as keep 4 N d bytes each
+    within 32 MB, between 1 and 16."""
+    assert lib.fa_order_group(4096, 128, 0) == 1
+    assert lib.fa_order_group(4096, 128, 1) == 16      # 2 MB per head
+    assert lib.fa_order_group(8192, 128, 1) == 8       # 4 MB per head
+    assert lib.fa_order_group(32000, 128, 1) == 2      # 16.4 MB per head
+    assert lib.fa_order_group(131072, 128, 1) == 1     # 67 MB per head
+    assert lib.fa_order_group(512, 64, 1) == 16
