@@ -84,3 +84,14 @@ def test_source_hash_ignores_comments_but_not_code():
     h = bench.kernel_source_sha256(k)
     assert re.fullmatch(r"[0-9a-f]{64}", h)
     assert bench.kernel_source_sha256(k) == h
+
+
+def test_fp8_entry_prefers_the_measured_gemm_and_keeps_the_assumed_ratio():
+    peaks = {"bf16_tflops": 2000.0}
+    e = bench.fp8_entry({"ms": 1.0, "tflops": 2400.0}, 3000.0, peaks)
+    assert e["fp8_peak"] == 3000.0 and e["frac_of_fp8_peak"] == pytest.approx(0.8)
+    assert e["fp8_peak_assumed"] == 4000.0 and e["frac_of_assumed_fp8_peak"] == pytest.approx(0.6)
+    assert "measured" in e["fp8_peak_kind"]
+    e = bench.fp8_entry({"ms": 1.0, "tflops": 2400.0}, None, peaks)
+    assert e["fp8_peak"] == 4000.0 and e["frac_of_fp8_peak"] == pytest.approx(0.6)
+    assert "assumed" in e["fp8_peak_kind"]

@@ -3,6 +3,8 @@ library's own forward) against the fp64 oracle backward, which recomputes its ow
 ragged tails, the fp32 path, the SIMT cross-check, canaries, determinism and the named
 workloads at full size (every head at N = 4096; at N = 32000 the oracle's row mode on 64
 sampled query rows and 64 key rows; identities at every head)."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -97,9 +99,12 @@ def test_workload_bwd_b4h16_n4096_d128_causal():
     got = run(x, w.causal)
     g = {n: got[n].cpu() for n in ("dq", "dk", "dv")}
     # each oracle thread holds P and dP of one head
-    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal,
-                               nthreads=oracle_threads(16.0 * w.N * (w.N + 2 * w.d) + 64e6))
+    nthr = oracle_threads(16.0 * w.N * (w.N + 2 * w.d) + 64e6)
+    t0 = time.perf_counter()
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, nthreads=nthr)
+    oracle_s = time.perf_counter() - t0
     stats = check_grads(g, ref, torch.bfloat16, w.name)
+    stats["oracle_s"], stats["oracle_threads"] = oracle_s, nthr
     for n in ("dq", "dk", "dv"):
         per_head = [rel_l2(g[n][b, h], ref[n][b, h]) for b in range(w.B) for h in range(w.H)]
         stats["worst_head_" + n] = max(per_head)
@@ -148,6 +153,7 @@ def test_workload_long_sequence_sampled_rows():
     assert sum(len(r) for r in key_rows.values()) == 64
     gq, rq = [], []
     gk, rk, gv, rv = [], [], [], []
+    t0 = time.perf_counter()
     for h in sorted(set(by_head) | set(key_rows)):
         rows = by_head.get(h, [])
         krows = key_rows.get(h, [])
@@ -164,6 +170,6 @@ def test_workload_long_sequence_sampled_rows():
     e_k = rel_l2(np.concatenate(gk), np.concatenate(rk))
     e_v = rel_l2(np.concatenate(gv), np.concatenate(rv))
     record_stats(w.name, {"dq_rows": sum(len(r) for r in gq), "dkv_rows": 64, "dq": e_q,
-                          "dk": e_k, "dv": e_v})
+                          "dk": e_k, "dv": e_v, "oracle_s": time.perf_counter() - t0})
     assert e_q <= TOL_GRAD_REL_L2 and e_k <= TOL_GRAD_REL_L2 and e_v <= TOL_GRAD_REL_L2
     check_gradient_identities(x, g, w)

@@ -2,6 +2,8 @@
 element, on seeded inputs.  Covers the fp32 SIMT path, the bf16 tensor-core path with ragged
 tails, canary guard regions, and the named workloads at their full sizes (every head of the
 N = 4096 and N = 8192 workloads; sampled rows at N = 32000)."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -47,9 +49,11 @@ def test_workload_fp32_n512_d64():
     w = WORKLOADS["fp32_b1h1_n512_d64"]
     x = generate(w)
     o, lse = run_fwd(x, w.causal)
+    t0 = time.perf_counter()
     ro, rl = oracle.attention_fwd(x["q"], x["k"], x["v"], w.scale, w.causal)
     stats = check_fwd(o, lse, ro, rl, torch.float32, w.name)
-    print(w.name, stats)
+    stats["oracle_s"] = time.perf_counter() - t0
+    record_stats(w.name, stats)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -111,11 +115,14 @@ def test_workload_full_size_every_head(name):
     nthr = oracle_threads(8.0 * w.N * (w.N + w.d) + 64e6)
     ro = np.empty(tuple(o_cpu.shape))
     rl = np.empty(tuple(lse_cpu.shape))
+    t0 = time.perf_counter()
     for b in range(w.B):
         rob, rlb = oracle.attention_fwd(x["q"][b:b + 1], x["k"][b:b + 1], x["v"][b:b + 1],
                                         w.scale, w.causal, nthreads=nthr)
         ro[b], rl[b] = rob[0], rlb[0]
+    oracle_s = time.perf_counter() - t0
     stats = check_fwd(o_cpu, lse_cpu, ro, rl, torch.bfloat16, name)
+    stats["oracle_s"], stats["oracle_threads"] = oracle_s, nthr
     # the worst head by max |dO|, for the record
     per_head = np.abs(f64(o_cpu) - ro).reshape(w.B * w.H, -1).max(axis=1)
     stats["heads"] = w.B * w.H
@@ -139,8 +146,18 @@ def test_workload_long_sequence_sampled_rows():
     by_head = {}
     for h, i in x["samples"]:
         by_head.setdefault(h, []).append(i)
+    got_o, got_l, ref_o, ref_l = [], [], [], []
+    t0 = time.perf_counter()
     for h, rows in sorted(by_head.items()):
         res = oracle.attention_rows_head(x["q"][0, h], x["k"][0, h], x["v"][0, h],
                                          torch.zeros(w.N, w.d), w.scale, w.causal, rows, [])
-        check_fwd(o_cpu[0, h, rows], lse_cpu[0, h, rows], res["o"], res["lse"], torch.bfloat16,
-                  f"N=32000 h={h}", check_mean=False)
+        got_o.append(f64(o_cpu[0, h, rows]))
+        got_l.append(f64(lse_cpu[0, h, rows]))
+        ref_o.append(res["o"])
+        ref_l.append(res["lse"])
+    oracle_s = time.perf_counter() - t0
+    stats = check_fwd(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o),
+                      np.concatenate(ref_l), torch.bfloat16, "N=32000 sampled rows",
+                      check_mean=False)
+    stats["rows"], stats["oracle_s"] = sum(len(r) for r in got_o), oracle_s
+    record_stats(w.name + " forward", stats)
