@@ -9,7 +9,10 @@ arrivals of one issuer keep their order, as MMAs complete in issue order.
 A wait is ``mbarrier.try_wait.parity``: it passes when the barrier's current phase parity
 differs from the parity asked for.  The model flags
   * a wait that passes while the barrier is not exactly one phase past the one the role wants
-    (a missed or an early phase: the parity test cannot tell them apart), and
+    (a missed or an early phase: the parity test cannot tell them apart),
+  * an arrival, where the model names the phase it is meant for, that lands in another phase
+    (on a barrier that several roles arrive at, one role running ahead could complete an
+    earlier phase in place of another), and
   * a schedule in which no role can move while some have not finished (deadlock).
 Random schedules explore the interleavings that the kernels' timing normally hides; the dQ
 kernel's dS barrier was a single barrier per warpgroup until this model (and a variant that
@@ -37,7 +40,9 @@ def run(progs: dict, counts: dict, rng: random.Random) -> None:
     pc = {r: 0 for r in progs}
     asyncq = {r: [] for r in progs}    # in-order asynchronous arrivals issued by each role
 
-    def arrive(b):
+    def arrive(b, ph=None):
+        if ph is not None and done[b] != ph:
+            raise Hazard(f"arrival for phase {ph} of {b} landed in phase {done[b]}")
         pend[b] += 1
         if pend[b] == counts[b]:
             pend[b] = 0
@@ -59,7 +64,7 @@ def run(progs: dict, counts: dict, rng: random.Random) -> None:
             return
         kind, r = rng.choice(moves)
         if kind == "async":
-            arrive(asyncq[r].pop(0))
+            arrive(*asyncq[r].pop(0))
             continue
         op, b, *k = progs[r][pc[r]]
         pc[r] += 1
@@ -67,9 +72,9 @@ def run(progs: dict, counts: dict, rng: random.Random) -> None:
             if done[b] != k[0] + 1:
                 raise Hazard(f"{r}: wait for phase {k[0]} of {b} passed with {done[b]} completed")
         elif op == A:
-            arrive(b)
+            arrive(b, *k)
         else:
-            asyncq[r].append(b)
+            asyncq[r].append((b, *k))
 
 
 # ----------------------------------------------------------------------------- dQ kernel
@@ -311,7 +316,8 @@ def fwd_persistent_protocol(tiles, stages=2, split=True):
     are counted over the whole sequence for the rings; each query-tile slot counts its own S
     products for its S and P barriers and its finished pairs for its O barrier; the producer loads
     a pair's Q tiles once the previous pair's S products have run (qfree); tile indices go through
-    the two-slot queue as in the backward."""
+    the two-slot queue as in the backward.  Releases of the K / V ring stages name their
+    phase."""
     halves = (0, 1) if split else (1,)
     wk = lambda j: (W, ("kfull", j % stages), j // stages)  # noqa: E731
 
@@ -351,7 +357,7 @@ def fwd_persistent_protocol(tiles, stages=2, split=True):
             for t in (0, 1):
                 if jt[t] > 0:
                     mma.append((C, ("sfull", t)))
-            mma.append((C, ("kempty", gk % stages)))
+            mma.append((C, ("kempty", gk % stages), gk // stages))
             if jmax == 1:
                 mma.append((C, "qfree"))
             for j in range(jmax):
@@ -369,10 +375,10 @@ def fwd_persistent_protocol(tiles, stages=2, split=True):
                             k_next = True
                             mma.append((C, ("sfull", t)))
                 if k_next:
-                    mma.append((C, ("kempty", (gj + 1) % stages)))
+                    mma.append((C, ("kempty", (gj + 1) % stages), (gj + 1) // stages))
                 if j + 2 == jmax:
                     mma.append((C, "qfree"))
-                mma.append((C, ("vempty", gj % stages)))
+                mma.append((C, ("vempty", gj % stages), gj // stages))
             cs = [cs[0] + j0, cs[1] + j1]
             gk += jmax
             at += 1
@@ -566,6 +572,7 @@ def test_fwd_persistent_protocol(tiles, stages, split):
     explore(lambda: fwd_persistent_protocol(tiles, stages, split), seeds=150)
 
 
+
 @pytest.mark.parametrize("tiles", [[1], [3], [2, 1, 2], [0, 4, 0, 1], [5, 2, 3, 1], [1] * 6])
 def test_dkv_persistent_protocol(tiles):
     explore(lambda: dkv_persistent_protocol(tiles))
@@ -590,3 +597,12 @@ def test_model_catches_a_deadlock():
     progs = {"producer": [(W, "empty", 0), (C, "full")], "consumer": [(W, "full", 0), (C, "empty")]}
     with pytest.raises(Hazard, match="deadlock"):
         run(progs, {"empty": 1, "full": 1}, random.Random(0))
+
+
+def test_model_catches_an_arrival_in_the_wrong_phase():
+    """Two roles release a barrier of count 2 once per phase; one that releases two phases
+    without waiting completes the first phase in place of the other role."""
+    progs = {"fast": [(A, "bar", 0), (A, "bar", 1), (A, "go")],
+             "slow": [(W, "go", 0), (A, "bar", 0), (A, "bar", 1)]}
+    with pytest.raises(Hazard, match="landed in phase"):
+        run(progs, {"bar": 2, "go": 1}, random.Random(0))
