@@ -13,7 +13,10 @@ differs from the parity asked for.  The model flags
   * an arrival, where the model names the phase it is meant for, that lands in another phase
     (on a barrier that several roles arrive at, one role running ahead could complete an
     earlier phase in place of another), and
-  * a schedule in which no role can move while some have not finished (deadlock).
+  * a schedule in which no role can move while some have not finished (deadlock), and
+  * in models that track a buffer's contents (a TMEM region several products take turns in):
+    a product issued into the buffer while some reader has not released its previous contents,
+    or a read that finds other contents than the role expects.
 Random schedules explore the interleavings that the kernels' timing normally hides; the dQ
 kernel's dS barrier was a single barrier per warpgroup until this model (and a variant that
 moved the K/V waits) showed that the warpgroups can complete two of its phases before the MMA
@@ -28,6 +31,10 @@ import pytest
 # ----------------------------------------------------------------------------- engine
 
 W, A, C = "wait", "arrive", "commit"  # C: asynchronous arrive (TMA completion or tcgen05.commit)
+# Buffer contents: WR (buffer, label, readers) when a product into the buffer is issued (the
+# earliest moment it may write), RD (buffer, label) when a role reads it, RL (buffer) when that
+# role is done with it.
+WR, RD, RL = "write", "read", "release"
 
 
 class Hazard(AssertionError):
@@ -39,6 +46,7 @@ def run(progs: dict, counts: dict, rng: random.Random) -> None:
     pend = {b: 0 for b in counts}      # arrivals in the current phase
     pc = {r: 0 for r in progs}
     asyncq = {r: [] for r in progs}    # in-order asynchronous arrivals issued by each role
+    bufs = {}                          # buffer -> [label, readers not yet released]
 
     def arrive(b, ph=None):
         if ph is not None and done[b] != ph:
@@ -68,7 +76,16 @@ def run(progs: dict, counts: dict, rng: random.Random) -> None:
             continue
         op, b, *k = progs[r][pc[r]]
         pc[r] += 1
-        if op == W:
+        if op == WR:
+            if bufs.get(b, [None, 0])[1] > 0:
+                raise Hazard(f"{r}: {k[0]} issued into {b} while {bufs[b][0]} is unread")
+            bufs[b] = [k[0], k[1]]
+        elif op == RD:
+            if bufs.get(b, [None])[0] != k[0]:
+                raise Hazard(f"{r}: read {k[0]} from {b}, which holds {bufs.get(b, [None])[0]}")
+        elif op == RL:
+            bufs[b][1] -= 1
+        elif op == W:
             if done[b] != k[0] + 1:
                 raise Hazard(f"{r}: wait for phase {k[0]} of {b} passed with {done[b]} completed")
         elif op == A:
@@ -404,10 +421,12 @@ def fwd_persistent_protocol(tiles, stages=2, split=True):
     return progs, counts
 
 
-def dkv_persistent_protocol(tiles, qs=3, gs=2):
+def dkv_persistent_protocol(tiles, qs=3, gs=2, s_waits_p=True):
     """The persistent dK/dV kernel over a sequence of key-block tiles (streamed query blocks per
     tile): K/V resident per tile and reloaded once its S^T and dP^T products have run (kvfree);
-    Q/dO rings and per-block barriers counted over the whole sequence."""
+    Q/dO rings and per-block barriers counted over the whole sequence.  The TMEM buffers X (S^T,
+    then P^T over it) and Y (dP^T, then dS^T) are tracked: S^T(j+1) may only be issued once
+    both groups have turned S^T(j) into P^T (s_waits_p=False issues it before that wait)."""
     def take(ti):
         o = ti + 1
         return [(W, ("tfull", o & 1), (o - 1) >> 1), (A, ("tempty", o & 1))]
@@ -438,17 +457,21 @@ def dkv_persistent_protocol(tiles, qs=3, gs=2):
     g = at = 0
     for ti, n in enumerate(tiles):
         if n > 0:
-            mma += [(W, "res", at), wq(g), (C, "s"), wg(g), (C, "dp")]
+            mma += [(W, "res", at), wq(g), (WR, "X", ("S", g), 2), (C, "s"), wg(g),
+                    (WR, "Y", ("dP", g), 2), (C, "dp")]
             if n == 1:
                 mma.append((C, "kvfree"))
             for it in range(n):
                 j = g + it
+                s_next = [wq(j + 1), (WR, "X", ("S", j + 1), 2), (C, "s")] if it + 1 < n else []
+                if not s_waits_p:
+                    mma += s_next
                 mma += [(W, ("p", 0), j), (W, ("p", 1), j), (C, ("gempty", j % gs))]
-                if it + 1 < n:
-                    mma += [wq(j + 1), (C, "s")]
+                if s_waits_p:
+                    mma += s_next
                 mma += [(W, ("e", 0), j), (W, ("e", 1), j), (C, ("qempty", j % qs))]
                 if it + 1 < n:
-                    mma += [wg(j + 1), (C, "dp")]
+                    mma += [wg(j + 1), (WR, "Y", ("dP", j + 1), 2), (C, "dp")]
                     if it + 2 == n:
                         mma.append((C, "kvfree"))
             mma.append((C, "acc"))
@@ -460,7 +483,9 @@ def dkv_persistent_protocol(tiles, qs=3, gs=2):
         prog, g, at = [], 0, 0
         for ti, n in enumerate(tiles):
             for j in range(g, g + n):
-                prog += [(W, "s", j), (A, ("p", 0)), (A, ("p", 1)), (W, "dp", j), (A, ("e", 0)),
+                # each group loads its columns, writes its half-results back, then signals
+                prog += [(W, "s", j), (RD, "X", ("S", j)), (A, ("p", 0)), (RL, "X"), (A, ("p", 1)),
+                         (W, "dp", j), (RD, "Y", ("dP", j)), (A, ("e", 0)), (RL, "Y"),
                          (A, ("e", 1))]
             prog += take(ti)
             if n > 0:
@@ -576,6 +601,13 @@ def test_fwd_persistent_protocol(tiles, stages, split):
 @pytest.mark.parametrize("tiles", [[1], [3], [2, 1, 2], [0, 4, 0, 1], [5, 2, 3, 1], [1] * 6])
 def test_dkv_persistent_protocol(tiles):
     explore(lambda: dkv_persistent_protocol(tiles))
+
+
+def test_dkv_model_catches_s_over_an_unread_buffer():
+    """S^T of the next block issued before both groups have read S^T and written P^T: the
+    product may overwrite the buffer they still read."""
+    with pytest.raises(Hazard, match="unread"):
+        explore(lambda: dkv_persistent_protocol([4, 3], s_waits_p=False))
 
 
 @pytest.mark.parametrize("stages", [3, 6])  # d = 128 and d = 64

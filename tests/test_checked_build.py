@@ -237,3 +237,22 @@ def test_shrunk_extents_are_caught(checked):
     # back to normal: no report
     fa.forward_varlen(q, k, v, cu_q, cu_k, 200, 200, causal=True)
     fa.fa_device_status()
+
+
+def test_shrunk_extents_are_caught_in_the_fixed_length_backward(checked):
+    """The same hook on the fixed-length bf16 backward (the preprocess, the dK/dV kernel's
+    stores and the dQ kernel's stores are all checked); with the hook off again the call
+    reports nothing."""
+    z = random_qkv(1, 2, 130, 128, seed=9)
+    q, k, v, do = (z[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True)
+    fa.fa_device_status()
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 2, 130, 128), dtype=torch.uint8, device="cuda")
+    grads = [torch.empty_like(t) for t in (q, k, v)]
+    checked.fa_debug_set_flags(SHRINK_EXTENTS)
+    try:
+        expect_out_of_bounds(lambda: fa.fa_bwd(q, k, v, o, do, lse, *grads, 0.1, True, ws))
+    finally:
+        checked.fa_debug_set_flags(0)
+    fa.fa_bwd(q, k, v, o, do, lse, *grads, 0.1, True, ws)
+    fa.fa_device_status()
