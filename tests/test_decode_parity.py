@@ -36,7 +36,7 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("splits", [1, 3, 16])
+@pytest.mark.parametrize("splits", [1, 2, 3, 8, 9, 16])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("case", list(CASES))
@@ -67,7 +67,7 @@ def test_decode_outputs_stay_inside_their_buffers_and_are_deterministic():
     x = random_varlen(lens_q, lens_k, H, Hkv, d, seed=8, with_do=False)
     q, k, v, cu_q, cu_k = (x[n].cuda() for n in ("q", "k", "v", "cu_q", "cu_k"))
     tq = q.shape[0]
-    for splits in (1, 4):
+    for splits in (1, 4, 16):  # one range, merged in the kernel, merged by the combine kernel
         outs = []
         for _ in range(2):
             o, co = guarded_empty((tq, H, d), torch.bfloat16)
