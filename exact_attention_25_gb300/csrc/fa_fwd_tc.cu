@@ -14,7 +14,7 @@
 // TMEM columns: S_t at [128t, 128t+128) (fp32), P_t (bf16 pairs) aliased on the upper half
 // of S_t, O_t at [256 + t*d, 256 + (t+1)*d) (fp32, un-normalised); at d = 64, O_t at
 // [256 + 128t, 384 + 128t), whose column 64 accumulates the row sum of the bf16 P (the P V
-// product runs at N = 128 against V and a constant ones-column panel).  At d = 64 and for
+// product runs at N = 80 against V and a constant ones-column panel).  At d = 64 and for
 // e4m3 the softmax warps signal P in two halves of 64 keys and the MMA warp issues each half
 // of the P V product as soon as it has landed (FwdCfg::SPLIT_P).
 //
@@ -48,9 +48,10 @@ struct FwdCfg {
     static constexpr int SMEM_Q = NT * TILE_BYTES;
     static constexpr int SMEM_K = STAGES * TILE_BYTES;
     static constexpr int SMEM_V = STAGES * TILE_BYTES;
-    // d = 64: the P V product runs at N = 128 against V and a constant panel whose first column
-    // is 1.0, so O's column 64 accumulates the sum of the bf16 P weights on the tensor core
-    // (the row sum that normalises O), instead of ~190 softmax instructions per row and block.
+    // d = 64: the P V product runs at N = 80 against V and the first 16 columns of a constant
+    // panel whose first column is 1.0, so O's column 64 accumulates the sum of the bf16 P
+    // weights on the tensor core (the row sum that normalises O), instead of ~190 softmax
+    // instructions per row and block.
     static constexpr bool SUM_ON_MMA = (D == 64 && !F8);
     static constexpr int O_COLS = SUM_ON_MMA ? 128 : D;  // TMEM columns of one O accumulator
     static constexpr int SMEM_ONES = SUM_ON_MMA ? PANEL_BYTES : 0;
@@ -371,8 +372,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
         // the whole warp runs the loop (warp-uniform values); elect.sync picks the issuer
         constexpr uint32_t kIdS = F8 ? idesc_e4m3_f32(128, C::BN)  // S = Q K^T
                                      : idesc_bf16_f32(128, C::BN, 0, 0);
+        // (d = 64: N = 80 covers V's 64 columns and the first 16 of the constant panel, whose
+        // column 0 gives the row sum; the rest of the panel is zero and needs no product)
         constexpr uint32_t kIdPV = F8 ? idesc_e4m3_f32(128, D)  // O += P V
-                                      : idesc_bf16_f32(128, C::O_COLS, 0, 1);
+                                      : idesc_bf16_f32(128, C::SUM_ON_MMA ? D + 16 : D, 0, 1);
         // Everything the issue loop needs lives in scalar registers: base descriptors are
         // built once and advanced by byte offsets (stage, tile, k-step), so the single
         // issuing thread keeps pace with the tensor core.
