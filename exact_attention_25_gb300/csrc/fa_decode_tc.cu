@@ -438,8 +438,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
 // Merge of the split ranges of every (token, head) row: one warp per row, each lane owning
 // d / 32 columns.  With M = max_s lse_s and w_s = e^{lse_s - M}:
 //   O = sum_s w_s O_s / sum_s w_s,   lse = M + log sum_s w_s;
-// a row whose ranges all saw no key (M = -inf) gets O = 0 and lse = -inf.
-template <int D>
+// a row whose ranges all saw no key (M = -inf) gets O = 0 and lse = -inf.  The ranges go in
+// batches of SB (2, 4 or 8, the smallest that holds all ranges, else 8) whose LSE and
+// partial-O loads are all issued before any is used (one memory round trip per batch);
+// batches merge by the same rule, the running sums rescaled to the running max.
+template <int D, int SB>
 __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodeParams p)
 {
     constexpr int EPL = D / 32;  // columns per lane
@@ -454,32 +457,48 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodePara
          row < rows; row += warps_total) {
         const size_t t = row / L.H;
         const int h = static_cast<int>(row - t * L.H);
-        float mx = -INFINITY;
-        for (int s = 0; s < p.splits; ++s)
-            mx = fmaxf(mx, p.lse_part[(static_cast<size_t>(s) * L.H + h) * L.Rq + t]);
+        float mx = -INFINITY, wsum = 0.0f;
         float acc[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-        float wsum = 0.0f;
-        if (mx != -INFINITY) {
-            for (int s = 0; s < p.splits; ++s) {
-                const float w = expf(p.lse_part[(static_cast<size_t>(s) * L.H + h) * L.Rq + t] - mx);
-                if (w == 0.0f) continue;  // the same for every lane of the warp
-                wsum += w;
-                const float* src =
-                    p.o_part + ((static_cast<size_t>(s) * L.Rq + t) * L.H + h) * D + lane * EPL;
-                if constexpr (EPL == 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(src);
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
-                    acc[2] = fmaf(w, v.z, acc[2]);
-                    acc[3] = fmaf(w, v.w, acc[3]);
-                } else {
-                    const float2 v = *reinterpret_cast<const float2*>(src);
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
+        for (int s0 = 0; s0 < p.splits; s0 += SB) {
+            float ls[SB];
+            float v[SB][EPL];
+#pragma unroll
+            for (int k = 0; k < SB; ++k) {
+                const int s = s0 + k;
+                ls[k] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) v[k][e] = 0.0f;
+                if (s < p.splits) {
+                    ls[k] = p.lse_part[(static_cast<size_t>(s) * L.H + h) * L.Rq + t];
+                    const float* src =
+                        p.o_part + ((static_cast<size_t>(s) * L.Rq + t) * L.H + h) * D + lane * EPL;
+                    if constexpr (EPL == 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(src);
+                        v[k][0] = x.x; v[k][1] = x.y; v[k][2] = x.z; v[k][3] = x.w;
+                    } else {
+                        const float2 x = *reinterpret_cast<const float2*>(src);
+                        v[k][0] = x.x; v[k][1] = x.y;
+                    }
                 }
             }
+            float bm = mx;
+#pragma unroll
+            for (int k = 0; k < SB; ++k) bm = fmaxf(bm, ls[k]);
+            if (bm == -INFINITY) continue;  // no range so far saw a key (the same for the warp)
+            const float rs = (mx == -INFINITY) ? 0.0f : expf(mx - bm);  // rescale the running sums
+            wsum *= rs;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] *= rs;
+#pragma unroll
+            for (int k = 0; k < SB; ++k) {
+                const float w = (ls[k] == -INFINITY) ? 0.0f : expf(ls[k] - bm);
+                wsum += w;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, v[k][e], acc[e]);
+            }
+            mx = bm;
         }
         const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
         const size_t o_off = t * L.o_rs + static_cast<size_t>(h) * L.o_hs;
@@ -531,7 +550,9 @@ static cudaError_t launch_decode_impl(const CUtensorMap& tq, const CUtensorMap& 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D>, p);
+    if (p.splits <= 2) return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D, 2>, p);
+    if (p.splits <= 4) return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D, 4>, p);
+    return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D, 8>, p);
 }
 
 cudaError_t launch_decode(int d, const CUtensorMap& tq, const CUtensorMap& tk,
