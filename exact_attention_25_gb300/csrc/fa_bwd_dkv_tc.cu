@@ -547,38 +547,31 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
             if (n_it > 0) {
                 if (ok && warp_wait_all(&bar_acc, at & 1, wd, kSiteBwdEltAcc)) {
                     tc_fence_after();
+                    const size_t offv = static_cast<size_t>(t.sr.k0 + krow) * L.dv_rs +
+                                        static_cast<size_t>(t.khead) * L.dv_hs;
+                    const size_t offk = static_cast<size_t>(t.sr.k0 + krow) * L.dk_rs +
+                                        static_cast<size_t>(t.khead) * L.dk_hs;
+                    const bool inv = krow < nk && in_extent(offv, D, L.dv_ext, p.status);
+                    const bool ink = krow < nk && in_extent(offk, D, L.dk_ext, p.status);
+                    // dV and dK of the same 32 columns in one Tensor Memory round trip
 #pragma unroll 1
-                    for (int which = 0; which < 2; ++which) {
-                        const uint32_t tAcc = which == 0 ? tDV : tDK;
-                        const float mul = which == 0 ? 1.0f : p.scale;
-                        const long long rs = which == 0 ? L.dv_rs : L.dk_rs;
-                        const long long hs = which == 0 ? L.dv_hs : L.dk_hs;
-                        const size_t off = static_cast<size_t>(t.sr.k0 + krow) * rs +
-                                           static_cast<size_t>(t.khead) * hs;
-                        __nv_bfloat16* dst_row =
-                            static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + off;
-                        const bool in = krow >= nk ||
-                                        in_extent(off, D, which == 0 ? L.dv_ext : L.dk_ext, p.status);
-#pragma unroll 1
-                        for (int ch = 0; ch < D / 64; ++ch) {
-                            const int c0 = h * (D / 2) + 32 * ch;
-                            uint32_t a[32];
-                            tmem_ld32(tAcc + c0, a);
-                            tmem_wait_ld();
-                            reg_fence32(a);
-                            uint32_t packed_v[16];
+                    for (int ch = 0; ch < D / 64; ++ch) {
+                        const int c0 = h * (D / 2) + 32 * ch;
+                        uint32_t a[32], b[32];
+                        tmem_ld32(tDV + c0, a);
+                        tmem_ld32(tDK + c0, b);
+                        tmem_wait_ld();
+                        reg_fence32(a);
+                        reg_fence32(b);
+                        uint32_t pv[16], pk[16];
 #pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                packed_v[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul,
-                                                          __uint_as_float(a[2 * c + 1]) * mul);
-                            if (krow < nk && in) {
-                                uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    dst[c] = make_uint4(packed_v[4 * c], packed_v[4 * c + 1],
-                                                        packed_v[4 * c + 2], packed_v[4 * c + 3]);
-                            }
+                        for (int c = 0; c < 16; ++c) {
+                            pv[c] = pack_bf16x2(__uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1]));
+                            pk[c] = pack_bf16x2(__uint_as_float(b[2 * c]) * p.scale,
+                                                __uint_as_float(b[2 * c + 1]) * p.scale);
                         }
+                        if (inv) st_row<2>(static_cast<__nv_bfloat16*>(p.dv) + offv + c0, pv);
+                        if (ink) st_row<2>(static_cast<__nv_bfloat16*>(p.dk) + offk + c0, pk);
                     }
                     // the accumulators are in registers: the next tile's first products may
                     // overwrite them (the MMA warp issues those only after this warp's next

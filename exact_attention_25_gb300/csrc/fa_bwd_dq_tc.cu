@@ -570,13 +570,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                         for (int c = 0; c < CH / 2; ++c)
                             packed_v[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * p.scale,
                                                       __uint_as_float(a[2 * c + 1]) * p.scale);
-                        if (qrow < nq && in) {
-                            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
-#pragma unroll
-                            for (int c = 0; c < CH / 8; ++c)
-                                dst[c] = make_uint4(packed_v[4 * c], packed_v[4 * c + 1],
-                                                    packed_v[4 * c + 2], packed_v[4 * c + 3]);
-                        }
+                        if (qrow < nq && in) st_row<CH / 16>(dst_row + c0, packed_v);
                     }
                     // the accumulator is in registers: the next tile's first product may
                     // overwrite it (the MMA warp issues it only after this warp's next arrive)

@@ -170,6 +170,34 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 }
 
 // ---------------------------------------------------------------------------------------
+// Row stores of the epilogues.  A thread holding one output row (a TMEM lane) writes it alone,
+// so each store instruction of a warp touches one line per thread; 32-byte stores halve those
+// accesses against 16-byte ones.  They need a 32-byte aligned address, which the entry points
+// do not guarantee (16 bytes), so the width is chosen per address.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void st_global_32b(void* dst, const uint32_t* v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// 8 * N32 words (32 * N32 bytes) of one row at dst (16-byte aligned)
+template <int N32>
+__device__ __forceinline__ void st_row(void* dst, const uint32_t* v)
+{
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+#pragma unroll
+        for (int h = 0; h < N32; ++h) st_global_32b(d + 32 * h, v + 8 * h);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 2 * N32; ++c)
+            reinterpret_cast<uint4*>(d)[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // TMEM allocation (whole warp executes these).
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
