@@ -89,16 +89,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     const int chunk = rest % p.head_chunks, bkv = rest / p.head_chunks;
     const int b = bkv / L.Hkv, hk = bkv % L.Hkv;
     const int h0 = hk * (L.H / L.Hkv) + chunk * p.G;  // first query head of this CTA
-    const SeqRows sr = seq_rows<true>(L, b);
-    const int nq = min(sr.nq, p.q_box), nk = sr.nk;
-    if (nq == 0) return;  // no queries in this sequence (whole CTA, before any sync)
     const int G = p.G;
-    const int shift = nk - nq;  // bottom-right causal alignment
-    // This CTA's key blocks [jb, jb + J): a balanced share of all blocks of the sequence (the
-    // last query sees every key, so under the causal mask too every block is needed).
-    const int nkb = (nk + C::BN - 1) / C::BN;
-    const int jb = static_cast<int>((static_cast<long long>(nkb) * split) / p.splits);
-    const int J = static_cast<int>((static_cast<long long>(nkb) * (split + 1)) / p.splits) - jb;
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
@@ -130,6 +121,20 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+    // This grid is launched as a programmatic dependent of the work before it on the stream, so
+    // its set-up above (which touches no global memory) overlaps that work's end; every input,
+    // the sequence starts included, is read only after that work has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const SeqRows sr = seq_rows<true>(L, b);
+    const int nq = min(sr.nq, p.q_box), nk = sr.nk;
+    const int shift = nk - nq;  // bottom-right causal alignment
+    // This CTA's key blocks [jb, jb + J): a balanced share of all blocks of the sequence (the
+    // last query sees every key, so under the causal mask too every block is needed).  A
+    // sequence without queries streams nothing and stores nothing.
+    const int nkb = (nk + C::BN - 1) / C::BN;
+    const int jb = static_cast<int>((static_cast<long long>(nkb) * split) / p.splits);
+    const int J = nq == 0 ? 0
+                          : static_cast<int>((static_cast<long long>(nkb) * (split + 1)) / p.splits) - jb;
     // The combine kernel may be scheduled now (programmatic dependent launch); it waits for
     // this whole grid to finish before it reads the partial results.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -447,8 +452,10 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodePara
 {
     constexpr int EPL = D / 32;  // columns per lane
     // launched as a programmatic dependent of the split kernel: wait until that grid has
-    // completed and its partial results are visible
+    // completed and its partial results are visible; the next decode step's split grid may then
+    // be scheduled (it waits for this grid before reading anything)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Layout& L = p.L;
     const size_t rows = static_cast<size_t>(L.Rq) * L.H;
     const int lane = threadIdx.x & 31;
@@ -532,9 +539,22 @@ static cudaError_t launch_decode_impl(const CUtensorMap& tq, const CUtensorMap& 
         attr_set[dev] = true;
     }
     dim3 grid(p.L.B * p.L.Hkv * p.head_chunks * p.splits);
-    fa_decode_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || p.splits == 1) return e;
+    {
+        // programmatic dependent launch: the split grid's set-up overlaps the end of the work
+        // before it on the stream
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, fa_decode_split_kernel<D>, tq, tk, tv, p);
+        if (e != cudaSuccess || p.splits == 1) return e;
+    }
     const long rows = static_cast<long>(p.L.Rq) * p.L.H;
     long blocks = (rows + 7) / 8;  // 8 warps (rows) per CTA
     const long cap = static_cast<long>(num_sms) * 8;

@@ -242,6 +242,10 @@ int fa_bwd_varlen_strided(const void* q, const void* k, const void* v, const voi
  *     key block (num_splits larger than the blocks of a sequence) contribute nothing.
  *   - workspace: caller-owned device buffer of fa_decode_workspace_bytes(total_q, H, d,
  *     num_splits) bytes (0 for num_splits = 1, when workspace may be NULL); overwritten.
+ *   - Its kernels are launched as programmatic dependents (CUDA's programmatic stream
+ *     serialization): their set-up may overlap the end of the work before them on the stream,
+ *     but they read no input and write no output before that work has completed, so stream
+ *     order is kept.
  * bf16 only, forward only.  Errors as fa_fwd_varlen, plus FA_ERR_WORKSPACE. */
 int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int max_seqlen_q,
