@@ -20,7 +20,8 @@ cudaError_t launch_bwd_preprocess(int d, int is_f32, const BwdParams& p, cudaStr
 cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st);
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
 cudaError_t launch_bwd_dkv_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
-cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st,
+                             bool after_dkv);
 cudaError_t launch_decode(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const DecodeParams& p, cudaStream_t st,
                           int num_sms);
@@ -312,7 +313,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
         CUtensorMap maps[4];
         if ((rc = make_maps(maps, q, k, v, dout, p.L, d, fixed_strides(N, d)))) return rc;
         if (stage < 0 || stage == 1) e = fa::launch_bwd_dkv_tc(d, maps, p, st);
-        if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq_tc(d, maps, p, st);
+        if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq_tc(d, maps, p, st, stage < 0);
     }
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return FA_OK;
@@ -560,7 +561,7 @@ extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const voi
     if ((rc = make_maps(maps, q, k, v, dout, p.L, d, st))) return rc;
     cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, cs, di->sms);
     if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, cs);
-    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, cs);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, cs, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return FA_OK;
 }
@@ -710,7 +711,7 @@ int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o,
     if ((rc = make_maps(maps, q, k, v, dout, p.L, d, st))) return rc;
     cudaError_t e = fa::launch_bwd_preprocess(d, 0, p, cs, di->sms);
     if (e == cudaSuccess) e = fa::launch_bwd_dkv_tc(d, maps, p, cs);
-    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, cs);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_tc(d, maps, p, cs, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return FA_OK;
 }

@@ -210,6 +210,10 @@ __global__ void __launch_bounds__(DkvCfg<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+    // launched as a programmatic dependent of the preprocess: read nothing before it is done;
+    // then the dQ grid may launch (it reads only what the preprocess wrote, and the inputs)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // Every role walks the same tile sequence: this CTA's own index (ordinal 0), then the
     // published ones.  Ordinal o >= 1 uses queue slot o & 1 as that slot's use (o - 1) >> 1, so
@@ -625,8 +629,17 @@ static cudaError_t launch_dkv(const CUtensorMap& k, const CUtensorMap& v, const 
         attr_set[dev] = true;
     }
     dim3 grid(p.L.B * p.L.Hkv * ((p.L.Nk + 127) / 128));
-    fa_bwd_dkv_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, q, g, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_bwd_dkv_tc_kernel<D, MODE>, k, v, q, g, p);
 }
 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)

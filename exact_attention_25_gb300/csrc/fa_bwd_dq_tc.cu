@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_g,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const BwdParams p)
+                        const __grid_constant__ CUtensorMap tm_v, const BwdParams p,
+                        int wait_first)
 {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -207,6 +208,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tbase = tmem_slot;
     const Watchdog wd{&abort_flag, p.status, p.wait_limit_ns};
+    // launched as a programmatic dependent: right after the dK/dV grid, whose CTAs let this one
+    // launch only once the preprocess is done, it needs no wait and runs in that grid's tail;
+    // after anything else (the preprocess itself), it waits before reading
+    if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Every role walks the same tile sequence: this CTA's own index (ordinal 0), then the
     // published ones.  Ordinal o >= 1 uses queue slot o & 1 as that slot's use (o - 1) >> 1
@@ -603,11 +608,14 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);
     }
+    // this grid does not complete before the one it follows
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, int MODE>
 static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const CUtensorMap& k,
-                             const CUtensorMap& v, const BwdParams& p, cudaStream_t st)
+                             const CUtensorMap& v, const BwdParams& p, cudaStream_t st,
+                             bool after_dkv)
 {
     using C = DqCfg<D>;
     static bool attr_set[64] = {};
@@ -621,20 +629,31 @@ static cudaError_t launch_dq(const CUtensorMap& q, const CUtensorMap& g, const C
         attr_set[dev] = true;
     }
     dim3 grid(p.L.B * p.L.H * ((p.L.Nq + 127) / 128));
-    fa_bwd_dq_tc_kernel<D, MODE><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(q, g, k, v, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int wait_first = after_dkv ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, fa_bwd_dq_tc_kernel<D, MODE>, q, g, k, v, p, wait_first);
 }
 
 // maps: [0] q, [1] k, [2] v, [3] dout (bf16, 128-row boxes)
-cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st)
+cudaError_t launch_bwd_dq_tc(int d, const CUtensorMap* maps, const BwdParams& p, cudaStream_t st,
+                             bool after_dkv)
 {
     const int mode = layout_mode(p.L.cu_q, p.L.H, p.L.Hkv, p.L.Nq, p.L.Nk);
     auto run = [&](auto dc) {
         constexpr int Dc = decltype(dc)::value;
-        if (mode == kModePacked) return launch_dq<Dc, kModePacked>(maps[0], maps[3], maps[1], maps[2], p, st);
+        if (mode == kModePacked) return launch_dq<Dc, kModePacked>(maps[0], maps[3], maps[1], maps[2], p, st, after_dkv);
         if (mode == kModeFixedGroup)
-            return launch_dq<Dc, kModeFixedGroup>(maps[0], maps[3], maps[1], maps[2], p, st);
-        return launch_dq<Dc, kModeFixed>(maps[0], maps[3], maps[1], maps[2], p, st);
+            return launch_dq<Dc, kModeFixedGroup>(maps[0], maps[3], maps[1], maps[2], p, st, after_dkv);
+        return launch_dq<Dc, kModeFixed>(maps[0], maps[3], maps[1], maps[2], p, st, after_dkv);
     };
     return d == 64 ? run(std::integral_constant<int, 64>{}) : run(std::integral_constant<int, 128>{});
 }

@@ -211,6 +211,9 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
 template <typename T, int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const BwdParams p)
 {
+    // the dK/dV grid after this one (a programmatic dependent) may set up now; it waits for this
+    // grid before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int EPV = 16 / sizeof(T);  // elements per 16-byte vector
     constexpr int TPR = D / EPV;         // threads per row (8, 16 or 32)
     constexpr int RPW = 32 / TPR;        // rows per warp and iteration

@@ -71,7 +71,12 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * same q, k, v, scale, causal); dq, dk, dv: outputs [B,H,N,d]; workspace: caller-owned
  * device buffer of at least fa_bwd_workspace_bytes(B,H,N,d) bytes, overwritten.
  * Gradients are of L = sum(dout o O): dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO with
- * dS = P o (dP - Delta), dP = dO V^T, Delta = rowsum(dO o O).  Deterministic. */
+ * dS = P o (dP - Delta), dP = dO V^T, Delta = rowsum(dO o O).  Deterministic.
+ * The dK/dV and dQ kernels of the tensor-core path are launched as programmatic dependents
+ * (CUDA's programmatic stream serialization): their set-up may overlap the kernel before them,
+ * and dQ may run in the tail of dK/dV (the two read the same inputs and write disjoint
+ * outputs), but nothing reads an input before the work that precedes fa_bwd on the stream has
+ * completed, and fa_bwd's last kernel completes only after all of its kernels have. */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
            float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
