@@ -143,6 +143,34 @@ int check_common(int B, int H, int N, int d, float scale, int causal, int dtype)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The bytes [p, p + n) of one tensor of a call.
+struct Span {
+    const void* p;
+    size_t n;
+};
+
+bool spans_meet(const Span& a, const Span& b)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Whether an output shares a byte with another output, an input or the workspace.  The
+// backward's kernels overlap in time (dQ runs in the tail of dK/dV), so such a call would race.
+bool outputs_overlap(const Span* out, int nout, const Span* in, int nin)
+{
+    for (int i = 0; i < nout; ++i) {
+        for (int j = i + 1; j < nout; ++j)
+            if (spans_meet(out[i], out[j])) return true;
+        for (int j = 0; j < nin; ++j)
+            if (spans_meet(out[i], in[j])) return true;
+    }
+    return false;
+}
+
+const char* const kOverlapMsg =
+    "dq, dk and dv must not overlap one another, an input or the workspace";
+
 // Element strides (row, head index) of the eight tensors of a call, in the order
 // q, k, v, o, dout, dq, dk, dv.
 struct Strides {
@@ -284,6 +312,14 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
     if (!workspace || workspace_bytes < need)
         return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
     if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    {
+        const size_t tb = static_cast<size_t>(B) * H * N * d * (dtype == FA_F32 ? 4 : 2);
+        const size_t sb = static_cast<size_t>(B) * H * N * 4;
+        const Span outs[3] = {{dq, tb}, {dk, tb}, {dv, tb}};
+        const Span ins[7] = {{q, tb}, {k, tb}, {v, tb}, {o, tb}, {dout, tb}, {lse, sb},
+                             {workspace, need}};
+        if (outputs_overlap(outs, 3, ins, 7)) return fail(FA_ERR_INVALID_ARG, kOverlapMsg);
+    }
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -541,6 +577,15 @@ extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const voi
     if (!workspace || workspace_bytes < need)
         return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
     if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    {
+        const size_t tq = static_cast<size_t>(B) * H * Nq * d * 2;
+        const size_t tk = static_cast<size_t>(B) * Hkv * Nk * d * 2;
+        const size_t sb = static_cast<size_t>(B) * H * Nq * 4;
+        const Span outs[3] = {{dq, tq}, {dk, tk}, {dv, tk}};
+        const Span ins[7] = {{q, tq}, {k, tk}, {v, tk}, {o, tq}, {dout, tq}, {lse, sb},
+                             {workspace, need}};
+        if (outputs_overlap(outs, 3, ins, 7)) return fail(FA_ERR_INVALID_ARG, kOverlapMsg);
+    }
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -693,6 +738,15 @@ int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o,
     if (!workspace || workspace_bytes < need)
         return fail(FA_ERR_WORKSPACE, "workspace must hold " + std::to_string(need) + " bytes");
     if (!aligned16(workspace)) return fail(FA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    if (!user_strides) {  // (strided views may interleave in one buffer: not checked)
+        const size_t tq = static_cast<size_t>(total_q) * H * d * 2;
+        const size_t tk = static_cast<size_t>(total_k) * Hkv * d * 2;
+        const size_t sb = static_cast<size_t>(total_q) * H * 4;
+        const Span outs[3] = {{dq, tq}, {dk, tk}, {dv, tk}};
+        const Span ins[7] = {{q, tq}, {k, tk}, {v, tk}, {o, tq}, {dout, tq}, {lse, sb},
+                             {workspace, need}};
+        if (outputs_overlap(outs, 3, ins, 7)) return fail(FA_ERR_INVALID_ARG, kOverlapMsg);
+    }
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -28,6 +28,9 @@
  *     visible keys (the base-2 value the kernels keep is converted, as that post describes).
  *   - Pointers are device pointers, 16-byte aligned.  The caller allocates and owns every
  *     buffer; the library allocates no device memory on these paths.
+ *   - Outputs must not overlap one another, an input or the workspace: the backward's kernels
+ *     run concurrently (dQ in the tail of dK/dV).  The backward entry points with contiguous
+ *     tensors check this on the host (FA_ERR_INVALID_ARG); strided views are not checked.
  *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous on it.
  *   - Return value: FA_OK (0) or a negative FA_ERR_* code.  Argument errors are detected on
  *     the host before anything is launched; nothing throws across the ABI.  Device-side
@@ -219,7 +222,8 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
  * tensor starts at base + i * row + h * head elements; its d elements are contiguous.
  * Each stride must be a positive multiple of 8 elements (16 bytes; else FA_ERR_MISALIGNED),
  * head >= d and row >= head (tensors stored token by token; else FA_ERR_INVALID_ARG).
- * Output views must not overlap.  Everything else as fa_fwd_varlen / fa_bwd_varlen. */
+ * Output views must not overlap one another or an input view (not checked).  Everything
+ * else as fa_fwd_varlen / fa_bwd_varlen. */
 int fa_fwd_varlen_strided(const void* q, const void* k, const void* v, void* o, float* lse,
                           const long long* strides, const int* cu_seqlens_q,
                           const int* cu_seqlens_k, int B, int max_seqlen_q, int max_seqlen_k,

@@ -133,6 +133,45 @@ def test_backward_rejects_bad_arguments(lib):
     assert bwd(lib, ws=MIS) == -3
 
 
+def test_backward_rejects_outputs_that_overlap_another_tensor(lib):
+    # B1 H2 N100 d128 bf16: 51200 bytes per tensor; tensors 1 MiB apart do not touch
+    B, H, N, d = 1, 2, 100, 128
+    need = lib.fa_bwd_workspace_bytes(B, H, N, d)
+    base = 0x1000000
+    names = ["q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "ws"]
+    addr = {n: base + i * (1 << 20) for i, n in enumerate(names)}
+
+    def call(**place):  # place: tensor -> (other tensor, byte offset from its start)
+        a = dict(addr)
+        for n, (other, off) in place.items():
+            a[n] = addr[other] + off
+        a = {n: P(x) for n, x in a.items()}
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"],
+                          a["dv"], B, H, N, d, ctypes.c_float(0.1), 1, 0, a["ws"], need, None)
+
+    # disjoint tensors pass validation (no GPU here: the call then fails with another code)
+    assert call() != -1
+    # dq over the end of q, dk over dq's last 16 bytes, dv inside the workspace, dk on lse
+    assert call(dq=("q", 51200 - 16)) == -1
+    assert "overlap" in lib.fa_last_error().decode()
+    assert call(dk=("dq", 51200 - 16)) == -1
+    assert call(dv=("ws", need - 16)) == -1
+    assert call(dk=("lse", 800 - 16)) == -1
+    # a tensor that ends exactly where the next begins does not overlap it
+    assert call(dq=("q", 51200)) != -1
+    assert call(dk=("lse", 800)) != -1
+
+    def gqa(dq_at):
+        ws = lib.fa_bwd_workspace_bytes(1, 4, 10, 128)
+        return lib.fa_bwd_gqa(P(0x1000000), P(0x2000000), P(0x3000000), P(0x4000000),
+                              P(0x5000000), P(0x6000000), P(dq_at), P(0x8000000), P(0x9000000),
+                              1, 4, 2, 10, 20, 128, ctypes.c_float(0.1), 1, P(0xA000000), ws,
+                              None)
+
+    assert gqa(0x7000000) != -1
+    assert gqa(0x5000000 + 4 * 10 * 128 * 2 - 16) == -1  # dq over the end of dout
+
+
 def test_workspace_size_contract(lib):
     assert lib.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert lib.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
