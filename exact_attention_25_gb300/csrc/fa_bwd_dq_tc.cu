@@ -447,8 +447,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             const int qrow = t.q0 + r;
             if (t.n_it > 0 && qrow < t.sr.nq &&
                 in_extent(row_base + qrow, 1, L.stat_ext, p.status)) {
-                nL2 = -p.lse2[row_base + qrow];
-                nDl = -p.delta[row_base + qrow];
+                // read at L2 (not through this SM's L1): in fa_bwd this grid starts without
+                // waiting, ordered after the preprocess that wrote these only through dK/dV
+                nL2 = -__ldcg(p.lse2 + row_base + qrow);
+                nDl = -__ldcg(p.delta + row_base + qrow);
             }
         };
         int ti = 0, g = 0, at = 0;
