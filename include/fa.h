@@ -267,9 +267,10 @@ int fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* l
  * num_splits = 1 or invalid sizes. */
 size_t fa_decode_workspace_bytes(int total_q, int H, int d, int num_splits);
 
-/* A split count for fa_fwd_decode on the current device: the one in [1, max(1, blocks / 8)]
- * (blocks = ceil(max_seqlen_k / 128)) whose B * Hkv * num_splits CTAs fill the last wave of one
- * CTA per SM best.  Returns it (>= 1) or a negative FA_ERR_* code. */
+/* A split count for fa_fwd_decode on the current device: the largest one whose B * Hkv *
+ * num_splits CTAs fit on the device's SMs at one per SM (at least 1), at most
+ * max(1, blocks / 8) (blocks = ceil(max_seqlen_k / 128)).  Returns it (>= 1) or a negative
+ * FA_ERR_* code. */
 int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k);
 
 /* Backward for callers that cannot allocate device memory.  This entry point has no
