@@ -14,7 +14,8 @@
 namespace fa {
 cudaError_t launch_fwd_tc(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const FwdParams& p, cudaStream_t st);
-cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t st);
+cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t st,
+                            int num_sms);
 cudaError_t launch_bwd_preprocess(int d, int is_f32, const BwdParams& p, cudaStream_t st,
                                   int num_sms);
 cudaError_t launch_bwd_simt(int d, int is_f32, const BwdParams& p, cudaStream_t st);
@@ -281,7 +282,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.L.order_group = order_group(N, d, causal);
     cudaError_t e;
     if (dtype == FA_F32 || impl == 1) {
-        e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st);
+        e = fa::launch_fwd_simt(d, dtype == FA_F32, p, st, di->sms);
     } else {
         CUtensorMap maps[4];
         if ((rc = make_maps(maps, q, k, v, nullptr, p.L, d, fixed_strides(N, d)))) return rc;

@@ -66,18 +66,18 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p)
 }
 
 // Stage rows [row0, row0+ROWS) of one head into shared memory as fp32 with row stride ld;
-// rows at or beyond N are zero.  Every thread of the 128-thread CTA first loads all of its
+// rows at or beyond N are zero.  Every thread of the NT-thread CTA first loads all of its
 // 4-element vectors into registers and only then stores them, so the loads of a whole tile
 // are in flight together.
-template <typename T, int D, int ROWS>
+template <typename T, int D, int ROWS, int NT = 128>
 __device__ __forceinline__ void stage_rows(float* dst, int ld, const T* head, int row0, int N)
 {
     constexpr int NV = ROWS * D / 4;          // 4-element vectors in the tile
-    constexpr int PER = (NV + 127) / 128;     // per thread
+    constexpr int PER = (NV + NT - 1) / NT;   // per thread
     float4 vals[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-        const int e = (static_cast<int>(threadIdx.x) + i * 128) * 4;
+        const int e = (static_cast<int>(threadIdx.x) + i * NT) * 4;
         const int r = e / D, c = e % D;
         const int g = row0 + r;
         vals[i] = (e < ROWS * D && g < N) ? load4(head + static_cast<size_t>(g) * D + c)
@@ -85,7 +85,43 @@ __device__ __forceinline__ void stage_rows(float* dst, int ld, const T* head, in
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-        const int e = (static_cast<int>(threadIdx.x) + i * 128) * 4;
+        const int e = (static_cast<int>(threadIdx.x) + i * NT) * 4;
+        if (e < ROWS * D) {
+            float* d = dst + (e / D) * ld + (e % D);
+            d[0] = vals[i].x;
+            d[1] = vals[i].y;
+            d[2] = vals[i].z;
+            d[3] = vals[i].w;
+        }
+    }
+}
+
+// The two halves of stage_rows, for a tile whose loads fly while the previous one is used:
+// rows [row0, row0+ROWS) of one head into this thread's registers (zero beyond N) ...
+template <typename T, int D, int ROWS, int NT>
+__device__ __forceinline__ void load_rows(float4 (&vals)[(ROWS * D / 4 + NT - 1) / NT],
+                                          const T* head, int row0, int N)
+{
+    constexpr int PER = (ROWS * D / 4 + NT - 1) / NT;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = (static_cast<int>(threadIdx.x) + i * NT) * 4;
+        const int r = e / D, c = e % D;
+        const int g = row0 + r;
+        vals[i] = (e < ROWS * D && g < N) ? load4(head + static_cast<size_t>(g) * D + c)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// ... and from the registers into shared memory with row stride ld.
+template <int D, int ROWS, int NT>
+__device__ __forceinline__ void store_rows(float* dst, int ld,
+                                           const float4 (&vals)[(ROWS * D / 4 + NT - 1) / NT])
+{
+    constexpr int PER = (ROWS * D / 4 + NT - 1) / NT;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = (static_cast<int>(threadIdx.x) + i * NT) * 4;
         if (e < ROWS * D) {
             float* d = dst + (e / D) * ld + (e % D);
             d[0] = vals[i].x;
@@ -112,11 +148,15 @@ __device__ __forceinline__ float dot_smem(const float* a, const float* b)
 }
 
 // ----------------------------------------------------------------------------------------
-// Forward: O and LSE for 16 query rows per CTA.
+// Forward: O and LSE for 16 query rows per CTA, RPW rows per warp (4: 128 threads, each V
+// element read from shared memory serves four rows; 1: 512 threads, for grids too small to
+// fill the GPU, where each warp's chain of dependent steps per key tile is the time).  Every
+// row is computed the same way either way.
 // ----------------------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
+template <typename T, int D, int RPW>
+__global__ void __launch_bounds__(kSimtRows / RPW * 32) fa_fwd_simt_kernel(const FwdParams p)
 {
+    constexpr int NT = kSimtRows / RPW * 32;  // threads
     constexpr int DL = D / 32;  // output columns per lane
     extern __shared__ float sm[];
     float* Qs = sm;                          // [16][D]
@@ -129,12 +169,12 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
     const T* q = static_cast<const T*>(p.q) + hoff;
     const T* k = static_cast<const T*>(p.k) + hoff;
     const T* v = static_cast<const T*>(p.v) + hoff;
-    stage_rows<T, D, kSimtRows>(Qs, D, q, row_base, N);
+    stage_rows<T, D, kSimtRows, NT>(Qs, D, q, row_base, N);
 
     const float c2 = p.scale_log2;
-    float m[kSimtRowsPerWarp], l[kSimtRowsPerWarp], o[kSimtRowsPerWarp][DL];
+    float m[RPW], l[RPW], o[RPW][DL];
 #pragma unroll
-    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+    for (int rr = 0; rr < RPW; ++rr) {
         m[rr] = -INFINITY;
         l[rr] = 0.0f;
 #pragma unroll
@@ -142,17 +182,36 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
     }
     const int last_row = min(N - 1, row_base + kSimtRows - 1);
     const int n_tiles = p.causal ? (last_row / kSimtTile + 1) : (N + kSimtTile - 1) / kSimtTile;
+    // With one row per warp the K and V tiles go through registers one tile ahead (one or two
+    // vectors a thread), so the loads of tile kt + 1 are in flight while tile kt is computed;
+    // with four rows per warp those registers would cost occupancy.
+    constexpr bool kAhead = RPW == 1;
+    constexpr int PER = (kSimtTile * D / 4 + NT - 1) / NT;
+    float4 kreg[PER], vreg[PER];
+    if constexpr (kAhead) {
+        load_rows<T, D, kSimtTile, NT>(kreg, k, 0, N);
+        load_rows<T, D, kSimtTile, NT>(vreg, v, 0, N);
+    }
     for (int kt = 0; kt < n_tiles; ++kt) {
         __syncthreads();
-        stage_rows<T, D, kSimtTile>(Ks, D + 1, k, kt * kSimtTile, N);
-        stage_rows<T, D, kSimtTile>(Vs, D, v, kt * kSimtTile, N);
+        if constexpr (kAhead) {
+            store_rows<D, kSimtTile, NT>(Ks, D + 1, kreg);
+            store_rows<D, kSimtTile, NT>(Vs, D, vreg);
+        } else {
+            stage_rows<T, D, kSimtTile, NT>(Ks, D + 1, k, kt * kSimtTile, N);
+            stage_rows<T, D, kSimtTile, NT>(Vs, D, v, kt * kSimtTile, N);
+        }
         __syncthreads();
+        if (kAhead && kt + 1 < n_tiles) {
+            load_rows<T, D, kSimtTile, NT>(kreg, k, (kt + 1) * kSimtTile, N);
+            load_rows<T, D, kSimtTile, NT>(vreg, v, (kt + 1) * kSimtTile, N);
+        }
         const int key = kt * kSimtTile + lane;
         // scores of this warp's rows against the tile's keys (lane = key) ...
-        float pr[kSimtRowsPerWarp], alpha[kSimtRowsPerWarp];
+        float pr[RPW], alpha[RPW];
 #pragma unroll
-        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
-            const int lr = warp * kSimtRowsPerWarp + rr;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int lr = warp * RPW + rr;
             const int row = row_base + lr;
             const float s = dot_smem<D>(Qs + lr * D, Ks + lane * (D + 1));
             const bool valid = key < N && (!p.causal || key <= row);
@@ -161,7 +220,7 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
         // ... the online-softmax update of each row (rows with nothing visible yet keep their
         // state: alpha = 1, weights 0) ...
 #pragma unroll
-        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+        for (int rr = 0; rr < RPW; ++rr) {
             const float mnew = fmaxf(m[rr], warp_max(pr[rr]));
             if (mnew == -INFINITY) {
                 alpha[rr] = 1.0f;
@@ -175,7 +234,7 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
         }
         // ... and O += P V for all rows at once (one V read per key serves every row)
 #pragma unroll
-        for (int rr = 0; rr < kSimtRowsPerWarp; ++rr)
+        for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
             for (int t = 0; t < DL; ++t) o[rr][t] *= alpha[rr];
 #pragma unroll 4
@@ -184,7 +243,7 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
 #pragma unroll
             for (int t = 0; t < DL; ++t) vc[t] = Vs[c * D + lane + 32 * t];
 #pragma unroll
-            for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
+            for (int rr = 0; rr < RPW; ++rr) {
                 const float pc = __shfl_sync(0xffffffffu, pr[rr], c);
 #pragma unroll
                 for (int t = 0; t < DL; ++t) o[rr][t] = fmaf(pc, vc[t], o[rr][t]);
@@ -193,8 +252,8 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_kernel(const FwdParams p)
     }
     T* out = static_cast<T*>(p.o) + hoff;
 #pragma unroll
-    for (int rr = 0; rr < kSimtRowsPerWarp; ++rr) {
-        const int row = row_base + warp * kSimtRowsPerWarp + rr;
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int row = row_base + warp * RPW + rr;
         if (row >= N) continue;
         const float inv = 1.0f / l[rr];
 #pragma unroll
@@ -418,21 +477,31 @@ static cudaError_t set_smem(K kernel, int bytes)
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <typename T, int D>
-static cudaError_t fwd_simt(const FwdParams& p, cudaStream_t st)
+template <typename T, int D, int RPW>
+static cudaError_t fwd_simt_rpw(const FwdParams& p, cudaStream_t st, dim3 grid)
 {
     const int smem = (kSimtRows * D + kSimtTile * (D + 1) + kSimtTile * D) * 4;
-    cudaError_t e = set_smem(fa_fwd_simt_kernel<T, D>, smem);
+    cudaError_t e = set_smem(fa_fwd_simt_kernel<T, D, RPW>, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kSimtRows - 1) / kSimtRows, p.BH);
-    fa_fwd_simt_kernel<T, D><<<grid, 128, smem, st>>>(p);
+    fa_fwd_simt_kernel<T, D, RPW><<<grid, kSimtRows / RPW * 32, smem, st>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t st)
+template <typename T, int D>
+static cudaError_t fwd_simt(const FwdParams& p, cudaStream_t st, int num_sms)
 {
-    if (is_f32) return d == 64 ? fwd_simt<float, 64>(p, st) : fwd_simt<float, 128>(p, st);
-    return d == 64 ? fwd_simt<__nv_bfloat16, 64>(p, st) : fwd_simt<__nv_bfloat16, 128>(p, st);
+    dim3 grid((p.N + kSimtRows - 1) / kSimtRows, p.BH);
+    // fewer CTAs than SMs: one row per warp shortens each CTA's dependent chain four times
+    if (static_cast<long long>(grid.x) * grid.y < num_sms) return fwd_simt_rpw<T, D, 1>(p, st, grid);
+    return fwd_simt_rpw<T, D, 4>(p, st, grid);
+}
+
+cudaError_t launch_fwd_simt(int d, int is_f32, const FwdParams& p, cudaStream_t st, int num_sms)
+{
+    if (is_f32)
+        return d == 64 ? fwd_simt<float, 64>(p, st, num_sms) : fwd_simt<float, 128>(p, st, num_sms);
+    return d == 64 ? fwd_simt<__nv_bfloat16, 64>(p, st, num_sms)
+                   : fwd_simt<__nv_bfloat16, 128>(p, st, num_sms);
 }
 
 template <typename T, int D>
