@@ -29,7 +29,7 @@ EXPORTS = (
     "fa_bwd_varlen", "fa_fwd_decode", "fa_decode_workspace_bytes", "fa_decode_num_splits",
     "fa_fwd_varlen_strided", "fa_bwd_varlen_strided", "fa_fwd_gqa", "fa_bwd_gqa",
     "fa_checked_build", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_fwd_fp8_varlen",
-    "fa_fwd_fp8_varlen_workspace_bytes", "fa_tile_order", "fa_order_group",
+    "fa_fwd_fp8_varlen_workspace_bytes", "fa_tile_order", "fa_order_group", "fa_decode_splits_for",
 )
 
 _lock = threading.Lock()
@@ -105,6 +105,8 @@ def load(path: str | None = None):
         lib.fa_tile_order.restype = ctypes.c_int
         lib.fa_order_group.argtypes = [i, i, i]
         lib.fa_order_group.restype = ctypes.c_int
+        lib.fa_decode_splits_for.argtypes = [i, i, i, i]
+        lib.fa_decode_splits_for.restype = ctypes.c_int
         lib.fa_checked_build.argtypes = []
         lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_fwd_fp8_workspace_bytes.restype = sz

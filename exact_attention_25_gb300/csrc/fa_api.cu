@@ -843,12 +843,10 @@ size_t decode_part_o_bytes(int total_q, int H, int d, int splits)
 
 }  // namespace
 
-extern "C" int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k)
+extern "C" int fa_decode_splits_for(int B, int Hkv, int max_seqlen_k, int num_sms)
 {
-    if (B < 1 || Hkv < 1 || max_seqlen_k < 1) return fail(FA_ERR_INVALID_ARG, "B, Hkv and max_seqlen_k must be >= 1");
-    DeviceInfo* di = nullptr;
-    int rc = device_info(&di);
-    if (rc) return rc;
+    if (B < 1 || Hkv < 1 || max_seqlen_k < 1 || num_sms < 1)
+        return fail(FA_ERR_INVALID_ARG, "B, Hkv, max_seqlen_k and num_sms must be >= 1");
     // One wave: the largest split count whose CTAs (B * Hkv * splits, one per SM) all run at
     // once, keeping at least 8 key blocks per split.  Once enough CTAs stream (each keeps about
     // 200 KB of loads in flight), the HBM time is the same for any split count; a second wave
@@ -856,10 +854,19 @@ extern "C" int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k)
     // combine a partial result.  Measured on GB300 (B = 8, Hkv = 8, d = 128): 2 splits over
     // 8 K, 16 K and 32 K keys ran 10-18 % faster than the 7-19 that filled whole waves.
     const long long units = static_cast<long long>(B) * Hkv;
-    const int nblk = (max_seqlen_k + 127) / 128;
+    const int nblk = static_cast<int>((static_cast<long long>(max_seqlen_k) + 127) / 128);
     const int smax = std::max(1, std::min(kDecodeMaxSplits, nblk / 8));
-    const long long fit = std::max(1LL, static_cast<long long>(di->sms) / units);
+    const long long fit = std::max(1LL, static_cast<long long>(num_sms) / units);
     return static_cast<int>(std::min<long long>(smax, fit));
+}
+
+extern "C" int fa_decode_num_splits(int B, int Hkv, int max_seqlen_k)
+{
+    if (B < 1 || Hkv < 1 || max_seqlen_k < 1) return fail(FA_ERR_INVALID_ARG, "B, Hkv and max_seqlen_k must be >= 1");
+    DeviceInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    return fa_decode_splits_for(B, Hkv, max_seqlen_k, di->sms);
 }
 
 extern "C" size_t fa_decode_workspace_bytes(int total_q, int H, int d, int num_splits)

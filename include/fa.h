@@ -353,6 +353,12 @@ int fa_tile_order(int id, int heads, int nblk, int gsize, int* head, int* rank);
  * Host-only. */
 int fa_order_group(int N, int d, int causal);
 
+/* The split count fa_decode_num_splits gives on a device with num_sms SMs (host copy, for tests
+ * and schedulers): min(max(1, blocks / 8), max(1, num_sms / (B * Hkv))), blocks =
+ * ceil(max_seqlen_k / 128), capped at 256.  Returns it, or FA_ERR_INVALID_ARG for a size or
+ * num_sms below 1.  Host-only. */
+int fa_decode_splits_for(int B, int Hkv, int max_seqlen_k, int num_sms);
+
 /* Library version string. */
 const char* fa_version(void);
 

@@ -332,6 +332,25 @@ def test_grouped_fixed_length_rejects_bad_arguments(lib):
     assert bcall(nbytes=16) == -4
 
 
+def test_decode_split_rule_takes_one_wave(lib):
+    """The split count fa_decode_num_splits suggests (its host copy): the largest whose
+    B * Hkv * splits CTAs all fit on the SMs at once, at least 8 key blocks of 128 per range."""
+    f = lib.fa_decode_splits_for
+    assert f(8, 8, 8192, 152) == 2      # 64 groups: 2 x 64 CTAs fit on 152 SMs, 3 x 64 do not
+    assert f(8, 8, 32768, 152) == 2
+    assert f(4, 8, 16384, 152) == 4
+    assert f(2, 8, 32768, 152) == 9
+    assert f(1, 8, 131072, 152) == 19
+    assert f(16, 8, 8192, 152) == 1
+    assert f(64, 8, 4096, 152) == 1     # more groups than SMs
+    assert f(8, 8, 2048, 152) == 2      # 16 blocks: at most two ranges of 8
+    assert f(1, 1, 1000, 152) == 1      # 8 blocks: one range
+    assert f(1, 1, 10 ** 9, 152) == 152  # bounded by the SMs ...
+    assert f(1, 1, 10 ** 9, 1000) == 256  # ... and by the 256-range limit
+    for bad in [(0, 8, 100, 152), (8, 0, 100, 152), (8, 8, 0, 152), (8, 8, 100, 0)]:
+        assert f(*bad) == -1
+
+
 def _order(lib, id_, heads, nblk, gsize):
     h, r = ctypes.c_int(), ctypes.c_int()
     assert lib.fa_tile_order(id_, heads, nblk, gsize, ctypes.byref(h), ctypes.byref(r)) == 0

@@ -91,7 +91,8 @@ def test_decode_step_at_serving_size_sampled_groups():
     lens_q, H, Hkv, d = [1] * len(lens_k), 32, 8, 128
     x = random_varlen(lens_q, lens_k, H, Hkv, d, seed=23, with_do=False)
     splits = fa.fa_decode_num_splits(len(lens_k), Hkv, max(lens_k))
-    assert splits >= 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert splits == fa.load().fa_decode_splits_for(len(lens_k), Hkv, max(lens_k), sms) >= 1
     got = run_decode(x, True, splits, d ** -0.5)
     G = H // Hkv
     groups = [1, 6]
