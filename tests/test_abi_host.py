@@ -11,6 +11,18 @@ import pytest
 
 from exact_attention_25_gb300 import _lib, build, perfmodel
 
+
+def _no_device():
+    import torch
+
+    return not torch.cuda.is_available()
+
+
+# A call with dummy pointers that passes every host check goes on to launch.  Such calls are made
+# only where no CUDA device exists (the call then fails at the device query); with a device they
+# would launch kernels on addresses that are not allocations.
+LAUNCH_SAFE = _no_device()
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
@@ -150,7 +162,8 @@ def test_backward_rejects_outputs_that_overlap_another_tensor(lib):
                           a["dv"], B, H, N, d, ctypes.c_float(0.1), 1, 0, a["ws"], need, None)
 
     # disjoint tensors pass validation (no GPU here: the call then fails with another code)
-    assert call() != -1
+    if LAUNCH_SAFE:  # passes the host checks
+        assert call() != -1
     # dq over the end of q, dk over dq's last 16 bytes, dv inside the workspace, dk on lse
     assert call(dq=("q", 51200 - 16)) == -1
     assert "overlap" in lib.fa_last_error().decode()
@@ -158,8 +171,10 @@ def test_backward_rejects_outputs_that_overlap_another_tensor(lib):
     assert call(dv=("ws", need - 16)) == -1
     assert call(dk=("lse", 800 - 16)) == -1
     # a tensor that ends exactly where the next begins does not overlap it
-    assert call(dq=("q", 51200)) != -1
-    assert call(dk=("lse", 800)) != -1
+    if LAUNCH_SAFE:  # passes the host checks
+        assert call(dq=("q", 51200)) != -1
+    if LAUNCH_SAFE:  # passes the host checks
+        assert call(dk=("lse", 800)) != -1
 
     def gqa(dq_at):
         ws = lib.fa_bwd_workspace_bytes(1, 4, 10, 128)
@@ -168,7 +183,8 @@ def test_backward_rejects_outputs_that_overlap_another_tensor(lib):
                               1, 4, 2, 10, 20, 128, ctypes.c_float(0.1), 1, P(0xA000000), ws,
                               None)
 
-    assert gqa(0x7000000) != -1
+    if LAUNCH_SAFE:  # passes the host checks
+        assert gqa(0x7000000) != -1
     assert gqa(0x5000000 + 4 * 10 * 128 * 2 - 16) == -1  # dq over the end of dout
 
 
@@ -271,6 +287,38 @@ def test_varlen_backward_rejects_bad_arguments(lib):
     assert call(nbytes=need - 1) == -4
     assert call(ws=MIS) == -3
     assert call(H=5) == -1
+
+
+def test_varlen_backward_rejects_overlapping_outputs_unless_strided(lib):
+    # 20 query and 20 key tokens, H4 over Hkv2, d128 bf16: q-side tensors 20480 bytes,
+    # k-side 10240, lse 320; tensors 1 MiB apart do not touch
+    need = lib.fa_bwd_varlen_workspace_bytes(20, 4, 128)
+    names = ["q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws"]
+    addr = {n: 0x1000000 + i * (1 << 20) for i, n in enumerate(names)}
+
+    def call(strides=None, **place):
+        a = dict(addr)
+        for n, (other, off) in place.items():
+            a[n] = addr[other] + off
+        a = {n: P(x) for n, x in a.items()}
+        args = [a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"]]
+        tail = [A, A, 2, 10, 10, 20, 20, 4, 2, 128, ctypes.c_float(0.1), 1, a["ws"], need, None]
+        if strides is None:
+            return lib.fa_bwd_varlen(*args, *tail)
+        return lib.fa_bwd_varlen_strided(*args, strides, *tail)
+
+    if LAUNCH_SAFE:  # passes the host checks
+        assert call() != -1
+    assert call(dq=("do", 20480 - 16)) == -1
+    assert "overlap" in lib.fa_last_error().decode()
+    assert call(dv=("dk", 10240 - 16)) == -1
+    assert call(dk=("ws", 0)) == -1
+    if LAUNCH_SAFE:  # passes the host checks
+        assert call(dq=("do", 20480)) != -1
+    # strided views may interleave in one buffer: not checked
+    arr = (ctypes.c_longlong * 16)(*([512, 128] * 4 + [512, 128] + [512, 128] + [256, 128] * 2))
+    if LAUNCH_SAFE:  # passes the host checks
+        assert call(strides=arr, dq=("do", 20480 - 16)) != -1
 
 
 def test_decode_rejects_bad_arguments(lib):
